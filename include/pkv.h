@@ -1,0 +1,230 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention over a paged KV cache, hand-written
+ * CUDA for one GB300 (sm_103a).
+ *
+ * The operations follow four serving engines' descriptions of the same hot
+ * path (InferX; infer-lab; llm-infer; RustInfer):
+ *   - a paged KV cache: fixed-size blocks and per-sequence block tables
+ *     (infer-lab, "Technique" table, PagedAttention; llm-infer, "What It
+ *     Does"; InferX, "Status" and roadmap M3);
+ *   - the KV write of each new token fused with RoPE (llm-infer, "What It
+ *     Does": graphs capture the KV writes, RMSNorm and RoPE fused);
+ *   - GQA decode attention with an online softmax, split across KV chunks
+ *     and merged (llm-infer, "References": FlashAttention-2 work
+ *     partitioning; infer-lab, "Strategy" table: tiled/online softmax);
+ *   - causal, ragged, chunked prefill over cached prefixes (infer-lab,
+ *     "Technique" table: chunked prefill; llm-infer, "What It Does": ragged
+ *     batched prefill);
+ *   - an FP8 e4m3 KV cache with per-head scales (InferX, "The kernels
+ *     underneath", M8) and a 128-token sliding window (RustInfer, "Status").
+ *
+ * Conventions for every entry point:
+ *   - Every pointer is a DEVICE pointer unless its comment says "host".
+ *   - The caller owns every buffer (caches, tables, q/out, cos/sin table,
+ *     workspace).  The library allocates no device memory on any call; it
+ *     caches CUDA tensor-map descriptors, which are host data.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream); no call synchronises the device.
+ *   - Arguments are validated on the host before any launch; a failed check
+ *     returns its status and touches no device memory.  pkv_last_error()
+ *     then describes the failure (thread-local, valid until the next call).
+ *   - Device-side checks (a block id outside [0, num_blocks), a position
+ *     outside the table, a wait that ran out) never trap: the offending
+ *     access is skipped or clamped and a bit is set in the device error word
+ *     read by pkv_device_errors().
+ *
+ * Cache layout (one pool for K, one for V): [num_blocks][Hkv][block_size][D]
+ * of bf16 or e4m3 bytes.  Token t of sequence s lives in block
+ * block_tables[s * max_blocks_per_seq + t / block_size], row
+ * t % block_size.  Query head h reads KV head h / (Hq / Hkv).
+ * q and out are [tokens][Hq][D] bf16; lse is [tokens][Hq] fp32, natural log.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,  /* null pointer, inconsistent sizes, bad lengths */
+    PKV_ERR_UNSUPPORTED = 2,  /* head_dim, block_size, dtype or group size not built */
+    PKV_ERR_WORKSPACE = 3,    /* workspace null, too small or misaligned */
+    PKV_ERR_CUDA = 4          /* a CUDA runtime/driver call or launch failed */
+} pkv_status;
+
+typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
+
+/* Device error word bits (pkv_device_errors). */
+#define PKV_DEVERR_BLOCK_ID 0x1u  /* a block id outside [0, num_blocks): access skipped */
+#define PKV_DEVERR_POSITION 0x2u  /* a position/sequence index outside its table: skipped */
+#define PKV_DEVERR_TIMEOUT 0x4u   /* a bounded wait gave up: that output is invalid */
+#define PKV_DEVERR_LENGTH 0x8u    /* a length beyond the table capacity: clamped */
+
+/* Shape of one paged KV pool pair (K and V share it).
+ * Supported: head_dim 64 or 128; block_size 16; num_q_heads a multiple of
+ * num_kv_heads with group size num_q_heads / num_kv_heads <= 16. */
+typedef struct {
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t kv_dtype;            /* pkv_kv_dtype */
+    int32_t max_blocks_per_seq;  /* row length of block_tables (int32 [num_seqs][this]) */
+    int64_t num_blocks;          /* blocks in each pool */
+} pkv_cache_desc;
+
+/* Bytes of one pool (K or V): num_blocks * Hkv * block_size * head_dim * elem.
+ * Host only; 0 for an invalid desc. */
+uint64_t pkv_cache_bytes(const pkv_cache_desc *desc);
+
+/* ---- a1: fused KV append + RoPE (llm-infer, "What It Does") ------------
+ * For each new token i (0 <= i < num_tokens): s = token_to_seq[i],
+ * p = positions[i]; slot = block block_tables[s][p / block_size], row
+ * p % block_size.  For every KV head h:
+ *   K row = RoPE(k_new[i][h], p) rounded to bf16 (RNE), or for e4m3
+ *           RNE-satfinite(RoPE(k_new[i][h], p) / k_scale[h]);
+ *   V row = v_new[i][h] copied, or RNE-satfinite(v_new[i][h] / v_scale[h]).
+ * q_inout[i][h'] is rotated in place for every query head (skipped if NULL).
+ * RoPE is the half-split form over the whole head: with a = x[j],
+ * b = x[j + D/2], c/s = rope_cos_sin[p][j][0/1]:
+ *   x'[j] = a*c - b*s,  x'[j + D/2] = b*c + a*s   (fp32, each op rounded).
+ * rope_cos_sin == NULL: no rotation (plain append).
+ *   k_cache, v_cache : pools, written.   k_scale, v_scale: fp32 [Hkv], e4m3 only.
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq].
+ *   token_to_seq, positions : int32 [num_tokens].
+ *   k_new, v_new     : bf16 [num_tokens][Hkv][D].  q_inout: bf16 [num_tokens][Hq][D].
+ *   rope_cos_sin     : fp32 [rope_max_pos][D/2][2] (pkv_rope_cos_sin_table).
+ * Two tokens must not target the same slot in one call. */
+pkv_status pkv_append_rope(const pkv_cache_desc *desc, void *k_cache, void *v_cache,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *block_tables, int32_t num_seqs,
+                           const int32_t *token_to_seq, const int32_t *positions,
+                           int32_t num_tokens, const void *k_new, const void *v_new,
+                           void *q_inout, const float *rope_cos_sin, int32_t rope_max_pos,
+                           pkv_stream_t stream);
+
+/* Host: fill host_out (fp32 [max_pos][rotary_dim/2][2]) with (cos, sin) of
+ * p * theta^(-2j/rotary_dim), computed in double and rounded once to fp32. */
+pkv_status pkv_rope_cos_sin_table(float theta, int32_t rotary_dim, int32_t max_pos,
+                                  float *host_out);
+
+/* ---- a2: block-table gather (infer-lab, "Technique" table) -------------
+ * out[cu_context_lens[s] + t][h][:] = cache[bt[s][t / bs]][h][t % bs][:] for
+ * t < context_lens[s]: a byte-exact copy of one pool into contiguous
+ * [total_tokens][Hkv][D] (bf16 or e4m3 bytes).  cu_context_lens: int32
+ * [num_seqs + 1], prefix sums of context_lens; total_tokens its last entry
+ * (host value).  The decode and prefill kernels do this gather themselves,
+ * block by block, through TMA; this export exists so the addressing can be
+ * checked bit for bit. */
+pkv_status pkv_gather_kv(const pkv_cache_desc *desc, const void *cache,
+                         const int32_t *block_tables, const int32_t *context_lens,
+                         const int32_t *cu_context_lens, int32_t num_seqs,
+                         int64_t total_tokens, void *out, pkv_stream_t stream);
+
+/* ---- a3-a7: split-KV GQA decode (FlashAttention-2 partitioning) ---------
+ * One query token per sequence, at position context_lens[s] - 1 (the new
+ * token, already appended).  For query head h, KV head h / G:
+ *   o = softmax(sm_scale * q k^T) v over the visible keys, lse = ln sum exp.
+ * Visible keys: t < context_lens[s]; with window > 0 also
+ * t > context_lens[s] - 1 - window.  e4m3 pools read k = code * k_scale[h],
+ * v = code * v_scale[h].
+ * The KV range of each (sequence, KV head) is cut into chunks of whole
+ * blocks (pkv_decode_plan); every chunk runs as one CTA whose warps share
+ * the G query heads of the group; partial (o, lse) states go to the
+ * workspace and the last chunk to finish merges them in the same launch.
+ *   q        : bf16 [num_seqs][Hq][D].      out: bf16 [num_seqs][Hq][D].
+ *   lse_out  : fp32 [num_seqs][Hq], nullable.
+ *   context_lens : int32 [num_seqs], each in [1, max_blocks_per_seq*bs].
+ *   max_context_len : host, >= every context_lens[s]; sizes the plan.
+ *   window   : <= 0 for full attention.
+ *   chunk_blocks : blocks per chunk; 0 lets the planner choose
+ *              (pkv_decode_plan), else 1..128.
+ *   workspace: >= pkv_decode_workspace_size(...) bytes, 256-byte aligned,
+ *              zero-filled before its first use; every call leaves it
+ *              zeroed again.  Calls that share a workspace must not overlap
+ *              on the GPU. */
+pkv_status pkv_decode_attention(const pkv_cache_desc *desc, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_tables, const int32_t *context_lens,
+                                int32_t num_seqs, int32_t max_context_len, float sm_scale,
+                                int32_t window, int32_t chunk_blocks, void *out, float *lse_out,
+                                void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Host: workspace bytes pkv_decode_attention needs for this shape and
+ * chunk_blocks (0 = planned; planning uses the current device's SM count).
+ * 0 when no workspace is needed (every sequence fits one chunk) or the
+ * arguments are invalid. */
+size_t pkv_decode_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
+                                 int32_t max_context_len, int32_t window, int32_t chunk_blocks);
+
+/* ---- a4: the split planner (InferX, "Measured": a kernel launched with too
+ * few CTAs cost 3.9x).  Host only.  Chooses the chunk length in whole blocks
+ * so that the (sequence, KV head, chunk) CTAs fill the GPU several times
+ * over; each sequence then has ceil(visible blocks / chunk) chunks.
+ *   num_sms: SM count to plan for (<= 0: the current device's). */
+pkv_status pkv_decode_plan(const pkv_cache_desc *desc, int32_t num_seqs,
+                           int32_t max_context_len, int32_t window, int32_t num_sms,
+                           int32_t *chunk_blocks_out, int32_t *max_splits_out);
+
+/* ---- a8: ragged causal chunked prefill (infer-lab, chunked prefill) -----
+ * Sequence s owns query tokens [qo_indptr[s], qo_indptr[s+1]) of q and
+ * kv_lens[s] cached keys, its own chunk's K/V already appended; query i sits
+ * at position kv_lens[s] - q_len + (i - qo_indptr[s]) and, with causal != 0,
+ * sees keys t <= that position (window > 0: also t > position - window).
+ *   q, out   : bf16 [total_q_tokens][Hq][D].  lse_out: fp32, nullable.
+ *   qo_indptr: int32 [num_seqs + 1] (device).  kv_lens: int32 [num_seqs].
+ *   qo_indptr_host, kv_lens_host: host copies (nullable, used for planning
+ *              and validation only; they must match the device arrays).
+ *   workspace: >= pkv_prefill_workspace_size(...) bytes (0 today; may be NULL).
+ * bf16 pools only. */
+pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *q,
+                                        const int32_t *qo_indptr, const void *k_cache,
+                                        const void *v_cache, const float *k_scale,
+                                        const float *v_scale, const int32_t *block_tables,
+                                        const int32_t *kv_lens, int32_t num_seqs,
+                                        int32_t total_q_tokens, const int32_t *qo_indptr_host,
+                                        const int32_t *kv_lens_host, float sm_scale,
+                                        int32_t causal, int32_t window, void *out,
+                                        float *lse_out, void *workspace,
+                                        size_t workspace_bytes, pkv_stream_t stream);
+
+/* Host: workspace bytes pkv_prefill_attention_ragged needs. */
+size_t pkv_prefill_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
+                                  int32_t total_q_tokens);
+
+/* ---- a5: merge of partial attention states (FlashAttention-2) -----------
+ * For P parts over disjoint key sets: M = max_i lse_i, w_i = exp(lse_i - M),
+ *   out = sum_i w_i o_i / sum_i w_i,  lse_out = M + ln sum_i w_i.
+ * Parts with lse = -inf are empty (weight 0, their o never read); if all are
+ * empty out = 0, lse_out = -inf.
+ *   o_parts : fp32 [num_parts][num_rows][num_heads][head_dim].
+ *   lse_parts: fp32 [num_parts][num_rows][num_heads].
+ *   out     : bf16 [num_rows][num_heads][head_dim].  lse_out: nullable. */
+pkv_status pkv_merge_states(const float *o_parts, const float *lse_parts, int32_t num_parts,
+                            int32_t num_rows, int32_t num_heads, int32_t head_dim, void *out,
+                            float *lse_out, pkv_stream_t stream);
+
+/* ---- diagnostics --------------------------------------------------------- */
+
+/* Message for the last non-OK status on this thread ("" if none). */
+const char *pkv_last_error(void);
+
+/* Host, synchronous: copy the current device's error word (PKV_DEVERR_*
+ * bits set by kernels since the last reset) to *flags_out; reset != 0
+ * clears it.  Waits for the device to finish preceding work. */
+pkv_status pkv_device_errors(uint32_t *flags_out, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,1 +1,229 @@
-"""placeholder"""
+"""Attention over a paged KV cache, hand-written CUDA for GB300 (sm_103a).
+
+A thin ctypes binding over ``libpkv.so`` (C ABI in ``include/pkv.h``).  Each
+function carries the C entry point's name and only marshals arguments: torch
+tensors become device pointers, the current torch stream becomes the launch
+stream, and a non-OK status raises :class:`PkvError` with the library's
+message.  Every step of the computation runs in the library's kernels; if the
+library is missing the call fails loudly -- there is no fallback.
+
+PyTorch is used here for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+DEVERR_BLOCK_ID = 0x1
+DEVERR_POSITION = 0x2
+DEVERR_TIMEOUT = 0x4
+DEVERR_LENGTH = 0x8
+
+_STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+           3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS.get(status, str(status)), message))
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    """pkv_cache_desc."""
+
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64)]
+
+
+def make_desc(*, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
+              kv_dtype=KV_BF16, block_size=16) -> CacheDesc:
+    if isinstance(kv_dtype, str):
+        kv_dtype = KV_FP8_E4M3 if kv_dtype.startswith("fp8") else KV_BF16
+    return CacheDesc(int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                     int(kv_dtype), int(max_blocks_per_seq), int(num_blocks))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libpkv.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError("libpkv.so is not built (%s); run __graft_entry__.build()" % path)
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        D = ctypes.POINTER(CacheDesc)
+        sig = {
+            "pkv_cache_bytes": (ctypes.c_uint64, [D]),
+            "pkv_append_rope": (ctypes.c_int, [D, P, P, P, P, P, i32, P, P, i32, P, P, P, P, i32, P]),
+            "pkv_rope_cos_sin_table": (ctypes.c_int, [f32, i32, i32, P]),
+            "pkv_gather_kv": (ctypes.c_int, [D, P, P, P, P, i32, i64, P, P]),
+            "pkv_decode_attention": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32, i32,
+                                                    i32, P, P, P, ctypes.c_size_t, P]),
+            "pkv_decode_workspace_size": (ctypes.c_size_t, [D, i32, i32, i32, i32]),
+            "pkv_decode_plan": (ctypes.c_int, [D, i32, i32, i32, i32, P, P]),
+            "pkv_prefill_attention_ragged": (ctypes.c_int, [D, P, P, P, P, P, P, P, P, i32, i32,
+                                                            P, P, f32, i32, i32, P, P, P,
+                                                            ctypes.c_size_t, P]),
+            "pkv_prefill_workspace_size": (ctypes.c_size_t, [D, i32, i32]),
+            "pkv_merge_states": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, P, P]),
+            "pkv_last_error": (ctypes.c_char_p, []),
+            "pkv_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise PkvError(status, load_library().pkv_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ------------------------------------------------------------ entry points --
+
+def pkv_cache_bytes(desc: CacheDesc) -> int:
+    return int(load_library().pkv_cache_bytes(ctypes.byref(desc)))
+
+
+def pkv_rope_cos_sin_table(theta: float, rotary_dim: int, max_pos: int) -> np.ndarray:
+    """Host fp32 [max_pos][rotary_dim/2][2] (cos, sin) table."""
+    out = np.empty((max_pos, rotary_dim // 2, 2), dtype=np.float32)
+    _check(load_library().pkv_rope_cos_sin_table(float(theta), int(rotary_dim), int(max_pos),
+                                                 _ptr(out)))
+    return out
+
+
+def pkv_append_rope(desc, k_cache, v_cache, block_tables, token_to_seq, positions, k_new, v_new,
+                    q=None, cos_sin=None, k_scale=None, v_scale=None, num_seqs=None, stream=None):
+    num_seqs = block_tables.shape[0] if num_seqs is None else num_seqs
+    max_pos = 0 if cos_sin is None else cos_sin.shape[0]
+    _check(load_library().pkv_append_rope(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), int(num_seqs), _ptr(token_to_seq), _ptr(positions),
+        int(positions.shape[0]), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(cos_sin), int(max_pos),
+        _stream(stream)))
+
+
+def pkv_gather_kv(desc, cache, block_tables, context_lens, cu_context_lens, total_tokens, out,
+                  stream=None):
+    _check(load_library().pkv_gather_kv(
+        ctypes.byref(desc), _ptr(cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(cu_context_lens), int(context_lens.shape[0]), int(total_tokens), _ptr(out),
+        _stream(stream)))
+
+
+def pkv_decode_workspace_size(desc, num_seqs, max_context_len, window=-1, chunk_blocks=0) -> int:
+    return int(load_library().pkv_decode_workspace_size(ctypes.byref(desc), int(num_seqs),
+                                                        int(max_context_len), int(window),
+                                                        int(chunk_blocks)))
+
+
+def pkv_decode_plan(desc, num_seqs, max_context_len, window=-1, num_sms=0):
+    """Host planner: returns (chunk_blocks, max_splits)."""
+    c, s = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().pkv_decode_plan(ctypes.byref(desc), int(num_seqs), int(max_context_len),
+                                          int(window), int(num_sms), ctypes.byref(c),
+                                          ctypes.byref(s)))
+    return c.value, s.value
+
+
+def pkv_decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                         sm_scale, out, lse=None, workspace=None, window=-1, chunk_blocks=0,
+                         k_scale=None, v_scale=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().pkv_decode_attention(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len),
+        float(sm_scale), int(window), int(chunk_blocks), _ptr(out), _ptr(lse), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+
+
+def pkv_prefill_workspace_size(desc, num_seqs, total_q_tokens) -> int:
+    return int(load_library().pkv_prefill_workspace_size(ctypes.byref(desc), int(num_seqs),
+                                                         int(total_q_tokens)))
+
+
+def pkv_prefill_attention_ragged(desc, q, qo_indptr, k_cache, v_cache, block_tables, kv_lens,
+                                 sm_scale, out, lse=None, qo_indptr_host=None, kv_lens_host=None,
+                                 causal=True, window=-1, workspace=None, k_scale=None,
+                                 v_scale=None, stream=None):
+    qh = None if qo_indptr_host is None else np.ascontiguousarray(qo_indptr_host, np.int32)
+    kh = None if kv_lens_host is None else np.ascontiguousarray(kv_lens_host, np.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().pkv_prefill_attention_ragged(
+        ctypes.byref(desc), _ptr(q), _ptr(qo_indptr), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(kv_lens), int(kv_lens.shape[0]),
+        int(q.shape[0]), _ptr(qh), _ptr(kh), float(sm_scale), int(bool(causal)), int(window),
+        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_merge_states(o_parts, lse_parts, out, lse_out=None, stream=None):
+    """o_parts fp32 [P][rows][H][D], lse_parts fp32 [P][rows][H] -> out bf16 [rows][H][D]."""
+    P, rows, H, D = o_parts.shape
+    _check(load_library().pkv_merge_states(_ptr(o_parts), _ptr(lse_parts), int(P), int(rows),
+                                           int(H), int(D), _ptr(out), _ptr(lse_out),
+                                           _stream(stream)))
+
+
+def pkv_device_errors(reset: bool = True) -> int:
+    """Synchronously read (and by default clear) the device error word."""
+    v = ctypes.c_uint32()
+    _check(load_library().pkv_device_errors(ctypes.byref(v), int(bool(reset))))
+    return int(v.value)
+
+
+def pkv_last_error() -> str:
+    return load_library().pkv_last_error().decode(errors="replace")
+
+
+__all__ = [n for n in dir() if n.startswith("pkv_")] + [
+    "CacheDesc", "make_desc", "PkvError", "load_library", "library_path", "KV_BF16",
+    "KV_FP8_E4M3"]

@@ -1,0 +1,602 @@
+// api.cu -- the C ABI of libpkv: argument validation, split planning,
+// tensor-map descriptors, launches and error reporting.  Everything the
+// path computes runs in the kernels of decode.cu, prefill.cu and
+// append_gather_merge.cu; this file only decides and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "internal.h"
+
+namespace pkv {
+int decode_smem_bytes(int d, int fp8);
+}
+
+// One device error word per device (every GPU that loads the library holds
+// its own copy).  Kernels get its address as an argument.
+__device__ uint32_t g_pkv_device_error;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------- device state --
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+pkv_status device_state(uint32_t** err_ptr, int* num_sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_err_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_pkv_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_num_sms[dev] = sms;
+        g_err_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    if (err_ptr) *err_ptr = g_err_ptr[dev];
+    if (num_sms) *num_sms = g_num_sms[dev];
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------ tensor maps --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void* ptr;
+    int64_t num_blocks;
+    int32_t hkv, d, fp8, dev;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && num_blocks == o.num_blocks && hkv == o.hkv && d == o.d &&
+               fp8 == o.fp8 && dev == o.dev;
+    }
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    uint64_t stamp;
+};
+
+constexpr int kMapCache = 16;
+thread_local MapEntry g_maps[kMapCache];
+thread_local int g_maps_used = 0;
+thread_local uint64_t g_map_clock = 0;
+
+// The tiled view of one pool: dims (innermost first) {D, block_size, Hkv,
+// num_blocks}; box {inner, 16, 1, 1}.  bf16 rows are split into 64-element
+// boxes with the 128-byte swizzle; e4m3 rows are one unswizzled box.
+pkv_status pool_map(const void* pool, const pkv_cache_desc* desc, CUtensorMap* out) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const MapKey key{pool, desc->num_blocks, desc->num_kv_heads, desc->head_dim,
+                     desc->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 0, dev};
+    for (int i = 0; i < g_maps_used; ++i) {
+        if (g_maps[i].key == key) {
+            g_maps[i].stamp = ++g_map_clock;
+            *out = g_maps[i].map;
+            return PKV_OK;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const pkv::BoxShape box = pkv::kv_box_shape(desc->head_dim, key.fp8);
+    const cuuint64_t elem = key.fp8 ? 1 : 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(desc->head_dim),
+                                static_cast<cuuint64_t>(desc->block_size),
+                                static_cast<cuuint64_t>(desc->num_kv_heads),
+                                static_cast<cuuint64_t>(desc->num_blocks)};
+    const cuuint64_t strides[3] = {dims[0] * elem, dims[0] * dims[1] * elem,
+                                   dims[0] * dims[1] * dims[2] * elem};
+    const cuuint32_t boxdim[4] = {static_cast<cuuint32_t>(box.inner),
+                                  static_cast<cuuint32_t>(desc->block_size), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUtensorMap map;
+    CUresult r = fn(&map,
+                    key.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                    const_cast<void*>(pool), dims, strides, boxdim, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    box.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    int slot = 0;
+    if (g_maps_used < kMapCache) {
+        slot = g_maps_used++;
+    } else {
+        for (int i = 1; i < kMapCache; ++i)
+            if (g_maps[i].stamp < g_maps[slot].stamp) slot = i;
+    }
+    g_maps[slot].key = key;
+    g_maps[slot].map = map;
+    g_maps[slot].stamp = ++g_map_clock;
+    *out = map;
+    return PKV_OK;
+}
+
+// -------------------------------------------------------------- validation --
+
+constexpr int kMaxGroup = 16;
+constexpr int kMaxChunk = 128;   // blocks per decode CTA (32 per warp)
+constexpr int kMinChunk = 16;
+constexpr int kMaxSplits = 512;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pkv_status check_desc(const pkv_cache_desc* d) {
+    if (!d) return fail(PKV_ERR_INVALID_ARG, "desc is NULL");
+    if (d->num_q_heads <= 0 || d->num_kv_heads <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "head counts must be positive (Hq=%d, Hkv=%d)",
+                    d->num_q_heads, d->num_kv_heads);
+    if (d->num_q_heads % d->num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                    d->num_q_heads, d->num_kv_heads);
+    if (d->num_q_heads / d->num_kv_heads > kMaxGroup)
+        return fail(PKV_ERR_UNSUPPORTED, "group size %d > %d", d->num_q_heads / d->num_kv_heads,
+                    kMaxGroup);
+    if (d->head_dim != 64 && d->head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", d->head_dim);
+    if (d->block_size != 16) return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 16)", d->block_size);
+    if (d->kv_dtype != PKV_KV_BF16 && d->kv_dtype != PKV_KV_FP8_E4M3)
+        return fail(PKV_ERR_UNSUPPORTED, "kv_dtype %d", d->kv_dtype);
+    if (d->num_blocks <= 0 || d->num_blocks > 0x7FFFFFFFLL)
+        return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld out of range", (long long)d->num_blocks);
+    if (d->max_blocks_per_seq <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    return PKV_OK;
+}
+
+int elem_bytes(const pkv_cache_desc* d) { return d->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2; }
+
+// ---------------------------------------------------------------- planner --
+
+int max_visible_blocks(int max_ctx, int window) {
+    int mb = (max_ctx + 15) / 16;
+    if (window > 0) mb = std::min(mb, (window + 14) / 16 + 1);
+    return std::max(mb, 1);
+}
+
+int resident_ctas(int d, int fp8) {
+    const int smem = pkv::decode_smem_bytes(d, fp8) + 1024;
+    return std::max(1, std::min(4, (228 * 1024) / smem));
+}
+
+pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, int window,
+                       int num_sms, int chunk_req, int* chunk_out, int* splits_out) {
+    const int mb = max_visible_blocks(max_ctx, window);
+    int chunk;
+    if (chunk_req > 0) {
+        if (chunk_req > kMaxChunk)
+            return fail(PKV_ERR_INVALID_ARG, "chunk_blocks %d > %d", chunk_req, kMaxChunk);
+        chunk = chunk_req;
+    } else {
+        // Ragged batches average about half their longest context; aim for
+        // ~4 waves of resident CTAs over the whole GPU.
+        const double pairs = double(num_seqs) * desc->num_kv_heads;
+        const double est_blocks = pairs * std::max(1.0, 0.6 * mb);
+        const double target =
+            double(std::max(num_sms, 1)) * resident_ctas(desc->head_dim, desc->kv_dtype) * 4.0;
+        chunk = int(std::ceil(est_blocks / target));
+        chunk = std::max(kMinChunk, std::min(kMaxChunk, chunk));
+        chunk = std::max(chunk, (mb + kMaxSplits - 1) / kMaxSplits);  // bound the split count
+        if (chunk > mb) chunk = mb;
+    }
+    const int splits = (mb + chunk - 1) / chunk;
+    if (splits > kMaxSplits)
+        return fail(PKV_ERR_UNSUPPORTED, "context needs %d splits of %d blocks (max %d)", splits, chunk,
+                    kMaxSplits);
+    *chunk_out = chunk;
+    *splits_out = splits;
+    return PKV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct DecodeWs {
+    size_t counters, lse, o, total;
+};
+
+DecodeWs decode_ws_layout(const pkv_cache_desc* d, int num_seqs, int splits) {
+    DecodeWs w{};
+    const size_t pairs = size_t(num_seqs) * d->num_kv_heads;
+    const size_t G = d->num_q_heads / d->num_kv_heads;
+    w.counters = 0;
+    w.lse = align256(pairs * sizeof(uint32_t));
+    w.o = w.lse + align256(pairs * splits * G * sizeof(float));
+    w.total = splits > 1 ? w.o + align256(pairs * splits * G * d->head_dim * sizeof(float))
+                         : 0;
+    return w;
+}
+
+}  // namespace
+
+namespace pkv {
+BoxShape kv_box_shape(int head_dim, int fp8) {
+    if (fp8) return BoxShape{head_dim, 1, 0};
+    return BoxShape{64, head_dim / 64, 1};
+}
+}  // namespace pkv
+
+// ===================================================================== ABI ==
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error; }
+
+uint64_t pkv_cache_bytes(const pkv_cache_desc* desc) {
+    if (check_desc(desc) != PKV_OK) return 0;
+    return uint64_t(desc->num_blocks) * desc->num_kv_heads * desc->block_size * desc->head_dim *
+           elem_bytes(desc);
+}
+
+pkv_status pkv_rope_cos_sin_table(float theta, int32_t rotary_dim, int32_t max_pos,
+                                  float* host_out) {
+    g_last_error[0] = 0;
+    if (!host_out) return fail(PKV_ERR_INVALID_ARG, "host_out is NULL");
+    if (rotary_dim <= 0 || rotary_dim % 2 || max_pos < 0 || !(theta > 0.f))
+        return fail(PKV_ERR_INVALID_ARG, "bad rope table shape (dim=%d, max_pos=%d, theta=%g)",
+                    rotary_dim, max_pos, double(theta));
+    const int half = rotary_dim / 2;
+    for (int p = 0; p < max_pos; ++p) {
+        for (int j = 0; j < half; ++j) {
+            const double inv_freq = std::pow(double(theta), -(2.0 * j) / double(rotary_dim));
+            const double ang = double(p) * inv_freq;
+            host_out[(size_t(p) * half + j) * 2 + 0] = float(std::cos(ang));
+            host_out[(size_t(p) * half + j) * 2 + 1] = float(std::sin(ang));
+        }
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_plan(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_context_len,
+                           int32_t window, int32_t num_sms, int32_t* chunk_blocks_out,
+                           int32_t* max_splits_out) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (!chunk_blocks_out || !max_splits_out) return fail(PKV_ERR_INVALID_ARG, "null output pointer");
+    if (num_seqs < 0 || max_context_len < 1)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d / max_context_len %d", num_seqs, max_context_len);
+    if (num_sms <= 0) {
+        st = device_state(nullptr, &num_sms);
+        if (st != PKV_OK) return st;
+    }
+    int c = 0, s = 0;
+    st = plan_decode(desc, num_seqs, max_context_len, window, num_sms, 0, &c, &s);
+    if (st != PKV_OK) return st;
+    *chunk_blocks_out = c;
+    *max_splits_out = s;
+    return PKV_OK;
+}
+
+size_t pkv_decode_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,
+                                 int32_t max_context_len, int32_t window, int32_t chunk_blocks) {
+    if (check_desc(desc) != PKV_OK || num_seqs <= 0 || max_context_len < 1) return 0;
+    int sms = 0;
+    if (chunk_blocks <= 0 && device_state(nullptr, &sms) != PKV_OK) return 0;
+    int c = 0, s = 0;
+    if (plan_decode(desc, num_seqs, max_context_len, window, sms, chunk_blocks, &c, &s) != PKV_OK)
+        return 0;
+    return decode_ws_layout(desc, num_seqs, s).total;
+}
+
+pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                                const void* v_cache, const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                int32_t num_seqs, int32_t max_context_len, float sm_scale,
+                                int32_t window, int32_t chunk_blocks, void* out, float* lse_out,
+                                void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_seqs > 65535)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
+    if (max_context_len < 1 || max_context_len > desc->max_blocks_per_seq * desc->block_size)
+        return fail(PKV_ERR_INVALID_ARG, "max_context_len %d outside [1, %d]", max_context_len,
+                    desc->max_blocks_per_seq * desc->block_size);
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
+    uint32_t* err = nullptr;
+    int sms = 0;
+    st = device_state(&err, &sms);
+    if (st != PKV_OK) return st;
+    int chunk = 0, splits = 0;
+    st = plan_decode(desc, num_seqs, max_context_len, window, sms, chunk_blocks, &chunk, &splits);
+    if (st != PKV_OK) return st;
+    const DecodeWs ws = decode_ws_layout(desc, num_seqs, splits);
+    if (ws.total > 0) {
+        if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", ws.total);
+        if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        if (workspace_bytes < ws.total)
+            return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, ws.total);
+    }
+    CUtensorMap kmap, vmap;
+    st = pool_map(k_cache, desc, &kmap);
+    if (st != PKV_OK) return st;
+    st = pool_map(v_cache, desc, &vmap);
+    if (st != PKV_OK) return st;
+    pkv::DecodeArgs a{};
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    a.counters = ws.total ? reinterpret_cast<uint32_t*>(wsb + ws.counters) : nullptr;
+    a.part_lse = ws.total ? reinterpret_cast<float*>(wsb + ws.lse) : nullptr;
+    a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;
+    a.err = err;
+    a.num_seqs = num_seqs;
+    a.hq = desc->num_q_heads;
+    a.hkv = desc->num_kv_heads;
+    a.group = desc->num_q_heads / desc->num_kv_heads;
+    a.d = desc->head_dim;
+    a.mbps = desc->max_blocks_per_seq;
+    a.window = window;
+    a.chunk_blocks = chunk;
+    a.max_splits = splits;
+    a.max_ctx = max_context_len;
+    a.fp8 = fp8 ? 1 : 0;
+    a.num_blocks = desc->num_blocks;
+    a.sm_scale = sm_scale;
+    cudaError_t e = pkv::launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return PKV_OK;
+}
+
+size_t pkv_prefill_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,
+                                  int32_t total_q_tokens) {
+    (void)desc;
+    (void)num_seqs;
+    (void)total_q_tokens;
+    return 0;
+}
+
+pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* q,
+                                        const int32_t* qo_indptr, const void* k_cache,
+                                        const void* v_cache, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_tables,
+                                        const int32_t* kv_lens, int32_t num_seqs,
+                                        int32_t total_q_tokens, const int32_t* qo_indptr_host,
+                                        const int32_t* kv_lens_host, float sm_scale,
+                                        int32_t causal, int32_t window, void* out,
+                                        float* lse_out, void* workspace,
+                                        size_t workspace_bytes, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    (void)k_scale;
+    (void)v_scale;
+    (void)workspace;
+    (void)workspace_bytes;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (desc->kv_dtype != PKV_KV_BF16)
+        return fail(PKV_ERR_UNSUPPORTED, "prefill reads bf16 pools only");
+    if (num_seqs < 0 || num_seqs > 65535)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
+    if (total_q_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "total_q_tokens < 0");
+    if (num_seqs == 0 || total_q_tokens == 0) return PKV_OK;
+    if (!q || !qo_indptr || !k_cache || !v_cache || !block_tables || !kv_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
+    const int G = desc->num_q_heads / desc->num_kv_heads;
+    const int QT = pkv::prefill_q_tile(G);
+    int max_q = total_q_tokens;
+    if (qo_indptr_host) {
+        if (qo_indptr_host[0] != 0 || qo_indptr_host[num_seqs] != total_q_tokens)
+            return fail(PKV_ERR_INVALID_ARG, "qo_indptr_host must run from 0 to total_q_tokens");
+        max_q = 0;
+        for (int s = 0; s < num_seqs; ++s) {
+            const int ql = qo_indptr_host[s + 1] - qo_indptr_host[s];
+            if (ql < 0) return fail(PKV_ERR_INVALID_ARG, "qo_indptr_host decreases at %d", s);
+            max_q = std::max(max_q, ql);
+            if (kv_lens_host) {
+                if (kv_lens_host[s] < ql)
+                    return fail(PKV_ERR_INVALID_ARG, "sequence %d: kv_len %d < q_len %d", s, kv_lens_host[s], ql);
+                if (kv_lens_host[s] > desc->max_blocks_per_seq * desc->block_size)
+                    return fail(PKV_ERR_INVALID_ARG, "sequence %d: kv_len %d beyond the table", s, kv_lens_host[s]);
+            }
+        }
+    }
+    const int max_qtiles = (max_q + QT - 1) / QT;
+    if (max_qtiles == 0) return PKV_OK;
+    uint32_t* err = nullptr;
+    st = device_state(&err, nullptr);
+    if (st != PKV_OK) return st;
+    CUtensorMap kmap, vmap;
+    st = pool_map(k_cache, desc, &kmap);
+    if (st != PKV_OK) return st;
+    st = pool_map(v_cache, desc, &vmap);
+    if (st != PKV_OK) return st;
+    pkv::PrefillArgs a{};
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.qo_indptr = qo_indptr;
+    a.kv_lens = kv_lens;
+    a.block_tables = block_tables;
+    a.err = err;
+    a.num_seqs = num_seqs;
+    a.hq = desc->num_q_heads;
+    a.hkv = desc->num_kv_heads;
+    a.group = G;
+    a.d = desc->head_dim;
+    a.mbps = desc->max_blocks_per_seq;
+    a.causal = causal ? 1 : 0;
+    a.window = window;
+    a.max_qtiles = max_qtiles;
+    a.q_tile = QT;
+    a.total_q = total_q_tokens;
+    a.num_blocks = desc->num_blocks;
+    a.sm_scale = sm_scale;
+    cudaError_t e = pkv::launch_prefill(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_append_rope(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                           const float* k_scale, const float* v_scale,
+                           const int32_t* block_tables, int32_t num_seqs,
+                           const int32_t* token_to_seq, const int32_t* positions,
+                           int32_t num_tokens, const void* k_new, const void* v_new,
+                           void* q_inout, const float* rope_cos_sin, int32_t rope_max_pos,
+                           pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0 || num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "negative count");
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !block_tables || !token_to_seq || !positions || !k_new || !v_new)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
+    if (rope_cos_sin && rope_max_pos <= 0) return fail(PKV_ERR_INVALID_ARG, "rope_max_pos must be positive");
+    uint32_t* err = nullptr;
+    st = device_state(&err, nullptr);
+    if (st != PKV_OK) return st;
+    pkv::AppendArgs a{};
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_tables = block_tables;
+    a.token_to_seq = token_to_seq;
+    a.positions = positions;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.q = q_inout;
+    a.cos_sin = rope_cos_sin;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.hq = desc->num_q_heads;
+    a.hkv = desc->num_kv_heads;
+    a.d = desc->head_dim;
+    a.mbps = desc->max_blocks_per_seq;
+    a.max_pos = rope_max_pos;
+    a.num_blocks = desc->num_blocks;
+    a.fp8 = fp8 ? 1 : 0;
+    a.err = err;
+    cudaError_t e = pkv::launch_append_rope(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_gather_kv(const pkv_cache_desc* desc, const void* cache, const int32_t* block_tables,
+                         const int32_t* context_lens, const int32_t* cu_context_lens,
+                         int32_t num_seqs, int64_t total_tokens, void* out, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || total_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative count");
+    if (num_seqs == 0 || total_tokens == 0) return PKV_OK;
+    if (!cache || !block_tables || !context_lens || !cu_context_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    if (!aligned(cache, 16) || !aligned(out, 16))
+        return fail(PKV_ERR_INVALID_ARG, "cache and out must be 16-byte aligned");
+    uint32_t* err = nullptr;
+    st = device_state(&err, nullptr);
+    if (st != PKV_OK) return st;
+    pkv::GatherArgs a{};
+    a.cache = cache;
+    a.block_tables = block_tables;
+    a.lens = context_lens;
+    a.cu_lens = cu_context_lens;
+    a.out = out;
+    a.num_seqs = num_seqs;
+    a.hkv = desc->num_kv_heads;
+    a.row_bytes = desc->head_dim * elem_bytes(desc);
+    a.mbps = desc->max_blocks_per_seq;
+    a.total_tokens = total_tokens;
+    a.num_blocks = desc->num_blocks;
+    a.err = err;
+    cudaError_t e = pkv::launch_gather(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_parts,
+                            int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                            float* lse_out, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    if (num_parts < 0 || num_rows < 0 || num_heads < 0 || head_dim <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad merge shape");
+    if (num_rows == 0 || num_heads == 0) return PKV_OK;
+    if (!out || (num_parts > 0 && (!o_parts || !lse_parts)))
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    pkv::MergeArgs a{o_parts, lse_parts, out, lse_out, num_parts, num_rows, num_heads, head_dim};
+    cudaError_t e = pkv::launch_merge(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_device_errors(uint32_t* flags_out, int32_t reset) {
+    g_last_error[0] = 0;
+    if (!flags_out) return fail(PKV_ERR_INVALID_ARG, "flags_out is NULL");
+    uint32_t* err = nullptr;
+    pkv_status st = device_state(&err, nullptr);
+    if (st != PKV_OK) return st;
+    cudaError_t e = cudaMemcpyFromSymbol(flags_out, g_pkv_device_error, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (reset) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_pkv_device_error, &zero, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "reset device error word");
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

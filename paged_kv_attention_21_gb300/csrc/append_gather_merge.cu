@@ -1,0 +1,235 @@
+// append_gather_merge.cu -- the three small kernels of the path:
+//   * fused KV append + RoPE (+ e4m3 quantisation)  (llm-infer, "What It Does":
+//     KV writes and fused RoPE inside the decode step);
+//   * block-table gather of one pool into contiguous rows (infer-lab,
+//     "Technique" table: PagedAttention block tables);
+//   * standalone merge of partial (o, lse) states (FlashAttention-2 work
+//     partitioning, cited under llm-infer "References").
+// All three are latency-bound: a few MB at most.  Loads and stores are
+// coalesced across the warp; no shared memory is needed.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+// ------------------------------------------------------- append + RoPE --
+//
+// One warp per (token, row), rows = the Hkv KV heads (K and V together)
+// followed by the Hq query heads.  Lane l owns the rotation pairs
+// (j, j + D/2) for j in [l*PPL, (l+1)*PPL).
+
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(256) append_rope_kernel(AppendArgs a) {
+    constexpr int HALF = D / 2;
+    constexpr int PPL = HALF / 32;  // 1 for D=64, 2 for D=128
+    const int lane = threadIdx.x & 31;
+    const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int rows = a.hkv + ((a.q != nullptr && a.cos_sin != nullptr) ? a.hq : 0);
+    const long long i = w / rows;
+    const int r = static_cast<int>(w % rows);
+    if (i >= a.num_tokens) return;
+
+    const int s = a.token_to_seq[i];
+    const int p = a.positions[i];
+    const bool ok = s >= 0 && s < a.num_seqs && p >= 0 && p / kBlockSize < a.mbps &&
+                    (a.cos_sin == nullptr || p < a.max_pos);
+    if (!ok) {
+        if (lane == 0) flag_error(a.err, PKV_DEVERR_POSITION);
+        return;
+    }
+    const int j0 = lane * PPL;
+    float c[PPL], sn[PPL];
+    const bool rope = a.cos_sin != nullptr;
+    if (rope) {
+        const float* cs = a.cos_sin + (static_cast<size_t>(p) * HALF + j0) * 2;
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            c[k] = cs[2 * k];
+            sn[k] = cs[2 * k + 1];
+        }
+    }
+
+    // Load this lane's pairs of a bf16 row and (optionally) rotate them.
+    auto rotate = [&](const __nv_bfloat16* x, float (&lo)[PPL], float (&hi)[PPL]) {
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            const float av = __bfloat162float(x[j0 + k]);
+            const float bv = __bfloat162float(x[HALF + j0 + k]);
+            if (rope) {
+                // x'[j] = a*c - b*s ; x'[j+D/2] = b*c + a*s ; each op rounded
+                lo[k] = __fsub_rn(__fmul_rn(av, c[k]), __fmul_rn(bv, sn[k]));
+                hi[k] = __fadd_rn(__fmul_rn(bv, c[k]), __fmul_rn(av, sn[k]));
+            } else {
+                lo[k] = av;
+                hi[k] = bv;
+            }
+        }
+    };
+
+    if (r < a.hkv) {
+        const int blk = a.block_tables[static_cast<size_t>(s) * a.mbps + p / kBlockSize];
+        if (blk < 0 || blk >= a.num_blocks) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+            return;
+        }
+        const size_t src = (static_cast<size_t>(i) * a.hkv + r) * D;
+        const size_t dst = ((static_cast<size_t>(blk) * a.hkv + r) * kBlockSize + p % kBlockSize) * D;
+        const __nv_bfloat16* kx = static_cast<const __nv_bfloat16*>(a.k_new) + src;
+        const __nv_bfloat16* vx = static_cast<const __nv_bfloat16*>(a.v_new) + src;
+        float lo[PPL], hi[PPL];
+        rotate(kx, lo, hi);
+        if constexpr (!kFp8) {
+            __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(a.k_cache) + dst;
+            __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(a.v_cache) + dst;
+#pragma unroll
+            for (int k = 0; k < PPL; ++k) {
+                kc[j0 + k] = __float2bfloat16_rn(lo[k]);
+                kc[HALF + j0 + k] = __float2bfloat16_rn(hi[k]);
+                vc[j0 + k] = vx[j0 + k];
+                vc[HALF + j0 + k] = vx[HALF + j0 + k];
+            }
+        } else {
+            uint8_t* kc = static_cast<uint8_t*>(a.k_cache) + dst;
+            uint8_t* vc = static_cast<uint8_t*>(a.v_cache) + dst;
+            const float ks = a.k_scale[r];
+            const float vs = a.v_scale[r];
+#pragma unroll
+            for (int k = 0; k < PPL; ++k) {
+                kc[j0 + k] = __nv_cvt_float_to_fp8(__fdiv_rn(lo[k], ks), __NV_SATFINITE, __NV_E4M3);
+                kc[HALF + j0 + k] =
+                    __nv_cvt_float_to_fp8(__fdiv_rn(hi[k], ks), __NV_SATFINITE, __NV_E4M3);
+                vc[j0 + k] = __nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(vx[j0 + k]), vs),
+                                                   __NV_SATFINITE, __NV_E4M3);
+                vc[HALF + j0 + k] =
+                    __nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(vx[HALF + j0 + k]), vs),
+                                          __NV_SATFINITE, __NV_E4M3);
+            }
+        }
+    } else {
+        const int h = r - a.hkv;
+        __nv_bfloat16* qx = static_cast<__nv_bfloat16*>(a.q) + (static_cast<size_t>(i) * a.hq + h) * D;
+        float lo[PPL], hi[PPL];
+        rotate(qx, lo, hi);
+        __syncwarp();  // every lane has read its pairs before any lane writes
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            qx[j0 + k] = __float2bfloat16_rn(lo[k]);
+            qx[HALF + j0 + k] = __float2bfloat16_rn(hi[k]);
+        }
+    }
+}
+
+cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
+    const int rows = a.hkv + ((a.q != nullptr && a.cos_sin != nullptr) ? a.hq : 0);
+    const long long warps = static_cast<long long>(a.num_tokens) * rows;
+    if (warps == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long blocks = (warps * 32 + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(blocks));
+    if (a.d == 64) {
+        if (a.fp8) append_rope_kernel<64, true><<<grid, threads, 0, stream>>>(a);
+        else append_rope_kernel<64, false><<<grid, threads, 0, stream>>>(a);
+    } else {
+        if (a.fp8) append_rope_kernel<128, true><<<grid, threads, 0, stream>>>(a);
+        else append_rope_kernel<128, false><<<grid, threads, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- gather --
+//
+// One thread per 16-byte chunk of an output row.
+
+__global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+    const int chunks = a.row_bytes / 16;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long per_token = static_cast<long long>(a.hkv) * chunks;
+    const long long g = idx / per_token;
+    if (g >= a.total_tokens) return;
+    const int h = static_cast<int>((idx / chunks) % a.hkv);
+    const int c = static_cast<int>(idx % chunks);
+    // sequence owning output row g: last s with cu_lens[s] <= g
+    int lo = 0, hi = a.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cu_lens[mid] <= g) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s = lo;
+    const int t = static_cast<int>(g - a.cu_lens[s]);
+    if (t < 0 || t >= a.lens[s] || t / kBlockSize >= a.mbps) {
+        if (c == 0 && h == 0) flag_error(a.err, PKV_DEVERR_POSITION);
+        return;
+    }
+    const int blk = a.block_tables[static_cast<size_t>(s) * a.mbps + t / kBlockSize];
+    if (blk < 0 || blk >= a.num_blocks) {
+        if (c == 0 && h == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+        return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(
+        static_cast<const uint8_t*>(a.cache) +
+        ((static_cast<size_t>(blk) * a.hkv + h) * kBlockSize + t % kBlockSize) * a.row_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
+                                          (static_cast<size_t>(g) * a.hkv + h) * a.row_bytes);
+    dst[c] = src[c];
+}
+
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
+    const long long n = a.total_tokens * a.hkv * (a.row_bytes / 16);
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long blocks = (n + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    gather_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- merge --
+//
+// One warp per (row, head); lanes stride over head_dim.
+//   M = max_i lse_i ; w_i = exp(lse_i - M) ; o = sum w_i o_i / sum w_i ;
+//   lse = M + ln sum w_i.   Empty parts (lse = -inf) are skipped.
+
+__global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long RH = static_cast<long long>(a.num_rows) * a.num_heads;
+    if (w >= RH) return;
+    float M = -INFINITY;
+    for (int i = 0; i < a.num_parts; ++i) M = fmaxf(M, a.lse_parts[i * RH + w]);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + w * a.head_dim;
+    if (M == -INFINITY) {
+        for (int d = lane; d < a.head_dim; d += 32) out[d] = __float2bfloat16_rn(0.0f);
+        if (a.lse_out && lane == 0) a.lse_out[w] = -INFINITY;
+        return;
+    }
+    float W = 0.0f;
+    for (int i = 0; i < a.num_parts; ++i) {
+        const float l = a.lse_parts[i * RH + w];
+        if (l != -INFINITY) W += expf(l - M);
+    }
+    const float invW = 1.0f / W;
+    for (int d = lane; d < a.head_dim; d += 32) {
+        float acc = 0.0f;
+        for (int i = 0; i < a.num_parts; ++i) {
+            const float l = a.lse_parts[i * RH + w];
+            if (l == -INFINITY) continue;
+            acc += expf(l - M) * a.o_parts[(i * RH + w) * a.head_dim + d];
+        }
+        out[d] = __float2bfloat16_rn(acc * invW);
+    }
+    if (a.lse_out && lane == 0) a.lse_out[w] = M + logf(W);
+}
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(a.num_rows) * a.num_heads;
+    if (warps == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long blocks = (warps * 32 + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

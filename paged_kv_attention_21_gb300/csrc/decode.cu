@@ -1,0 +1,507 @@
+// decode.cu -- split-KV GQA decode attention over the paged cache.
+//
+// What it computes (FlashAttention-2 work partitioning, cited under
+// llm-infer "References"; the paged cache of infer-lab's "Technique" table):
+// for sequence s, KV head kvh and each of its G query heads,
+//     o = softmax(sm_scale * q K^T) V     over the visible keys,
+// where K/V rows are gathered block by block through the block table.
+//
+// Work decomposition.  The visible blocks of every (sequence, KV head) are
+// cut into chunks of `chunk_blocks` blocks (the planner in api.cu); one CTA
+// owns one chunk.  Its 4 warps take the chunk's blocks round-robin, each
+// warp running its own NSTAGE-deep pipeline of TMA bulk-tensor loads
+// (K tile + V tile of one block, 16 rows x D) completed on a per-stage
+// mbarrier.  A warp computes, per block,
+//     S[16 x 16] = Q[16 x D] . K^T     (mma.sync m16n8k16; rows = the G query
+//                                       heads of the group, padded to 16)
+//     online softmax on S (running max / sum per row, exp2 domain)
+//     O[16 x D] += P[16 x 16] . V
+// so ONE read of each K/V block serves the whole GQA group.  At the end the
+// 4 warps combine in shared memory; a chunk that is its sequence's only one
+// writes bf16 output, otherwise it writes an fp32 (o, lse) partial to the
+// workspace and takes a ticket; the last chunk to arrive merges
+//     M = max lse_i, w_i = exp(lse_i - M), o = sum w_i o_i / sum w_i
+// and resets the ticket, all in the same launch.
+//
+// e4m3 pools: the TMA loads fp8 bytes, each warp converts the tile to f16
+// (exact) in shared memory and runs the f16 MMA; k_scale folds into the
+// logit scale and v_scale into the output.
+//
+// Roofline: HBM.  Per (block, KV head) the kernel reads 2*16*D*elem bytes
+// and does 4*16*D*G flops, G flop/byte for bf16 -- far below the tensor
+// pipe's ridge, so the design goal is bytes in flight, not MMA rate.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+template <int D, bool kFp8>
+struct DecodeCfg {
+    static constexpr int kStages = 3;
+    static constexpr int kElem = kFp8 ? 1 : 2;
+    static constexpr int kTileBytes = kBlockSize * D * kElem;  // one block of one head
+    static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
+    // bf16: 128-byte swizzled boxes of 64 elements; fp8: one unswizzled box
+    static constexpr int kBoxInner = kFp8 ? D : 64;
+    static constexpr int kBoxes = D / kBoxInner;
+    static constexpr int kBoxBytes = kBlockSize * kBoxInner * kElem;
+    static constexpr int kConvBytes = kFp8 ? 2 * kBlockSize * D * 2 : 0;  // f16 K + V
+    static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
+    static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
+    static constexpr int kCombBytes = kWarps * 16 * kCombStride * 4;
+    static constexpr int kBodyBytes = kWarps * kWarpBytes > kCombBytes ? kWarps * kWarpBytes
+                                                                       : kCombBytes;
+    static constexpr int kSmemBytes = kBodyBytes + 1024;  // + alignment slack
+};
+
+// f16 staging of an fp8 tile: src [16][D] bytes (row-major) -> dst [D/64][16][64]
+// f16 with the 128-byte swizzle, the layout the bf16 path gets from TMA.
+template <int D>
+__device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, int lane) {
+    constexpr int kChunksPerRow = D / 16;
+    constexpr int kChunks = kBlockSize * kChunksPerRow;
+#pragma unroll
+    for (int c = lane; c < kChunks; c += 32) {
+        const int r = c / kChunksPerRow;
+        const int cc = c % kChunksPerRow;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + c * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+            h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+            h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+        }
+        const int d0 = cc * 2;  // destination 16-byte chunk (8 f16) index in the row
+        *reinterpret_cast<uint4*>(dst + (d0 >> 3) * 2048 + sw128(r, d0 & 7)) =
+            make_uint4(h[0], h[1], h[2], h[3]);
+        const int d1 = d0 + 1;
+        *reinterpret_cast<uint4*>(dst + (d1 >> 3) * 2048 + sw128(r, d1 & 7)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
+
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
+                                                          const __grid_constant__ CUtensorMap kmap,
+                                                          const __grid_constant__ CUtensorMap vmap) {
+    using C = DecodeCfg<D, kFp8>;
+    constexpr int KSTEPS = D / 16;   // k-steps of Q.K^T
+    constexpr int NTILES = D / 8;    // n-tiles of O
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
+    __shared__ float s_m[kWarps][16];
+    __shared__ float s_l[kWarps][16];
+    __shared__ int s_flag;
+
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int seq = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+
+    int ctx = a.context_lens[seq];
+    // the split plan (and the workspace) covers contexts up to max_ctx, which
+    // the host checked against the table capacity
+    if (ctx > a.max_ctx) {
+        if (threadIdx.x == 0 && split == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+        ctx = a.max_ctx;
+    }
+    const int lo = (a.window > 0 && ctx > a.window) ? ctx - a.window : 0;
+    if (ctx <= 0) {  // no visible key: o = 0, lse = -inf
+        if (split == 0) {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
+                               (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
+            for (int i = threadIdx.x; i < G * D; i += kThreads) o[i] = __float2bfloat16_rn(0.f);
+            if (a.lse_out && threadIdx.x < G)
+                a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+    const int first_blk = lo / kBlockSize;
+    const int last_blk = (ctx - 1) / kBlockSize;
+    const int nsplit = (last_blk - first_blk + a.chunk_blocks) / a.chunk_blocks;
+    if (split >= nsplit) return;
+    const int b0 = first_blk + split * a.chunk_blocks;
+    const int b1 = min(last_blk + 1, b0 + a.chunk_blocks);
+    const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kWarps - 1) / kWarps : 0;
+
+    if (threadIdx.x < kWarps * C::kStages) mbar_init(&bars[threadIdx.x / C::kStages][threadIdx.x % C::kStages], 1);
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        s_flag = 0;
+    }
+    fence_barrier_init();
+    __syncthreads();
+
+    // Physical block ids of this warp's blocks: lane k holds the k-th one.
+    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
+    int phys = 0;
+    if (lane < my_n) {
+        phys = bt[b0 + warp + lane * kWarps];
+        if (phys < 0 || phys >= a.num_blocks) {
+            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+            phys = 0;  // read a valid block; the output is flagged invalid
+        }
+    }
+    uint8_t* wbase = smem + warp * C::kWarpBytes;
+    // Lane 0 issues the prologue; the shuffle reads lane k's id from lane 0's
+    // point of view, so every lane takes part in it.
+#pragma unroll
+    for (int k = 0; k < C::kStages; ++k) {
+        const int pb = __shfl_sync(0xFFFFFFFFu, phys, k & 31);
+        if (lane == 0 && k < my_n) {
+            const int st = k;
+            uint8_t* kdst = wbase + st * C::kStageBytes;
+            uint8_t* vdst = kdst + C::kTileBytes;
+            mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+                tma_load_4d(kdst + bx * C::kBoxBytes, &kmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
+                tma_load_4d(vdst + bx * C::kBoxBytes, &vmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
+            }
+        }
+    }
+
+    // Q fragments (A operand, rows = heads of the group, zero-padded to 16).
+    const int g0 = lane >> 2;
+    const int tig = lane & 3;
+    uint32_t qa[KSTEPS][4];
+    {
+        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) +
+                                  (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {
+                const int row = g0 + ((part & 1) ? 8 : 0);
+                const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
+                uint32_t v = 0;
+                if (row < G) v = *reinterpret_cast<const uint32_t*>(qb + row * D + col);
+                if constexpr (kFp8) v = pack2<true>(bf16_lo(v), bf16_hi(v));
+                qa[kk][part] = v;
+            }
+        }
+    }
+    float scale_log2 = a.sm_scale * 1.4426950408889634f;
+    if constexpr (kFp8) scale_log2 *= a.k_scale[kvh];
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float o[NTILES][4];
+#pragma unroll
+    for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    uint8_t* convK = wbase + C::kStages * C::kStageBytes;
+    uint8_t* convV = convK + (kFp8 ? kBlockSize * D * 2 : 0);
+    bool failed = false;
+    int k = 0;
+    for (; k < my_n; ++k) {
+        const int st = k % C::kStages;
+        const uint32_t ph = (k / C::kStages) & 1;
+        const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[warp][st], ph));
+        if (!ready) {
+            failed = true;
+            break;
+        }
+        const uint8_t* ktile = wbase + st * C::kStageBytes;
+        const uint8_t* vtile = ktile + C::kTileBytes;
+        if constexpr (kFp8) {
+            convert_fp8_tile<D>(ktile, convK, lane);
+            convert_fp8_tile<D>(vtile, convV, lane);
+            __syncwarp();
+            ktile = convK;
+            vtile = convV;
+        }
+        const uint32_t kaddr = smem_u32(ktile);
+        const uint32_t vaddr = smem_u32(vtile);
+
+        // ---- S = Q . K^T  (16 heads x 16 tokens)
+        float sacc[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+        {
+            const int tok = (lane & 7) + ((lane >> 4) << 3);
+            const int csel = (lane >> 3) & 1;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int chunk = 2 * kk + csel;
+                uint32_t b00, b01, b10, b11;
+                ldmatrix_x4(b00, b01, b10, b11,
+                            kaddr + (chunk >> 3) * 2048 + sw128(tok, chunk & 7));
+                mma_16816<kFp8>(sacc[0], qa[kk], b00, b01);
+                mma_16816<kFp8>(sacc[1], qa[kk], b10, b11);
+            }
+        }
+
+        // ---- mask + online softmax (exp2 domain)
+        const int blk = b0 + warp + k * kWarps;
+        const int tok_base = blk * kBlockSize;
+        const bool edge = tok_base < lo || tok_base + kBlockSize > ctx;
+        float x[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[n][e] = sacc[n][e] * scale_log2;
+                if (edge) {
+                    const int t = tok_base + n * 8 + 2 * tig + (e & 1);
+                    if (t < lo || t >= ctx) x[n][e] = -INFINITY;
+                }
+            }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+        const float mn0 = fmaxf(m_run[0], mx0);
+        const float mn1 = fmaxf(m_run[1], mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m_run[0] - mu0);
+        const float al1 = fast_exp2(m_run[1] - mu1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            p[n][0] = fast_exp2(x[n][0] - mu0);
+            p[n][1] = fast_exp2(x[n][1] - mu0);
+            p[n][2] = fast_exp2(x[n][2] - mu1);
+            p[n][3] = fast_exp2(x[n][3] - mu1);
+        }
+        l_run[0] = l_run[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        l_run[1] = l_run[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int nt = 0; nt < NTILES; ++nt) {
+                o[nt][0] *= al0;
+                o[nt][1] *= al0;
+                o[nt][2] *= al1;
+                o[nt][3] *= al1;
+            }
+        }
+        uint32_t pa[4];
+        pa[0] = pack2<kFp8>(p[0][0], p[0][1]);
+        pa[1] = pack2<kFp8>(p[0][2], p[0][3]);
+        pa[2] = pack2<kFp8>(p[1][0], p[1][1]);
+        pa[3] = pack2<kFp8>(p[1][2], p[1][3]);
+
+        // ---- O += P . V   (V rows masked to zero past the visible range so a
+        // NaN in an unused slot never meets a zero weight inside the MMA)
+        uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
+        if (edge) {
+            const int t0 = tok_base + 2 * tig;
+            const bool v0 = t0 >= lo && t0 < ctx, v1 = t0 + 1 >= lo && t0 + 1 < ctx;
+            const bool v8 = t0 + 8 >= lo && t0 + 8 < ctx, v9 = t0 + 9 >= lo && t0 + 9 < ctx;
+            keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
+            keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
+        }
+        {
+            const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int csel = lane >> 4;
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                const int chunk = 2 * j + csel;
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(v0, v1, v2, v3,
+                                  vaddr + (chunk >> 3) * 2048 + sw128(tok, chunk & 7));
+                v0 &= keep_lo;
+                v2 &= keep_lo;
+                v1 &= keep_hi;
+                v3 &= keep_hi;
+                mma_16816<kFp8>(o[2 * j], pa, v0, v1);
+                mma_16816<kFp8>(o[2 * j + 1], pa, v2, v3);
+            }
+        }
+        __syncwarp();
+        // refill this stage with the block NSTAGE ahead
+        const int kn = k + C::kStages;
+        const int pb = __shfl_sync(0xFFFFFFFFu, phys, kn & 31);
+        if (lane == 0 && kn < my_n) {
+            fence_proxy_async_smem();
+            uint8_t* kdst = wbase + st * C::kStageBytes;
+            uint8_t* vdst = kdst + C::kTileBytes;
+            mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+                tma_load_4d(kdst + bx * C::kBoxBytes, &kmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
+                tma_load_4d(vdst + bx * C::kBoxBytes, &vmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
+            }
+        }
+    }
+    if (failed) {
+        // drain the loads still in flight (bounded), then report
+        for (int kk = k + 1; kk < min(my_n, k + C::kStages); ++kk)
+            (void)mbar_wait(&bars[warp][kk % C::kStages], (kk / C::kStages) & 1);
+        if (lane == 0) {
+            flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            atomicOr(&s_flag, 1);
+        }
+    }
+
+    // ---- combine the 4 warps of the CTA
+    l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], 1);
+    l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], 2);
+    l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], 1);
+    l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], 2);
+    __syncthreads();  // every warp is done with its stage buffers
+    float* comb = reinterpret_cast<float*>(smem);
+    {
+        float* cw = comb + warp * 16 * C::kCombStride;
+#pragma unroll
+        for (int nt = 0; nt < NTILES; ++nt) {
+            const int col = nt * 8 + 2 * tig;
+            *reinterpret_cast<float2*>(cw + g0 * C::kCombStride + col) = make_float2(o[nt][0], o[nt][1]);
+            *reinterpret_cast<float2*>(cw + (g0 + 8) * C::kCombStride + col) =
+                make_float2(o[nt][2], o[nt][3]);
+        }
+        if (tig == 0) {
+            s_m[warp][g0] = m_run[0];
+            s_m[warp][g0 + 8] = m_run[1];
+            s_l[warp][g0] = l_run[0];
+            s_l[warp][g0 + 8] = l_run[1];
+        }
+    }
+    __syncthreads();
+    const bool cta_failed = s_flag != 0;
+    const float vs = kFp8 ? a.v_scale[kvh] : 1.f;
+    const size_t pair = static_cast<size_t>(seq) * a.hkv + kvh;
+    if (!cta_failed) {
+        for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+            const int r = idx / D;
+            const int d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][r]);
+            float L = 0.f, acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
+                L += f * s_l[w][r];
+                acc += f * comb[(w * 16 + r) * C::kCombStride + d];
+            }
+            const float ov = acc / L * vs;
+            const float lse = (M + __log2f(L)) * 0.6931471805599453f;
+            if (nsplit == 1) {
+                static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d] =
+                    __float2bfloat16_rn(ov);
+                if (a.lse_out && d == 0) a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] = lse;
+            } else {
+                const size_t prow = (pair * a.max_splits + split) * G + r;
+                a.part_o[prow * D + d] = ov;
+                if (d == 0) a.part_lse[prow] = lse;
+            }
+        }
+    }
+    if (nsplit == 1) return;
+
+    // ---- ticket: the last chunk of this (sequence, KV head) merges
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_flag = static_cast<int>(atomicAdd(&a.counters[pair], 1u));
+    __syncthreads();
+    if (s_flag != nsplit - 1) return;
+    __threadfence();
+    // weights per (split, row) in shared memory: wts[split][16], then M, W per row
+    float* wts = reinterpret_cast<float*>(smem);
+    float* rowM = wts + a.max_splits * 16;
+    float* rowW = rowM + 16;
+    {
+        const int r = threadIdx.x >> 3;  // 16 rows x 8 threads
+        const int sub = threadIdx.x & 7;
+        float M = -INFINITY;
+        if (r < G)
+            for (int i = sub; i < nsplit; i += 8)
+                M = fmaxf(M, __ldcg(a.part_lse + (pair * a.max_splits + i) * G + r));
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+        float W = 0.f;
+        if (r < G)
+            for (int i = sub; i < nsplit; i += 8) {
+                const float l = __ldcg(a.part_lse + (pair * a.max_splits + i) * G + r);
+                const float wv = l == -INFINITY ? 0.f : __expf(l - M);
+                wts[i * 16 + r] = wv;
+                W += wv;
+            }
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) W += __shfl_xor_sync(0xFFFFFFFFu, W, off);
+        if (sub == 0) {
+            rowM[r] = M;
+            rowW[r] = W;
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+        const int r = idx / D;
+        const int d = idx % D;
+        float acc = 0.f;
+        for (int i = 0; i < nsplit; ++i) {
+            const float wv = wts[i * 16 + r];
+            if (wv != 0.f) acc += wv * __ldcg(a.part_o + ((pair * a.max_splits + i) * G + r) * D + d);
+        }
+        const float W = rowW[r];
+        static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d] =
+            __float2bfloat16_rn(W > 0.f ? acc / W : 0.f);
+        if (a.lse_out && d == 0)
+            a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] =
+                W > 0.f ? rowM[r] + __logf(W) : -INFINITY;
+    }
+    if (threadIdx.x == 0) a.counters[pair] = 0u;
+}
+
+template <int D, bool kFp8>
+cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+    using C = DecodeCfg<D, kFp8>;
+    static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+    auto kern = decode_kernel<D, kFp8>;
+    // The shared-memory opt-in is a per-device function attribute: set it on
+    // the first launch on each device (never inside a stream capture).
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid(a.max_splits, a.hkv, a.num_seqs);
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(a, kmap, vmap);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_smem_bytes(int d, int fp8) {
+    if (d == 64) return fp8 ? DecodeCfg<64, true>::kSmemBytes : DecodeCfg<64, false>::kSmemBytes;
+    return fp8 ? DecodeCfg<128, true>::kSmemBytes : DecodeCfg<128, false>::kSmemBytes;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream) {
+    if (a.d == 64) {
+        return a.fp8 ? launch_decode_t<64, true>(a, kmap, vmap, stream)
+                     : launch_decode_t<64, false>(a, kmap, vmap, stream);
+    }
+    return a.fp8 ? launch_decode_t<128, true>(a, kmap, vmap, stream)
+                 : launch_decode_t<128, false>(a, kmap, vmap, stream);
+}
+
+}  // namespace pkv

@@ -1,0 +1,99 @@
+// internal.h -- host-side interface between the C ABI layer (api.cu) and the
+// kernel translation units.  Launchers return cudaGetLastError() of their
+// launch; argument validation happens in api.cu before they are called.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct AppendArgs {
+    void* k_cache;
+    void* v_cache;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* block_tables;
+    const int32_t* token_to_seq;
+    const int32_t* positions;
+    const void* k_new;
+    const void* v_new;
+    void* q;  // nullable
+    const float* cos_sin;  // nullable
+    int32_t num_seqs, num_tokens, hq, hkv, d, mbps, max_pos;
+    int64_t num_blocks;
+    int32_t fp8;
+    uint32_t* err;
+};
+cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream);
+
+struct GatherArgs {
+    const void* cache;
+    const int32_t* block_tables;
+    const int32_t* lens;
+    const int32_t* cu_lens;
+    void* out;
+    int32_t num_seqs, hkv, row_bytes, mbps;
+    int64_t total_tokens, num_blocks;
+    uint32_t* err;
+};
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
+
+struct MergeArgs {
+    const float* o_parts;
+    const float* lse_parts;
+    void* out;
+    float* lse_out;
+    int32_t num_parts, num_rows, num_heads, head_dim;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+    const void* q;
+    void* out;
+    float* lse_out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const float* k_scale;
+    const float* v_scale;
+    uint32_t* counters;   // [num_seqs * hkv], zero on entry and exit
+    float* part_lse;      // [num_seqs * hkv * max_splits * group]
+    float* part_o;        // [num_seqs * hkv * max_splits * group * d]
+    uint32_t* err;
+    int32_t num_seqs, hq, hkv, group, d, mbps, window, chunk_blocks, max_splits, fp8;
+    int32_t max_ctx;  // host bound on context_lens: the split plan covers up to it
+    int64_t num_blocks;
+    float sm_scale;
+};
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream);
+
+struct PrefillArgs {
+    const void* q;
+    void* out;
+    float* lse_out;
+    const int32_t* qo_indptr;
+    const int32_t* kv_lens;
+    const int32_t* block_tables;
+    uint32_t* err;
+    int32_t num_seqs, hq, hkv, group, d, mbps, causal, window, max_qtiles, q_tile;
+    int32_t total_q;  // rows of q / out
+    int64_t num_blocks;
+    float sm_scale;
+};
+// Query tokens per CTA tile for a group size (rows = tokens * group <= 64).
+int prefill_q_tile(int group);
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream);
+
+// Tensor-map box shape used by the attention kernels for a pool:
+// innermost box extent in elements, and the swizzle.
+struct BoxShape {
+    int inner;  // elements per box row
+    int boxes;  // boxes per (block, head) tile
+    int swizzle128;
+};
+BoxShape kv_box_shape(int head_dim, int fp8);
+
+}  // namespace pkv

@@ -252,15 +252,18 @@ def make_decode_batch(spec: DecodeSpec, device="cpu", pool=None, free_blocks=Non
 
 def make_decode_instances(spec: DecodeSpec, n: int, device="cpu"):
     """``n`` decode batches of one shape over disjoint regions of one pool
-    (each instance draws its own lengths, tables and queries)."""
-    first = make_decode_batch(spec, device)
+    (each instance draws its own lengths, tables and queries); every table
+    has ceil(ctx_hi / block_size) columns."""
+    mbps = (spec.ctx_hi + spec.block_size - 1) // spec.block_size
+    first = make_decode_batch(spec, device, max_blocks_per_seq=mbps)
     pool = (first.k_cache, first.v_cache, first.k_scale, first.v_scale)
     used = set(first.tables_host[first.tables_host >= 0].tolist())
     out = [first]
     for i in range(1, n):
         free = np.array([b for b in range(first.k_cache.shape[0]) if b not in used],
                         dtype=np.int32)
-        inst = make_decode_batch(spec, device, pool=pool, free_blocks=free, seed_offset=1000 * i)
+        inst = make_decode_batch(spec, device, pool=pool, free_blocks=free, seed_offset=1000 * i,
+                                 max_blocks_per_seq=mbps)
         used |= set(inst.tables_host[inst.tables_host >= 0].tolist())
         out.append(inst)
     return out

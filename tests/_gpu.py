@@ -1,0 +1,100 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+the oracle on host copies of the same seeded bytes, and compare."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_attention_21_gb300 as pkv
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+NTHREADS = max(1, min(32, os.cpu_count() or 1))
+
+# The attention tolerance: bf16 inputs, fp32 accumulation, bf16 output.
+MAX_ERR = 1e-2
+MEAN_ERR = 1e-3
+LSE_ERR = 2e-3
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().numpy().view(np.uint8)
+
+
+def pool_np(t: torch.Tensor) -> np.ndarray:
+    return u8(t) if t.dtype == torch.uint8 else u16(t)
+
+
+def desc_for(spec, k_cache, tables) -> pkv.CacheDesc:
+    return pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                         head_dim=spec.head_dim, num_blocks=k_cache.shape[0],
+                         max_blocks_per_seq=tables.shape[1], kv_dtype=spec.kv_dtype)
+
+
+def on_device(batch):
+    """Move a DecodeBatch's tensors to the GPU (returns a dict)."""
+    f = lambda t: None if t is None else t.to(DEV)
+    return dict(q=f(batch.q), k_cache=f(batch.k_cache), v_cache=f(batch.v_cache),
+                k_scale=f(batch.k_scale), v_scale=f(batch.v_scale),
+                block_tables=f(batch.block_tables), context_lens=f(batch.context_lens),
+                k_new=f(batch.k_new), v_new=f(batch.v_new))
+
+
+def gpu_decode(desc, d, max_ctx, sm_scale, window=-1, chunk=0):
+    B, hq, D = d["q"].shape
+    ws_size = pkv.pkv_decode_workspace_size(desc, B, max_ctx, window, chunk)
+    ws = torch.zeros(max(ws_size, 256), dtype=torch.uint8, device=DEV)
+    out = torch.full_like(d["q"], float("nan"))
+    lse = torch.full((B, hq), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.pkv_decode_attention(desc, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], max_ctx, sm_scale, out, lse, ws, window=window,
+                             chunk_blocks=chunk, k_scale=d["k_scale"], v_scale=d["v_scale"])
+    torch.cuda.synchronize()
+    return out, lse, ws
+
+
+def oracle_decode(spec, q_bits, k_np, v_np, tables, lens, window=-1, k_scale=None, v_scale=None):
+    B = len(lens)
+    return oracle.paged_attention(q=q_bits, k_cache=k_np, v_cache=v_np, block_tables=tables,
+                                  qo_indptr=np.arange(B + 1), kv_lens=lens,
+                                  num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                                  sm_scale=spec.sm_scale, causal=True, window=window,
+                                  kv_dtype=1 if spec.kv_dtype == "fp8_e4m3" else 0,
+                                  k_scale=k_scale, v_scale=v_scale, nthreads=NTHREADS)
+
+
+def compact_pool(k_cache, v_cache, tables, seqs):
+    """Host copy of only the blocks the chosen sequences use, with their
+    tables renumbered (test plumbing: torch indexing, no method arithmetic)."""
+    tabs = tables[seqs]
+    ids = np.unique(tabs[tabs >= 0])
+    remap = np.full(int(k_cache.shape[0]), -1, dtype=np.int64)
+    remap[ids] = np.arange(len(ids))
+    idx = torch.from_numpy(ids.astype(np.int64)).to(k_cache.device)
+    k = pool_np(k_cache.index_select(0, idx))
+    v = pool_np(v_cache.index_select(0, idx))
+    new_tabs = np.where(tabs >= 0, remap[np.maximum(tabs, 0)], -1).astype(np.int32)
+    return k, v, new_tabs
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, what: str, max_err=MAX_ERR, mean_err=MEAN_ERR):
+    g = got.float().cpu().numpy()
+    assert np.all(np.isfinite(g)), "%s: non-finite output" % what
+    err = np.abs(g - ref)
+    assert err.max() <= max_err and err.mean() <= mean_err, \
+        "%s: max|err| %.3g (<= %g), mean|err| %.3g (<= %g)" % (what, err.max(), max_err,
+                                                               err.mean(), mean_err)
+    return float(err.max()), float(err.mean())
+
+
+def assert_lse_close(got: torch.Tensor, ref: np.ndarray, what: str):
+    g = got.float().cpu().numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(g), fin), "%s: lse finiteness differs" % what
+    assert np.abs(g[fin] - ref[fin]).max() <= LSE_ERR, "%s: lse" % what

@@ -1,0 +1,177 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and its host-side logic (RoPE table, pool size, planner, argument
+validation) behaves as specified.  Validation failures return before any CUDA
+call, so they are testable here."""
+import ctypes
+import json
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_attention_21_gb300 as pkv
+from paged_kv_attention_21_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return pkv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path_entry_points():
+    names = declared_functions()
+    for n in ("pkv_append_rope", "pkv_decode_attention", "pkv_prefill_attention_ragged",
+              "pkv_merge_states", "pkv_gather_kv", "pkv_decode_workspace_size",
+              "pkv_prefill_workspace_size", "pkv_rope_cos_sin_table", "pkv_last_error",
+              "pkv_decode_plan", "pkv_cache_bytes", "pkv_device_errors"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(pkv.library_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_rope_table_equals_oracle_bit_for_bit(lib):
+    for theta, dim, n in ((1e6, 128, 4096), (1e4, 64, 1000), (5e5, 128, 100)):
+        a = pkv.pkv_rope_cos_sin_table(theta, dim, n)
+        b = oracle.rope_table(theta, dim, n)
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_pool_bytes_match_the_printed_kv_pool_size(lib):
+    g = json.load(open(os.path.join(GOLDEN, "kv_pool_bytes.json")))
+    for dtype, printed in ((pkv.KV_BF16, g["bf16_gb_printed"]), (pkv.KV_FP8_E4M3,
+                                                                  g["fp8_gb_printed"])):
+        d = pkv.make_desc(num_q_heads=16, num_kv_heads=g["num_kv_heads"], head_dim=g["head_dim"],
+                          num_blocks=g["num_blocks"], max_blocks_per_seq=1, kv_dtype=dtype,
+                          block_size=g["block_size"])
+        total = pkv.pkv_cache_bytes(d) * 2 * g["num_layers"]  # K and V, every layer
+        assert abs(total / 1e9 - printed) <= g["printed_precision_gb"]
+
+
+def _desc(**kw):
+    base = dict(num_q_heads=16, num_kv_heads=2, head_dim=128, num_blocks=1000,
+                max_blocks_per_seq=256)
+    base.update(kw)
+    return pkv.make_desc(**base)
+
+
+def test_invalid_arguments_return_status_before_any_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: validation fails first
+    cases = [
+        (None, pkv.PkvError, 1),
+    ]
+    # null desc
+    st = lib.pkv_decode_attention(None, fake, fake, fake, None, None, fake, fake, 1, 10, 0.1, -1,
+                                  0, fake, None, None, 0, None)
+    assert st == 1 and "desc" in pkv.pkv_last_error()
+    bad = [
+        (_desc(num_q_heads=15), 1, "multiple"),
+        (_desc(head_dim=96), 2, "head_dim"),
+        (_desc(num_q_heads=64, num_kv_heads=2), 2, "group"),
+        (_desc(block_size=32), 2, "block_size"),
+        (_desc(kv_dtype=7), 2, "kv_dtype"),
+        (_desc(num_blocks=0), 1, "num_blocks"),
+    ]
+    for d, code, word in bad:
+        st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,
+                                      10, 0.1, -1, 0, fake, None, None, 0, None)
+        assert st == code, (word, st)
+        assert word in pkv.pkv_last_error()
+    d = _desc()
+    # context longer than the table can hold
+    st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,
+                                  256 * 16 + 1, 0.1, -1, 0, fake, None, None, 0, None)
+    assert st == 1 and "max_context_len" in pkv.pkv_last_error()
+    # e4m3 without scales
+    d8 = _desc(kv_dtype=pkv.KV_FP8_E4M3)
+    st = lib.pkv_decode_attention(ctypes.byref(d8), fake, fake, fake, None, None, fake, fake, 1,
+                                  10, 0.1, -1, 0, fake, None, None, 0, None)
+    assert st == 1 and "scale" in pkv.pkv_last_error()
+    # null pointers
+    st = lib.pkv_decode_attention(ctypes.byref(d), None, fake, fake, None, None, fake, fake, 1,
+                                  10, 0.1, -1, 0, fake, None, None, 0, None)
+    assert st == 1
+    # misaligned q
+    st = lib.pkv_decode_attention(ctypes.byref(d), P(0x10002), fake, fake, None, None, fake, fake,
+                                  1, 10, 0.1, -1, 0, fake, None, None, 0, None)
+    assert st == 1 and "aligned" in pkv.pkv_last_error()
+    # bad sm_scale
+    st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,
+                                  10, float("nan"), -1, 0, fake, None, None, 0, None)
+    assert st == 1
+    # zero sequences: a no-op, OK
+    st = lib.pkv_decode_attention(ctypes.byref(d), None, None, None, None, None, None, None, 0,
+                                  10, 0.1, -1, 0, None, None, None, 0, None)
+    assert st == 0
+    # prefill: e4m3 pools unsupported; kv_len < q_len rejected
+    st = lib.pkv_prefill_attention_ragged(ctypes.byref(d8), fake, fake, fake, fake, None, None,
+                                          fake, fake, 1, 4, None, None, 0.1, 1, -1, fake, None,
+                                          None, 0, None)
+    assert st == 2
+    qo = np.array([0, 4], np.int32)
+    kl = np.array([3], np.int32)
+    st = lib.pkv_prefill_attention_ragged(ctypes.byref(d), fake, fake, fake, fake, None, None,
+                                          fake, fake, 1, 4, qo.ctypes.data_as(P),
+                                          kl.ctypes.data_as(P), 0.1, 1, -1, fake, None, None, 0,
+                                          None)
+    assert st == 1 and "kv_len" in pkv.pkv_last_error()
+    # append and merge
+    st = lib.pkv_append_rope(ctypes.byref(d), None, fake, None, None, fake, 1, fake, fake, 1, fake,
+                             fake, None, None, 0, None)
+    assert st == 1
+    st = lib.pkv_merge_states(None, None, 2, 4, 4, 64, fake, None, None)
+    assert st == 1
+    st = lib.pkv_rope_cos_sin_table(1e4, 63, 10, fake)
+    assert st == 1
+
+
+def test_planner_fills_the_gpu_and_respects_limits(lib):
+    sms = 152
+    # (Hq, Hkv, D, dtype, B, max_ctx, window)
+    shapes = [(8, 2, 64, 0, 4, 255, -1), (16, 2, 128, 0, 64, 4096, -1),
+              (32, 8, 128, 0, 256, 768, -1), (32, 8, 128, 0, 120, 32768, -1),
+              (64, 8, 64, 1, 128, 16384, -1), (64, 8, 64, 1, 128, 16384, 128),
+              (16, 2, 128, 0, 1, 1 << 19, -1)]
+    for hq, hkv, d, dt, B, ctx, win in shapes:
+        desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=10,
+                             max_blocks_per_seq=(ctx + 15) // 16, kv_dtype=dt)
+        chunk, splits = pkv.pkv_decode_plan(desc, B, ctx, win, sms)
+        vis_blocks = (ctx + 15) // 16 if win <= 0 else min((ctx + 15) // 16, (win + 14) // 16 + 1)
+        assert 1 <= chunk <= 128
+        assert splits == math.ceil(vis_blocks / chunk) and splits <= 512
+        if B * hkv * vis_blocks >= 16 * sms * 8:
+            # large batches: enough CTAs for several waves, none smaller than 16 blocks
+            assert B * hkv * splits >= sms and chunk >= 16
+    # a window never needs more blocks than it can touch
+    desc = pkv.make_desc(num_q_heads=64, num_kv_heads=8, head_dim=64, num_blocks=10,
+                         max_blocks_per_seq=1024, kv_dtype=1)
+    assert pkv.pkv_decode_plan(desc, 128, 16384, 128, sms) == (9, 1)
+
+
+def test_workspace_size_layout(lib):
+    d = _desc()
+    B, ctx = 10, 1000  # 63 blocks
+    assert pkv.pkv_decode_workspace_size(d, B, ctx, -1, 64) == 0  # one split: none needed
+    sz = pkv.pkv_decode_workspace_size(d, B, ctx, -1, 16)  # 4 splits
+    pairs, G, D, S = B * 2, 8, 128, 4
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert sz == a256(pairs * 4) + a256(pairs * S * G * 4) + a256(pairs * S * G * D * 4)
+    assert pkv.pkv_decode_workspace_size(d, B, ctx, -1, 129) == 0  # chunk > 128 rejected
