@@ -447,12 +447,12 @@ def oracle_sample(W, seconds, nthreads):
     vs = None if b.v_scale is None else b.v_scale.cpu().numpy()
     kvd = 1 if spec.kv_dtype == "fp8_e4m3" else 0
     elem = 1 if kvd else 2
-    order = np.argsort(b.lens_host)  # start short, grow
+    order = np.argsort(b.lens_host)  # start short, grow; wrap around until the time is spent
     done_bytes, done_s, seqs_done = 0, 0.0, 0
     batch = 1
     pos = 0
-    while done_s < seconds and pos < len(order):
-        seqs = order[pos:pos + batch].tolist()
+    while done_s < seconds:
+        seqs = [int(order[(pos + j) % len(order)]) for j in range(batch)]
         k, v, tabs = host_pool(seqs)
         lens = b.lens_host[seqs]
         t0 = time.perf_counter()
@@ -465,9 +465,10 @@ def oracle_sample(W, seconds, nthreads):
         done_bytes += int(lens.sum()) * spec.num_kv_heads * spec.head_dim * elem * 2
         seqs_done += len(seqs)
         pos += batch
-        batch *= 2
-    desc = "%d of %d sequences of one batch (all %d query heads), %.1f s" % (
-        seqs_done, spec.batch, spec.num_q_heads, done_s)
+        batch = min(batch * 2, len(order))
+    desc = ("%d sequence passes over one %d-sequence batch (all %d query heads, "
+            "host copies of their blocks), %.1f s of oracle time" % (
+                seqs_done, spec.batch, spec.num_q_heads, done_s))
     return done_bytes / done_s / 1e9, desc, nthreads
 
 

@@ -446,18 +446,51 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
-        const int r = idx / D;
-        const int d = idx % D;
-        float acc = 0.f;
-        for (int i = 0; i < nsplit; ++i) {
-            const float wv = wts[i * 16 + r];
-            if (wv != 0.f) acc += wv * __ldcg(a.part_o + ((pair * a.max_splits + i) * G + r) * D + d);
+    // Each thread owns float4 slots (row, 4 columns); the loads of all splits
+    // are independent, four in flight per slot, so the merge costs a few L2
+    // round trips rather than one per split.
+    constexpr int kSlotsPerRow = D / 4;
+    const float4* po = reinterpret_cast<const float4*>(a.part_o);
+    for (int slot = threadIdx.x; slot < G * kSlotsPerRow; slot += kThreads) {
+        const int r = slot / kSlotsPerRow;
+        const int c4 = slot % kSlotsPerRow;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int i = 0;
+        for (; i + 4 <= nsplit; i += 4) {
+            float4 v[4];
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                w[u] = wts[(i + u) * 16 + r];
+                v[u] = __ldcg(po + ((pair * a.max_splits + i + u) * G + r) * kSlotsPerRow + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (w[u] != 0.f) {
+                    acc.x += w[u] * v[u].x;
+                    acc.y += w[u] * v[u].y;
+                    acc.z += w[u] * v[u].z;
+                    acc.w += w[u] * v[u].w;
+                }
+            }
+        }
+        for (; i < nsplit; ++i) {
+            const float w = wts[i * 16 + r];
+            const float4 v = __ldcg(po + ((pair * a.max_splits + i) * G + r) * kSlotsPerRow + c4);
+            if (w != 0.f) {
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
         }
         const float W = rowW[r];
-        static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d] =
-            __float2bfloat16_rn(W > 0.f ? acc / W : 0.f);
-        if (a.lse_out && d == 0)
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
+                            (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + c4 * 4;
+        *reinterpret_cast<uint2*>(ob) =
+            make_uint2(pack2<false>(acc.x * inv, acc.y * inv), pack2<false>(acc.z * inv, acc.w * inv));
+        if (a.lse_out && c4 == 0)
             a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] =
                 W > 0.f ? rowM[r] + __logf(W) : -INFINITY;
     }

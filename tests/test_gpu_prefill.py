@@ -105,11 +105,12 @@ def test_shared_prefix_blocks_equal_private_copies():
     spec = _small(num_chunks=2)
     pb = wl.make_prefill_batch(spec, "cpu", q_lens=[50, 50], prefixes=[400, 400])
     # sequence 1 shares sequence 0's 25 full prefix blocks; give it private copies
-    kc, vc = pb.k_cache.clone(), pb.v_cache.clone()
-    tabs = pb.tables_host.copy()
-    used = set(tabs[tabs >= 0].tolist())
-    free = [i for i in range(kc.shape[0]) if i not in used]
     shared = 400 // 16
+    nb = pb.k_cache.shape[0]
+    kc = torch.cat([pb.k_cache, torch.zeros_like(pb.k_cache[:shared])])
+    vc = torch.cat([pb.v_cache, torch.zeros_like(pb.v_cache[:shared])])
+    tabs = pb.tables_host.copy()
+    free = list(range(nb, nb + shared))  # fresh blocks appended to the pool
     assert np.array_equal(tabs[0, :shared], tabs[1, :shared])
     for j in range(shared):
         kc[free[j]] = kc[tabs[1, j]]
@@ -128,7 +129,7 @@ def test_decode_equals_one_token_prefill():
                          max_blocks_per_seq=b.tables_host.shape[1])
     d = dict(q=b.q.to(DEV), k_cache=b.k_cache.to(DEV), v_cache=b.v_cache.to(DEV), k_scale=None,
              v_scale=None, block_tables=b.block_tables.to(DEV), context_lens=b.context_lens.to(DEV))
-    dec, dec_lse = gpu_decode(desc, d, b.max_context_len, spec.sm_scale)
+    dec, dec_lse, _ = gpu_decode(desc, d, b.max_context_len, spec.sm_scale)
     pspec = wl.PrefillSpec("one-token", num_chunks=12, chunk_len=1, prefix_lo=0, prefix_hi=0,
                            num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
                            head_dim=spec.head_dim, seed=0)
