@@ -84,23 +84,25 @@ def compact_pool(k_cache, v_cache, tables, seqs):
 
 
 def assert_close(got: torch.Tensor, ref: np.ndarray, what: str, max_err=MAX_ERR, mean_err=MEAN_ERR):
-    """The kernel's bf16 output against the oracle's fp32 result rounded to
-    bf16 by the oracle's own RNE encoder -- the output format of the API -- so
-    the bounds measure the computation, not the final rounding (which alone
-    averages ~1e-3 on O(1) outputs).  The raw fp32 difference is held to the
-    max bound plus half a bf16 ulp of the reference."""
+    """Attention tolerance for a bf16 output.  The kernel's result is bf16 (the
+    API's output format), the oracle's fp32, so the comparison separates the
+    computation from the final rounding:
+      * max: |out - ref| <= 1e-2 + half a bf16 ulp of ref (2^-8 |ref|), the
+        rounding of the output format itself;
+      * mean: |out - bf16(ref)| averaged <= 1e-3, with bf16(ref) the oracle's
+        result rounded by the oracle's own RNE encoder (the rounding alone
+        averages ~1e-3 on O(1) outputs)."""
     g = got.float().cpu().numpy()
     assert np.all(np.isfinite(g)), "%s: non-finite output" % what
     ref = np.asarray(ref, dtype=np.float32)
+    raw = np.abs(g - ref)
+    bound = max_err + np.abs(ref) * 2.0 ** -8
+    assert np.all(raw <= bound), "%s: max|err| %.3g beyond 1e-2 + half ulp (worst excess %.3g)" % (
+        what, raw.max(), (raw - bound).max())
     ref_b = oracle.f32_from_bf16(oracle.bf16_from_f32(ref))
     err = np.abs(g - ref_b)
-    assert err.max() <= max_err and err.mean() <= mean_err, \
-        "%s: max|err| %.3g (<= %g), mean|err| %.3g (<= %g)" % (what, err.max(), max_err,
-                                                               err.mean(), mean_err)
-    raw = np.abs(g - ref)
-    assert np.all(raw <= max_err + np.abs(ref) * 2.0 ** -9), "%s: raw max|err| %.3g" % (
-        what, raw.max())
-    return float(err.max()), float(err.mean())
+    assert err.mean() <= mean_err, "%s: mean|err| %.3g (<= %g)" % (what, err.mean(), mean_err)
+    return float(raw.max()), float(err.mean())
 
 
 def assert_lse_close(got: torch.Tensor, ref: np.ndarray, what: str):
