@@ -213,6 +213,36 @@ pkv_status pkv_merge_states(const float *o_parts, const float *lse_parts, int32_
                             int32_t num_rows, int32_t num_heads, int32_t head_dim, void *out,
                             float *lse_out, pkv_stream_t stream);
 
+/* ---- decode with no workspace argument (no counterpart on the pages) ---
+ * The same computation as pkv_decode_attention, for callers that cannot
+ * allocate device memory at the point of the call -- for example code that
+ * runs inside an allocator's own callbacks, under a framework that owns and
+ * locks the memory pool, or in a plugin that is handed only the tensors it
+ * reads and writes -- and so cannot pass the decode workspace.  Instead of a
+ * caller workspace it uses one fixed scratch array of 16 MiB (256-byte
+ * aligned) that lives in the library's device memory: every GPU that loads
+ * libpkv holds its own copy until the process exits.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - A batch whose split plan needs more than 16 MiB of scratch (see
+ *     pkv_decode_workspace_size) is rejected with PKV_ERR_WORKSPACE; pass a
+ *     larger chunk_blocks, or use pkv_decode_attention.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     the call clears the merge tickets it needs on `stream` before the
+ *     kernel.  Calls that overlap on the GPU (different streams, or several
+ *     host threads) race on the array: serialise them.
+ * Arguments are those of pkv_decode_attention without workspace and
+ * workspace_bytes. */
+pkv_status pkv_decode_attention_static(const pkv_cache_desc *desc, const void *q,
+                                       const void *k_cache, const void *v_cache,
+                                       const float *k_scale, const float *v_scale,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int32_t num_seqs, int32_t max_context_len, float sm_scale,
+                                       int32_t window, int32_t chunk_blocks, void *out,
+                                       float *lse_out, pkv_stream_t stream);
+
 /* ---- diagnostics --------------------------------------------------------- */
 
 /* Message for the last non-OK status on this thread ("" if none). */

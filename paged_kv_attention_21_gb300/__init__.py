@@ -89,6 +89,8 @@ def load_library():
                                                             P, P, f32, i32, i32, P, P, P,
                                                             ctypes.c_size_t, P]),
             "pkv_prefill_workspace_size": (ctypes.c_size_t, [D, i32, i32]),
+            "pkv_decode_attention_static": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32,
+                                                           i32, i32, P, P, P]),
             "pkv_merge_states": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, P, P]),
             "pkv_last_error": (ctypes.c_char_p, []),
             "pkv_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32]),
@@ -184,6 +186,17 @@ def pkv_decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, 
         _ptr(block_tables), _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len),
         float(sm_scale), int(window), int(chunk_blocks), _ptr(out), _ptr(lse), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def pkv_decode_attention_static(desc, q, k_cache, v_cache, block_tables, context_lens,
+                                max_context_len, sm_scale, out, lse=None, window=-1,
+                                chunk_blocks=0, k_scale=None, v_scale=None, stream=None):
+    """Decode for callers that cannot allocate: no workspace argument, the
+    library's fixed 16 MiB device scratch instead (see include/pkv.h)."""
+    _check(load_library().pkv_decode_attention_static(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len),
+        float(sm_scale), int(window), int(chunk_blocks), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def pkv_prefill_workspace_size(desc, num_seqs, total_q_tokens) -> int:

@@ -600,3 +600,124 @@ pkv_status pkv_device_errors(uint32_t* flags_out, int32_t reset) {
 }
 
 }  // extern "C"
+
+// ============================================ decode without allocation ==
+//
+// Some callers cannot allocate device memory when they call in: code that
+// runs where cudaMalloc is forbidden or unsafe (inside a custom allocator's
+// own callbacks, in a process whose memory pool is locked by its framework,
+// or in a plugin that is handed only the tensors it reads and writes), so
+// they cannot provide the decode workspace.  This entry point uses a fixed
+// scratch array that lives in the library's own device memory instead.
+
+// Fixed scratch for pkv_decode_attention_static: 16 MiB, 256-byte aligned.
+// Every GPU that loads the library holds one copy of it until the process
+// exits.  Every call shares it and it keeps the last call's contents.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) uint8_t g_pkv_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+std::mutex g_static_mutex;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.  In host code the array's name is
+// only a host-side stand-in, so the address must come from the runtime.
+pkv_status static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_pkv_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static decode scratch)");
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_decode_attention_static(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float sm_scale,
+    int32_t window, int32_t chunk_blocks, void* out, float* lse_out, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_seqs > 65535)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
+    if (max_context_len < 1 || max_context_len > desc->max_blocks_per_seq * desc->block_size)
+        return fail(PKV_ERR_INVALID_ARG, "max_context_len %d outside [1, %d]", max_context_len,
+                    desc->max_blocks_per_seq * desc->block_size);
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
+    uint32_t* err = nullptr;
+    int sms = 0;
+    st = device_state(&err, &sms);
+    if (st != PKV_OK) return st;
+    int chunk = 0, splits = 0;
+    st = plan_decode(desc, num_seqs, max_context_len, window, sms, chunk_blocks, &chunk, &splits);
+    if (st != PKV_OK) return st;
+    const DecodeWs ws = decode_ws_layout(desc, num_seqs, splits);
+    if (ws.total > kStaticScratchBytes)
+        return fail(PKV_ERR_WORKSPACE,
+                    "this batch needs %zu bytes of decode scratch, more than the %zu-byte static "
+                    "array; use pkv_decode_attention with a workspace, or a larger chunk_blocks",
+                    ws.total, kStaticScratchBytes);
+    void* scratch = nullptr;
+    st = static_scratch(&scratch);
+    if (st != PKV_OK) return st;
+    CUtensorMap kmap, vmap;
+    st = pool_map(k_cache, desc, &kmap);
+    if (st != PKV_OK) return st;
+    st = pool_map(v_cache, desc, &vmap);
+    if (st != PKV_OK) return st;
+    uint8_t* wsb = static_cast<uint8_t*>(scratch);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ws.total > 0) {
+        // the tickets must start at zero; the array keeps whatever the last call left
+        const size_t pairs = size_t(num_seqs) * desc->num_kv_heads;
+        cudaError_t e = cudaMemsetAsync(wsb + ws.counters, 0, pairs * sizeof(uint32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "clear static decode tickets");
+    }
+    pkv::DecodeArgs a{};
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.counters = ws.total ? reinterpret_cast<uint32_t*>(wsb + ws.counters) : nullptr;
+    a.part_lse = ws.total ? reinterpret_cast<float*>(wsb + ws.lse) : nullptr;
+    a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;
+    a.err = err;
+    a.num_seqs = num_seqs;
+    a.hq = desc->num_q_heads;
+    a.hkv = desc->num_kv_heads;
+    a.group = desc->num_q_heads / desc->num_kv_heads;
+    a.d = desc->head_dim;
+    a.mbps = desc->max_blocks_per_seq;
+    a.window = window;
+    a.chunk_blocks = chunk;
+    a.max_splits = splits;
+    a.max_ctx = max_context_len;
+    a.fp8 = fp8 ? 1 : 0;
+    a.num_blocks = desc->num_blocks;
+    a.sm_scale = sm_scale;
+    cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return PKV_OK;
+}
