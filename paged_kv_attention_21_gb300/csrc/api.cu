@@ -163,7 +163,7 @@ pkv_status pool_map(const void* pool, const pkv_cache_desc* desc, CUtensorMap* o
 
 constexpr int kMaxGroup = 16;
 constexpr int kMaxChunk = 128;   // blocks per decode CTA (32 per warp)
-constexpr int kMinChunk = 16;
+constexpr int kMinChunk = 32;
 constexpr int kMaxSplits = 512;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -202,8 +202,9 @@ int max_visible_blocks(int max_ctx, int window) {
 }
 
 int resident_ctas(int d, int fp8) {
+    // shared memory bound, and the register bound of ~150 registers x 128 threads
     const int smem = pkv::decode_smem_bytes(d, fp8) + 1024;
-    return std::max(1, std::min(4, (228 * 1024) / smem));
+    return std::max(1, std::min(3, (228 * 1024) / smem));
 }
 
 pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, int window,
@@ -215,12 +216,14 @@ pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, in
             return fail(PKV_ERR_INVALID_ARG, "chunk_blocks %d > %d", chunk_req, kMaxChunk);
         chunk = chunk_req;
     } else {
-        // Ragged batches average about half their longest context; aim for
-        // ~4 waves of resident CTAs over the whole GPU.
+        // Ragged batches average about half their longest context.  Every CTA
+        // pays a fixed start (first TMA round trip) and end (combine, partial
+        // write, ticket), so aim for one wave of resident CTAs: the fewest,
+        // largest chunks that still occupy every slot.
         const double pairs = double(num_seqs) * desc->num_kv_heads;
-        const double est_blocks = pairs * std::max(1.0, 0.6 * mb);
+        const double est_blocks = pairs * std::max(1.0, 0.55 * mb);
         const double target =
-            double(std::max(num_sms, 1)) * resident_ctas(desc->head_dim, desc->kv_dtype) * 4.0;
+            double(std::max(num_sms, 1)) * resident_ctas(desc->head_dim, desc->kv_dtype);
         chunk = int(std::ceil(est_blocks / target));
         chunk = std::max(kMinChunk, std::min(kMaxChunk, chunk));
         chunk = std::max(chunk, (mb + kMaxSplits - 1) / kMaxSplits);  // bound the split count
