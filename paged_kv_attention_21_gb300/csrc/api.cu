@@ -220,10 +220,14 @@ pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, in
         // pays a fixed start (first TMA round trip) and end (combine, partial
         // write, ticket), so aim for one wave of resident CTAs: the fewest,
         // largest chunks that still occupy every slot.
+        // Each pair rounds its last chunk up, adding about half a CTA per pair,
+        // so size chunks to fill the resident slots without spilling into a
+        // second (mostly idle) wave.
         const double pairs = double(num_seqs) * desc->num_kv_heads;
         const double est_blocks = pairs * std::max(1.0, 0.55 * mb);
-        const double target =
+        const double slots =
             double(std::max(num_sms, 1)) * resident_ctas(desc->head_dim, desc->kv_dtype);
+        const double target = std::max(slots - 0.5 * pairs, 0.25 * slots);
         chunk = int(std::ceil(est_blocks / target));
         chunk = std::max(kMinChunk, std::min(kMaxChunk, chunk));
         chunk = std::max(chunk, (mb + kMaxSplits - 1) / kMaxSplits);  // bound the split count

@@ -20,6 +20,8 @@ namespace pkv {
 
 template <int D, bool kFp8>
 __global__ void __launch_bounds__(256) append_rope_kernel(AppendArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int HALF = D / 2;
     constexpr int PPL = HALF / 32;  // 1 for D=64, 2 for D=128
     const int lane = threadIdx.x & 31;
@@ -127,14 +129,15 @@ cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
     const long long blocks = (warps * 32 + threads - 1) / threads;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(blocks));
+    cudaError_t e;
     if (a.d == 64) {
-        if (a.fp8) append_rope_kernel<64, true><<<grid, threads, 0, stream>>>(a);
-        else append_rope_kernel<64, false><<<grid, threads, 0, stream>>>(a);
+        if (a.fp8) e = launch_pdl(append_rope_kernel<64, true>, grid, dim3(threads), 0, stream, a);
+        else e = launch_pdl(append_rope_kernel<64, false>, grid, dim3(threads), 0, stream, a);
     } else {
-        if (a.fp8) append_rope_kernel<128, true><<<grid, threads, 0, stream>>>(a);
-        else append_rope_kernel<128, false><<<grid, threads, 0, stream>>>(a);
+        if (a.fp8) e = launch_pdl(append_rope_kernel<128, true>, grid, dim3(threads), 0, stream, a);
+        else e = launch_pdl(append_rope_kernel<128, false>, grid, dim3(threads), 0, stream, a);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 // --------------------------------------------------------------- gather --
@@ -142,6 +145,8 @@ cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
 // One thread per 16-byte chunk of an output row.
 
 __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int chunks = a.row_bytes / 16;
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long per_token = static_cast<long long>(a.hkv) * chunks;
@@ -181,8 +186,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
     const int threads = 256;
     const long long blocks = (n + threads - 1) / threads;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    gather_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, a);
 }
 
 // ---------------------------------------------------------------- merge --
@@ -192,6 +196,8 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
 //   lse = M + ln sum w_i.   Empty parts (lse = -inf) are skipped.
 
 __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long RH = static_cast<long long>(a.num_rows) * a.num_heads;
@@ -228,8 +234,7 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     const int threads = 256;
     const long long blocks = (warps * 32 + threads - 1) / threads;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, a);
 }
 
 }  // namespace pkv

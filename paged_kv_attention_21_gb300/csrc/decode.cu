@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     __shared__ float s_l[kWarps][16];
     __shared__ int s_flag;
 
+    pdl_wait();
+    pdl_launch_dependents();
     const int split = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
@@ -518,8 +520,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
         attr_set[dev] = true;
     }
     dim3 grid(a.max_splits, a.hkv, a.num_seqs);
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(a, kmap, vmap);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), C::kSmemBytes, stream, a, kmap, vmap);
 }
 
 }  // namespace

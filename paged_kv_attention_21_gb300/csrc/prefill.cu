@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(kPThreads) prefill_kernel(const PrefillArgs a,
     __shared__ __align__(8) uint64_t empty[C::kStages];
     __shared__ int s_fail;
 
+    pdl_wait();
+    pdl_launch_dependents();
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
     const int G = a.group;
@@ -393,8 +395,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& kmap, cons
         attr_set[dev] = true;
     }
     dim3 grid(a.max_qtiles, a.hkv, a.num_seqs);
-    kern<<<grid, kPThreads, C::kSmemBytes, stream>>>(a, kmap, vmap);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kPThreads), C::kSmemBytes, stream, a, kmap, vmap);
 }
 
 }  // namespace

@@ -109,4 +109,5 @@ def assert_lse_close(got: torch.Tensor, ref: np.ndarray, what: str):
     g = got.float().cpu().numpy()
     fin = np.isfinite(ref)
     assert np.array_equal(np.isfinite(g), fin), "%s: lse finiteness differs" % what
-    assert np.abs(g[fin] - ref[fin]).max() <= LSE_ERR, "%s: lse" % what
+    err = np.abs(g[fin] - ref[fin])
+    assert err.max() <= LSE_ERR, "%s: lse max|err| %.3g (<= %g)" % (what, err.max(), LSE_ERR)
