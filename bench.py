@@ -187,8 +187,8 @@ class DecodeWorkload:
         self.config = config
         one_bytes = None
         n_inst = 4
-        if config == 4:
-            n_inst = 1  # 8.3 GB of K/V per step: far beyond L2 already
+        if config in (4, 5):
+            n_inst = 1  # 8.3 GB / 1.1 GB of K/V per step: far beyond L2 already
         self.insts = wl.make_decode_instances(spec, n_inst, dev)
         self.layers = [self.insts]
         if config == 5:

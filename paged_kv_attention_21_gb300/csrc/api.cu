@@ -1,6 +1,6 @@
 // api.cu -- the C ABI of libpkv: argument validation, split planning,
 // tensor-map descriptors, launches and error reporting.  Everything the
-// path computes runs in the kernels of decode.cu, prefill.cu and
+// path computes runs in the kernels of decode.cu, prefill_tc.cu and
 // append_gather_merge.cu; this file only decides and launches.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -269,6 +269,26 @@ BoxShape kv_box_shape(int head_dim, int fp8) {
 }
 }  // namespace pkv
 
+namespace {
+
+// 3-D tiled view of q [total_q][Hq][D] bf16: box {64, G, QT}, 128-byte swizzle;
+// one box is the query tile of one KV group (QT tokens x G heads x 64 columns).
+pkv_status q_map(const void* q, int total_q, const pkv_cache_desc* desc, int G, int QT, CUtensorMap* out) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {cuuint64_t(desc->head_dim), cuuint64_t(desc->num_q_heads), cuuint64_t(total_q)};
+    const cuuint64_t strides[2] = {cuuint64_t(desc->head_dim) * 2, cuuint64_t(desc->head_dim) * desc->num_q_heads * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(QT)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (%d)", int(r));
+    return PKV_OK;
+}
+
+}  // namespace
+
 // ===================================================================== ABI ==
 
 extern "C" {
@@ -441,7 +461,7 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
         return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
     if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
     const int G = desc->num_q_heads / desc->num_kv_heads;
-    const int QT = pkv::prefill_q_tile(G);
+    const int QT = pkv::prefill_tc_q_tile(G);
     int max_q = total_q_tokens;
     if (qo_indptr_host) {
         if (qo_indptr_host[0] != 0 || qo_indptr_host[num_seqs] != total_q_tokens)
@@ -490,7 +510,10 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     a.total_q = total_q_tokens;
     a.num_blocks = desc->num_blocks;
     a.sm_scale = sm_scale;
-    cudaError_t e = pkv::launch_prefill(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+    CUtensorMap qmap;
+    st = q_map(q, total_q_tokens, desc, G, QT, &qmap);
+    if (st != PKV_OK) return st;
+    cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PKV_OK;
 }

@@ -82,10 +82,11 @@ struct PrefillArgs {
     int64_t num_blocks;
     float sm_scale;
 };
-// Query tokens per CTA tile for a group size (rows = tokens * group <= 64).
-int prefill_q_tile(int group);
-cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           cudaStream_t stream);
+// Query tokens per CTA tile for a group size (rows = tokens * group <= 128).
+int prefill_tc_q_tile(int group);
+// qmap: 3-D tiled view of q [total_q][Hq][D], box {64, G, q_tile}, 128-byte swizzle.
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, cudaStream_t stream);
 
 // Tensor-map box shape used by the attention kernels for a pool:
 // innermost box extent in elements, and the swizzle.

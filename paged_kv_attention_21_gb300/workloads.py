@@ -255,7 +255,7 @@ def make_decode_instances(spec: DecodeSpec, n: int, device="cpu"):
     (each instance draws its own lengths, tables and queries); every table
     has ceil(ctx_hi / block_size) columns."""
     mbps = (spec.ctx_hi + spec.block_size - 1) // spec.block_size
-    if spec.pool_blocks is None:
+    if spec.pool_blocks is None and n > 1:
         # room for n batches at the longest lengths, plus slack
         spec = dataclasses.replace(spec, pool_blocks=int(1.25 * n * spec.batch * mbps) + 16)
     first = make_decode_batch(spec, device, max_blocks_per_seq=mbps)
