@@ -129,6 +129,17 @@ pkv_status pkv_gather_kv(const pkv_cache_desc *desc, const void *cache,
                          const int32_t *cu_context_lens, int32_t num_seqs,
                          int64_t total_tokens, void *out, pkv_stream_t stream);
 
+/* ---- copy-on-write of shared blocks (infer-lab, "Technique" table:
+ * PagedAttention refcounting and copy-on-write; llm-infer, "What It Does") --
+ * For i < num_pairs, block dst_blocks[i] of both pools receives the bytes of
+ * block src_blocks[i] (every head, every row).  src_blocks, dst_blocks: int32
+ * [num_pairs].  dst ids must be distinct and must not appear among the src
+ * ids of the same call.  An id outside [0, num_blocks) skips that pair and
+ * sets PKV_DEVERR_BLOCK_ID. */
+pkv_status pkv_copy_blocks(const pkv_cache_desc *desc, void *k_cache, void *v_cache,
+                           const int32_t *src_blocks, const int32_t *dst_blocks, int32_t num_pairs,
+                           pkv_stream_t stream);
+
 /* ---- a3-a7: split-KV GQA decode (FlashAttention-2 partitioning) ---------
  * One query token per sequence, at position context_lens[s] - 1 (the new
  * token, already appended).  For query head h, KV head h / G:

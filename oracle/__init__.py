@@ -18,6 +18,8 @@ Function by function, what each follows (the page title, then the section):
   "What It Does"; infer-lab source layout: RoPE, GQA).
 * ``gather_kv`` -- block-table addressing (infer-lab, "Technique" table:
   PagedAttention block tables).
+* ``copy_blocks`` -- copy-on-write of shared blocks (infer-lab, "Technique"
+  table: refcounting, copy-on-write; llm-infer, "What It Does").
 * ``paged_attention`` -- softmax attention over the paged cache: decode,
   ragged causal chunked prefill, sliding window (infer-lab invariants;
   llm-infer "References": FlashAttention-2; RustInfer "Status": 128-token SWA).
@@ -85,6 +87,8 @@ def _load():
         lib.orc_paged_attention.argtypes = [i32, i32, i32, i32, i32, i64, i32, P, P, P, P, P,
                                             i32, P, P, P, f32, i32, i32, P, P, i32, i32]
         lib.orc_paged_attention.restype = ctypes.c_int
+        lib.orc_copy_blocks.argtypes = [P, i64, i64, P, P, i32]
+        lib.orc_copy_blocks.restype = ctypes.c_int
         lib.orc_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P]
         lib.orc_merge_states.restype = None
         for name in ("orc_bf16_to_f32_array", "orc_f32_to_bf16_array", "orc_e4m3_to_f32_array",
@@ -168,6 +172,18 @@ def append_rope(*, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, k_
     if rc != 0:
         raise ValueError("oracle append_rope: out-of-range index (rc=%d)" % rc)
     return qo
+
+
+def copy_blocks(cache, src, dst):
+    """Copy-on-write: block dst[i] of the pool (numpy, mutated) gets block src[i]."""
+    lib = _load()
+    assert cache.flags.c_contiguous
+    s = _c(src, np.int32)
+    d = _c(dst, np.int32)
+    block_bytes = cache[0].nbytes
+    rc = lib.orc_copy_blocks(_ptr(cache), cache.shape[0], block_bytes, _ptr(s), _ptr(d), len(s))
+    if rc != 0:
+        raise ValueError("oracle copy_blocks: out-of-range block id")
 
 
 def gather_kv(cache, block_tables, lens, *, block_size):

@@ -220,6 +220,25 @@ int orc_append_rope(int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t kv_d
     return rc;
 }
 
+/* ------------------------------------------------------------ block copy --- */
+
+/* Copy-on-write of paged blocks: block dst[i] of a pool receives the bytes
+ * of block src[i] (every head, every row).  block_bytes = Hkv*bs*D*elem.
+ * Returns 0, or -1 if an id is out of range (that pair is skipped). */
+int orc_copy_blocks(void *cache, int64_t num_blocks, int64_t block_bytes, const int32_t *src,
+                    const int32_t *dst, int32_t num_pairs) {
+    int rc = 0;
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) {
+            rc = -1;
+            continue;
+        }
+        memcpy((uint8_t *)cache + (size_t)dst[i] * block_bytes,
+               (const uint8_t *)cache + (size_t)src[i] * block_bytes, (size_t)block_bytes);
+    }
+    return rc;
+}
+
 /* --------------------------------------------------------------- gather --- */
 
 /* out[cu[s] + t][h][:] = cache[block_tables[s][t / bs]][h][t % bs][:] for

@@ -92,6 +92,7 @@ def load_library():
             "pkv_decode_attention_static": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32,
                                                            i32, i32, P, P, P]),
             "pkv_merge_states": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, P, P]),
+            "pkv_copy_blocks": (ctypes.c_int, [D, P, P, P, P, i32, P]),
             "pkv_last_error": (ctypes.c_char_p, []),
             "pkv_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32]),
         }
@@ -160,6 +161,13 @@ def pkv_gather_kv(desc, cache, block_tables, context_lens, cu_context_lens, tota
         ctypes.byref(desc), _ptr(cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(cu_context_lens), int(context_lens.shape[0]), int(total_tokens), _ptr(out),
         _stream(stream)))
+
+
+def pkv_copy_blocks(desc, k_cache, v_cache, src_blocks, dst_blocks, stream=None):
+    """Copy-on-write: block dst_blocks[i] of both pools receives block src_blocks[i]."""
+    _check(load_library().pkv_copy_blocks(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(src_blocks), _ptr(dst_blocks),
+                                          int(src_blocks.shape[0]), _stream(stream)))
 
 
 def pkv_decode_workspace_size(desc, num_seqs, max_context_len, window=-1, chunk_blocks=0) -> int:

@@ -598,6 +598,35 @@ pkv_status pkv_gather_kv(const pkv_cache_desc* desc, const void* cache, const in
     return PKV_OK;
 }
 
+pkv_status pkv_copy_blocks(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                           const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                           pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0 || num_pairs > 0x7FFFFFFF / 2) return fail(PKV_ERR_INVALID_ARG, "num_pairs %d", num_pairs);
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src_blocks || !dst_blocks)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(PKV_ERR_INVALID_ARG, "the pools must be 16-byte aligned");
+    uint32_t* err = nullptr;
+    st = device_state(&err, nullptr);
+    if (st != PKV_OK) return st;
+    pkv::CopyArgs a{};
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.src = src_blocks;
+    a.dst = dst_blocks;
+    a.num_pairs = num_pairs;
+    a.num_blocks = desc->num_blocks;
+    a.block_bytes = int64_t(desc->num_kv_heads) * desc->block_size * desc->head_dim * elem_bytes(desc);
+    a.err = err;
+    cudaError_t e = pkv::launch_copy_blocks(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "copy launch");
+    return PKV_OK;
+}
+
 pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_parts,
                             int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
                             float* lse_out, pkv_stream_t stream) {

@@ -1,11 +1,13 @@
-// append_gather_merge.cu -- the three small kernels of the path:
+// append_gather_merge.cu -- the small kernels of the path:
 //   * fused KV append + RoPE (+ e4m3 quantisation)  (llm-infer, "What It Does":
 //     KV writes and fused RoPE inside the decode step);
 //   * block-table gather of one pool into contiguous rows (infer-lab,
 //     "Technique" table: PagedAttention block tables);
+//   * copy-on-write of whole blocks (infer-lab, "Technique" table:
+//     refcounting, copy-on-write; llm-infer, "What It Does");
 //   * standalone merge of partial (o, lse) states (FlashAttention-2 work
 //     partitioning, cited under llm-infer "References").
-// All three are latency-bound: a few MB at most.  Loads and stores are
+// All of them are latency-bound: a few MB at most.  Loads and stores are
 // coalesced across the warp; no shared memory is needed.
 #include "common.cuh"
 #include "internal.h"
@@ -187,6 +189,33 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
     const long long blocks = (n + threads - 1) / threads;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, a);
+}
+
+// ----------------------------------------------------------- block copy --
+//
+// Copy-on-write: one CTA per (pair, pool); 16-byte vector copies of the
+// whole block (every head and row).
+
+__global__ void __launch_bounds__(256) copy_blocks_kernel(CopyArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int i = blockIdx.x;
+    const int src = a.src[i];
+    const int dst = a.dst[i];
+    if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+        if (threadIdx.x == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+        return;
+    }
+    uint8_t* pool = static_cast<uint8_t*>(blockIdx.y == 0 ? a.k_cache : a.v_cache);
+    const uint4* s = reinterpret_cast<const uint4*>(pool + static_cast<size_t>(src) * a.block_bytes);
+    uint4* d = reinterpret_cast<uint4*>(pool + static_cast<size_t>(dst) * a.block_bytes);
+    const int n = static_cast<int>(a.block_bytes / 16);
+    for (int c = threadIdx.x; c < n; c += blockDim.x) d[c] = s[c];
+}
+
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
+    if (a.num_pairs == 0) return cudaSuccess;
+    return launch_pdl(copy_blocks_kernel, dim3(a.num_pairs, 2), dim3(256), 0, stream, a);
 }
 
 // ---------------------------------------------------------------- merge --

@@ -40,6 +40,17 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
 
+struct CopyArgs {
+    void* k_cache;
+    void* v_cache;
+    const int32_t* src;
+    const int32_t* dst;
+    int32_t num_pairs;
+    int64_t num_blocks, block_bytes;
+    uint32_t* err;
+};
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
+
 struct MergeArgs {
     const float* o_parts;
     const float* lse_parts;

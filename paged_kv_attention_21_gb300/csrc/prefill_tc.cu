@@ -13,7 +13,8 @@
 // (row r -> token r / G, head r % G), so each K/V tile read serves the whole
 // group.  Warp roles:
 //   warp 0      TMA producer: the Q tile once (3-D tensor map over q), then
-//               K and V tiles of 128 keys (8 blocks) into a 2-stage ring;
+//               K and V tiles of 128 keys (8 blocks) into separate rings
+//               (K 3 stages, one tile ahead of V, 2 stages);
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
 //               S buffers, then O += P_{j-1} V_{j-1} into the TMEM O
 //               accumulator -- so S_{j+1} runs on the tensor pipe while the
@@ -45,14 +46,17 @@ struct TcCfg {
     static constexpr int kHalves = D / 64;             // 64-column (128-byte) halves of a row
     static constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes
     static constexpr int kQBytes = kHalves * kHalfBytes;
-    static constexpr int kKBytes = kHalves * kHalfBytes;  // 128 keys x D
+    static constexpr int kKBytes = kHalves * kHalfBytes;  // 128 keys x D (K or V tile)
     static constexpr int kPBytes = 2 * kHalfBytes;        // 128 rows x 128 keys
-    static constexpr int kStages = 2;
+    // K and V live in separate rings: a K stage frees as soon as its S = Q K^T
+    // is done, so K runs a full tile further ahead of the MMA than V.
+    static constexpr int kKStages = 3;
+    static constexpr int kVStages = 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffKV = kOffP + kPBytes;
-    static constexpr int kStageBytes = 2 * kKBytes;       // K then V
-    static constexpr int kBodyBytes = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffK = kOffP + kPBytes;
+    static constexpr int kOffV = kOffK + kKStages * kKBytes;
+    static constexpr int kBodyBytes = kOffV + kVStages * kKBytes;
     // at least 120 KB so that one CTA owns an SM (and all 512 TMEM columns)
     static constexpr int kSmemBytes = (kBodyBytes + 1024 > 120 * 1024) ? kBodyBytes + 1024 : 120 * 1024;
     static constexpr uint32_t kTmemCols = 512;            // S0 | S1 | O
@@ -78,9 +82,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t bar_q;
-    __shared__ __align__(8) uint64_t bar_k[2];
+    __shared__ __align__(8) uint64_t bar_k[3];
+    __shared__ __align__(8) uint64_t bar_k_empty[3];
     __shared__ __align__(8) uint64_t bar_v[2];
-    __shared__ __align__(8) uint64_t bar_kv_empty[2];
+    __shared__ __align__(8) uint64_t bar_v_empty[2];
     __shared__ __align__(8) uint64_t bar_s_full[2];
     __shared__ __align__(8) uint64_t bar_s_free[2];
     __shared__ __align__(8) uint64_t bar_p_full;
@@ -124,10 +129,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::kKStages; ++i) {
             mbar_init(&bar_k[i], 1);
+            mbar_init(&bar_k_empty[i], 1);
+        }
+        for (int i = 0; i < C::kVStages; ++i) {
             mbar_init(&bar_v[i], 1);
-            mbar_init(&bar_kv_empty[i], 1);
+            mbar_init(&bar_v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_s_full[i], 1);
             mbar_init(&bar_s_free[i], 4);
         }
@@ -161,52 +171,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int h = 0; h < C::kHalves; ++h)
                     tma_load_3d(sQ + h * C::kHalfBytes, &qmap, &bar_q, h * 64, kvh * G, q0 + tok0);
             }
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                const int blk0 = (t_begin + j) * kTcBlocks;
-                int id = 0;
-                if (lane < kTcBlocks && blk0 + lane < nblk_seq) {
-                    id = bt[blk0 + lane];
-                    if (id < 0 || id >= a.num_blocks) {
-                        flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                        id = 0;
+            // order of loads: K_0, K_1, V_0, K_2, V_1, ... -- K one tile ahead of V
+            int ids_prev = 0;
+            for (int j = 0; j <= n_tiles; ++j) {
+                int ids_cur = 0;
+                if (j < n_tiles) {
+                    const int blk0 = (t_begin + j) * kTcBlocks;
+                    if (lane < kTcBlocks && blk0 + lane < nblk_seq) {
+                        ids_cur = bt[blk0 + lane];
+                        if (ids_cur < 0 || ids_cur >= a.num_blocks) {
+                            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            ids_cur = 0;
+                        }
+                    }
+                    const int st = j % C::kKStages;
+                    int ok = 1;
+                    if (lane == 0) ok = mbar_wait(&bar_k_empty[st], ((j / C::kKStages) & 1) ^ 1) ? 1 : 0;
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
+                        if (lane == 0) atomicOr(&s_fail, 1);
+                        break;
+                    }
+                    const int nvalid = min(kTcBlocks, nblk_seq - blk0);
+                    uint8_t* sK = smem + C::kOffK + st * C::kKBytes;
+                    int ids[kTcBlocks];
+#pragma unroll
+                    for (int b = 0; b < kTcBlocks; ++b) ids[b] = __shfl_sync(0xFFFFFFFFu, ids_cur, b);
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(&bar_k[st], nvalid * kBlockSize * D * 2);
+#pragma unroll
+                        for (int b = 0; b < kTcBlocks; ++b) {
+                            if (b >= nvalid) break;
+#pragma unroll
+                            for (int h = 0; h < C::kHalves; ++h)
+                                tma_load_4d(sK + h * C::kHalfBytes + b * 2048, &kmap, &bar_k[st], h * 64, 0,
+                                            kvh, ids[b]);
+                        }
                     }
                 }
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(&bar_kv_empty[st], ((j >> 1) & 1) ^ 1) ? 1 : 0;
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
-                    if (lane == 0) atomicOr(&s_fail, 1);
-                    break;
-                }
-                const int nvalid = min(kTcBlocks, nblk_seq - blk0);
-                uint8_t* sK = smem + C::kOffKV + st * C::kStageBytes;
-                uint8_t* sV = sK + C::kKBytes;
-                int ids[kTcBlocks];
-#pragma unroll
-                for (int b = 0; b < kTcBlocks; ++b) ids[b] = __shfl_sync(0xFFFFFFFFu, id, b);
-                if (lane == 0) {
-                    const uint32_t bytes = nvalid * kBlockSize * D * 2;
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(&bar_k[st], bytes);
-#pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b) {
-                        if (b >= nvalid) break;
-#pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_4d(sK + h * C::kHalfBytes + b * 2048, &kmap, &bar_k[st], h * 64, 0,
-                                        kvh, ids[b]);
+                if (j >= 1) {
+                    const int i = j - 1;
+                    const int st = i % C::kVStages;
+                    int ok = 1;
+                    if (lane == 0) ok = mbar_wait(&bar_v_empty[st], ((i / C::kVStages) & 1) ^ 1) ? 1 : 0;
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
+                        if (lane == 0) atomicOr(&s_fail, 1);
+                        break;
                     }
-                    mbar_arrive_expect_tx(&bar_v[st], bytes);
+                    const int blk0 = (t_begin + i) * kTcBlocks;
+                    const int nvalid = min(kTcBlocks, nblk_seq - blk0);
+                    uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
+                    int ids[kTcBlocks];
 #pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b) {
-                        if (b >= nvalid) break;
+                    for (int b = 0; b < kTcBlocks; ++b) ids[b] = __shfl_sync(0xFFFFFFFFu, ids_prev, b);
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(&bar_v[st], nvalid * kBlockSize * D * 2);
 #pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_4d(sV + h * C::kHalfBytes + b * 2048, &vmap, &bar_v[st], h * 64, 0,
-                                        kvh, ids[b]);
+                        for (int b = 0; b < kTcBlocks; ++b) {
+                            if (b >= nvalid) break;
+#pragma unroll
+                            for (int h = 0; h < C::kHalves; ++h)
+                                tma_load_4d(sV + h * C::kHalfBytes + b * 2048, &vmap, &bar_v[st], h * 64, 0,
+                                            kvh, ids[b]);
+                        }
                     }
                 }
+                ids_prev = ids_cur;
             }
         }
     } else if (warp == 1) {
@@ -218,12 +251,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; ok && j <= n_tiles; ++j) {
             if (j < n_tiles) {
                 const int st = j & 1;
-                bool r1 = mbar_wait(&bar_k[st], (j >> 1) & 1);
+                const int ks = j % C::kKStages;
+                bool r1 = mbar_wait(&bar_k[ks], (j / C::kKStages) & 1);
                 bool r2 = mbar_wait(&bar_s_free[st], ((j >> 1) & 1) ^ 1);
                 if (!__all_sync(0xFFFFFFFFu, r1 && r2) || *reinterpret_cast<volatile int*>(&s_fail)) { ok = false; break; }
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint8_t* sK = smem + C::kOffKV + st * C::kStageBytes;
+                    const uint8_t* sK = smem + C::kOffK + ks * C::kKBytes;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int h = kk >> 2;
@@ -233,18 +267,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc::mma_bf16(tmem + st * kTcN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
                     }
                     tc::commit(&bar_s_full[st]);
+                    tc::commit(&bar_k_empty[ks]);  // this K tile is no longer needed
                 }
                 __syncwarp();
             }
             if (j >= 1) {
                 const int i = j - 1;
-                const int st = i & 1;
+                const int st = i % C::kVStages;
                 bool r1 = mbar_wait(&bar_p_full, i & 1);
-                bool r2 = mbar_wait(&bar_v[st], (i >> 1) & 1);
+                bool r2 = mbar_wait(&bar_v[st], (i / C::kVStages) & 1);
                 if (!__all_sync(0xFFFFFFFFu, r1 && r2) || *reinterpret_cast<volatile int*>(&s_fail)) { ok = false; break; }
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint8_t* sV = smem + C::kOffKV + st * C::kStageBytes + C::kKBytes;
+                    const uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
 #pragma unroll
                     for (int kk = 0; kk < kTcN / 16; ++kk) {
                         const int h = kk >> 2;
@@ -256,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc::mma_bf16(tmem + C::kColO, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::commit(&bar_o_done);
-                    tc::commit(&bar_kv_empty[st]);
+                    tc::commit(&bar_v_empty[st]);
                 }
                 __syncwarp();
             }
@@ -286,30 +321,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            float x[kTcN];
-#pragma unroll
-            for (int c = 0; c < kTcN / 32; ++c)
-                tc::ld32(lane_base + sb * kTcN + c * 32, *reinterpret_cast<float(*)[32]>(x + c * 32));
-            tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_s_free[sb]);  // S buffer may be overwritten
-
-            // mask and row max (exp2 domain)
+            const uint32_t s_col = lane_base + sb * kTcN;
             const bool full_vis = (!a.causal || k0 + kTcN - 1 <= pos_min) && (k0 + kTcN <= kv_len) &&
                                   (a.window <= 0 || k0 > pos_max - a.window);
+            // S is read from TMEM twice, 32 columns at a time (row max, then
+            // exponentials): small code and few registers, where a whole row
+            // in registers made the loop body too large for the instruction
+            // cache.
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < kTcN / 32; ++c) {
+                float v[32];
+                tc::ld32(s_col + c * 32, v);
+                tc::wait_ld();
 #pragma unroll
-            for (int c = 0; c < kTcN; ++c) {
-                float v = x[c] * scale_log2;
-                if (!full_vis) {
-                    const int key = k0 + c;
-                    const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                     (a.window <= 0 || key > pos - a.window);
-                    if (!vis) v = -INFINITY;
+                for (int e = 0; e < 32; ++e) {
+                    float val = v[e] * scale_log2;
+                    if (!full_vis) {
+                        const int key = k0 + c * 32 + e;
+                        const bool vis = key < kv_len && (!a.causal || key <= pos) &&
+                                         (a.window <= 0 || key > pos - a.window);
+                        if (!vis) val = -INFINITY;
+                    }
+                    mx = fmaxf(mx, val);
                 }
-                x[c] = v;
-                mx = fmaxf(mx, v);
             }
             // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
             const float m_new = fmaxf(m_used, mx);
@@ -324,15 +359,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // keys past kv_len in the last tile: zero their V rows so that a
             // NaN in an unused slot never meets a zero weight in the MMA
             if (k0 + kTcN > kv_len) {
-                const int st = j & 1;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_v[st], (j >> 1) & 1))) {
+                const int st = j % C::kVStages;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_v[st], (j / C::kVStages) & 1))) {
                     ok = false;
                     break;
                 }
-                uint8_t* sV = smem + C::kOffKV + st * C::kStageBytes + C::kKBytes;
+                uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
                 const int first = max(0, kv_len - k0);
                 // 4 warps x 32 lanes zero rows [first, 128) of every half
-                for (int row = first + (r >> 3) ; row < kTcN; row += 16) {
+                for (int row = first + (r >> 3); row < kTcN; row += 16) {
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h)
                         *reinterpret_cast<uint4*>(sV + h * C::kHalfBytes + row * 128 + (r & 7) * 16) =
@@ -347,7 +382,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc::fence_after_sync();
                 if (__any_sync(0xFFFFFFFFu, need)) {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         float v[32];
                         tc::ld32(lane_base + C::kColO + c * 32, v);
@@ -363,20 +398,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // to bf16 pairs into the swizzled K-major P tile
             const float mu = m_used == -INFINITY ? 0.f : m_used;
             float rowsum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kTcN / 32; ++c) {
+                float v[32];
+                tc::ld32(s_col + c * 32, v);
+                tc::wait_ld();
 #pragma unroll
-            for (int c = 0; c < kTcN / 8; ++c) {        // 16 chunks of 8 keys
-                uint32_t pk[4];
+                for (int q8 = 0; q8 < 4; ++q8) {          // 4 chunks of 8 keys
+                    uint32_t pk[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float p0 = fast_exp2(x[c * 8 + 2 * u] - mu);
-                    const float p1 = fast_exp2(x[c * 8 + 2 * u + 1] - mu);
-                    rowsum += p0 + p1;
-                    pk[u] = pack2<false>(p0, p1);
+                    for (int u = 0; u < 4; ++u) {
+                        float p2[2];
+#pragma unroll
+                        for (int w = 0; w < 2; ++w) {
+                            const int e = q8 * 8 + 2 * u + w;
+                            float val = v[e] * scale_log2;
+                            if (!full_vis) {
+                                const int key = k0 + c * 32 + e;
+                                const bool vis = key < kv_len && (!a.causal || key <= pos) &&
+                                                 (a.window <= 0 || key > pos - a.window);
+                                if (!vis) val = -INFINITY;
+                            }
+                            p2[w] = fast_exp2(val - mu);
+                        }
+                        rowsum += p2[0] + p2[1];
+                        pk[u] = pack2<false>(p2[0], p2[1]);
+                    }
+                    const int chunk = c * 4 + q8;          // 16-byte chunk (8 keys) in the row
+                    *reinterpret_cast<uint4*>(sP + (chunk >> 3) * C::kHalfBytes + sw128(r, chunk & 7)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                const int h = c >> 3;
-                *reinterpret_cast<uint4*>(sP + h * C::kHalfBytes + sw128(r, c & 7)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_s_free[sb]);  // S buffer may be overwritten
             l += rowsum;
             fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
             tc::fence_before_sync();

@@ -164,3 +164,25 @@ def test_bad_block_id_is_flagged_not_faulted():
     pkv.pkv_append_rope(desc, d["k_cache"], d["v_cache"], d["block_tables"], seq, pos2, kn, kn)
     assert pkv.pkv_device_errors(reset=True) & pkv.DEVERR_POSITION
     assert pkv.pkv_device_errors() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_copy_blocks_bit_exact(fp8):
+    spec = wl.scaled(wl.FP8_DECODE if fp8 else wl.QWEN3_4B, batch=8, ctx_hi=500)
+    b = wl.make_decode_batch(spec, "cpu")
+    d = on_device(b)
+    desc = desc_for(spec, b.k_cache, b.tables_host)
+    nb = b.k_cache.shape[0]
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(nb)
+    src, dst = perm[:40].astype(np.int32), perm[40:80].astype(np.int32)
+    src[1] = src[0]  # one source shared by two copies
+    pkv.pkv_copy_blocks(desc, d["k_cache"], d["v_cache"], torch.from_numpy(src).to(DEV),
+                        torch.from_numpy(dst).to(DEV))
+    torch.cuda.synchronize()
+    kh, vh = pool_np(b.k_cache).copy(), pool_np(b.v_cache).copy()
+    oracle.copy_blocks(kh, src, dst)
+    oracle.copy_blocks(vh, src, dst)
+    assert np.array_equal(pool_np(d["k_cache"]), kh)
+    assert np.array_equal(pool_np(d["v_cache"]), vh)
+    assert pkv.pkv_device_errors() == 0

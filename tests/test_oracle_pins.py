@@ -519,3 +519,14 @@ def test_lse_matches_scipy_logsumexp():
     for h in range(4):
         logits = 0.125 * K @ bits_to_f64(case.q[0, h])
         assert abs(lse[0, h] - scipy.special.logsumexp(logits)) < 2e-5
+
+
+def test_copy_blocks_matches_numpy_assignment():
+    rng = np.random.default_rng(27)
+    pool = rng.integers(0, 65535, size=(20, 2, BS, 16), dtype=np.uint16)
+    ref = pool.copy()
+    src = np.array([3, 3, 7, 19], np.int32)
+    dst = np.array([0, 11, 12, 5], np.int32)
+    ref[dst] = ref[src]
+    oracle.copy_blocks(pool, src, dst)
+    assert np.array_equal(pool, ref)
