@@ -14,12 +14,13 @@
 // group.  Warp roles:
 //   warp 0      TMA producer: the Q tile once (3-D tensor map over q), then
 //               K and V tiles of 128 keys (8 blocks) into separate rings
-//               (K 3 stages, one tile ahead of V, 2 stages);
+//               (2 stages each; K frees at S completion, V at PV completion);
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
 //               S buffers, then O += P_{j-1} V_{j-1} into the TMEM O
 //               accumulator -- so S_{j+1} runs on the tensor pipe while the
 //               softmax warps work on S_j;
-//   warps 2..5  softmax, one thread per row (its TMEM lane): masked row max,
+//   warps 2..9  softmax, two threads per row (its TMEM lane; 64 key columns
+//               each, row maxima exchanged in shared memory): masked row max,
 //               lazy rescale of O only when the max grows by more than 2^8,
 //               P = 2^(x - m) (fp32 exp2, packed to bf16) written to shared
 //               memory in the 128-byte-swizzled K-major layout the MMA reads,
@@ -37,7 +38,7 @@ namespace {
 constexpr int kTcM = 128;                         // query rows per tile
 constexpr int kTcN = 128;                         // keys per KV tile
 constexpr int kTcBlocks = kTcN / kBlockSize;      // 8 blocks per KV tile
-constexpr int kTcWarps = 6;
+constexpr int kTcWarps = 10;  // producer, MMA issuer, 8 softmax warps (2 per row quadrant)
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;         // log2 of the largest stale-max factor
 
@@ -50,7 +51,7 @@ struct TcCfg {
     static constexpr int kPBytes = 2 * kHalfBytes;        // 128 rows x 128 keys
     // K and V live in separate rings: a K stage frees as soon as its S = Q K^T
     // is done, so K runs a full tile further ahead of the MMA than V.
-    static constexpr int kKStages = 3;
+    static constexpr int kKStages = 2;
     static constexpr int kVStages = 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffP = kOffQ + kQBytes;
@@ -92,6 +93,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t bar_o_done;
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
+    __shared__ float s_red_max[2][2][kTcM];  // [tile parity][column half][row]
+    __shared__ float s_red_sum[2][kTcM];     // [column half][row]
+    __shared__ __align__(8) uint64_t bar_pair[4][3];  // per quadrant: tile parity 0/1, final
 
     pdl_wait();
     pdl_launch_dependents();
@@ -139,9 +143,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_s_full[i], 1);
-            mbar_init(&bar_s_free[i], 4);
+            mbar_init(&bar_s_free[i], 8);
         }
-        mbar_init(&bar_p_full, 4);
+        mbar_init(&bar_p_full, 8);
+        for (int qd = 0; qd < 4; ++qd)
+            for (int i = 0; i < 3; ++i) mbar_init(&bar_pair[qd][i], 64);
         mbar_init(&bar_o_done, 1);
         s_fail = 0;
         tma_prefetch_desc(&qmap);
@@ -302,15 +308,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // -------------------------------------------------------------- softmax
+        // Two warps share each row quadrant: warp w (2..9) reads TMEM lanes of
+        // quadrant w % 4 and owns key columns [64h, 64h + 64) and O columns
+        // [h D/2, (h+1) D/2) with h = (w - 2) / 4.  The pair exchanges row maxima
+        // through shared memory on a named barrier; row sums stay per half.
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int half = (warp - 2) >> 2;          // key / O column half
         const int r = quad * 32 + lane;            // the row this thread owns
         const int t = r / G;
         const bool row_ok = r < QT * G && t < ntok;
         const int pos = off + tok0 + t;
         const float scale_log2 = a.sm_scale * 1.4426950408889634f;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const int sm_tid = (warp - 2) * 32 + lane;  // 0..255
+        // the two warps of this quadrant meet on an mbarrier (bounded wait):
+        // slot 0/1 for the per-tile max exchange (by tile parity), 2 at the end
+        auto pair_sync = [&](int slot, uint32_t parity) {
+            mbar_arrive(&bar_pair[quad][slot]);
+            return mbar_wait(&bar_pair[quad][slot], parity);
+        };
         float m_used = -INFINITY;
-        float l = 0.f;
+        float l = 0.f;                             // this half's share of the row sum
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int sb = j & 1;
@@ -321,31 +339,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            const uint32_t s_col = lane_base + sb * kTcN;
+            const uint32_t s_col = lane_base + sb * kTcN + half * 64;
+            const int kh = k0 + half * 64;          // first key of this half
             const bool full_vis = (!a.causal || k0 + kTcN - 1 <= pos_min) && (k0 + kTcN <= kv_len) &&
                                   (a.window <= 0 || k0 > pos_max - a.window);
-            // S is read from TMEM twice, 32 columns at a time (row max, then
-            // exponentials): small code and few registers, where a whole row
-            // in registers made the loop body too large for the instruction
-            // cache.
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < kTcN / 32; ++c) {
-                float v[32];
-                tc::ld32(s_col + c * 32, v);
-                tc::wait_ld();
+            float x[64];
+            tc::ld32(s_col, *reinterpret_cast<float(*)[32]>(x));
+            tc::ld32(s_col + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_s_free[sb]);  // S is in registers
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float val = v[e] * scale_log2;
-                    if (!full_vis) {
-                        const int key = k0 + c * 32 + e;
-                        const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                         (a.window <= 0 || key > pos - a.window);
-                        if (!vis) val = -INFINITY;
-                    }
-                    mx = fmaxf(mx, val);
+            for (int e = 0; e < 64; ++e) {
+                float val = x[e] * scale_log2;
+                if (!full_vis) {
+                    const int key = kh + e;
+                    const bool vis = key < kv_len && (!a.causal || key <= pos) &&
+                                     (a.window <= 0 || key > pos - a.window);
+                    if (!vis) val = -INFINITY;
                 }
+                x[e] = val;
+                m4[e & 3] = fmaxf(m4[e & 3], val);
             }
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            s_red_max[sb][half][r] = mx;
+            if (!__all_sync(0xFFFFFFFFu, pair_sync(sb, (j >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            mx = fmaxf(mx, s_red_max[sb][half ^ 1][r]);
             // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + kRescaleThreshold ||
@@ -366,11 +390,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
                 const int first = max(0, kv_len - k0);
-                // 4 warps x 32 lanes zero rows [first, 128) of every half
-                for (int row = first + (r >> 3); row < kTcN; row += 16) {
+                // 8 warps x 32 lanes zero rows [first, 128) of every half
+                for (int row = first + (sm_tid >> 3); row < kTcN; row += 32) {
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h)
-                        *reinterpret_cast<uint4*>(sV + h * C::kHalfBytes + row * 128 + (r & 7) * 16) =
+                        *reinterpret_cast<uint4*>(sV + h * C::kHalfBytes + row * 128 + (sm_tid & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                 }
             }
@@ -382,57 +406,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc::fence_after_sync();
                 if (__any_sync(0xFFFFFFFFu, need)) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
                         float v[32];
-                        tc::ld32(lane_base + C::kColO + c * 32, v);
+                        const uint32_t col = lane_base + C::kColO + half * (D / 2) + c * 32;
+                        tc::ld32(col, v);
                         tc::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                        tc::st32(lane_base + C::kColO + c * 32, v);
+                        tc::st32(col, v);
                     }
                     tc::wait_st();
                 }
             }
             // P = 2^(x - m) in fp32 (the row sum l stays exact to fp32), packed
-            // to bf16 pairs into the swizzled K-major P tile
+            // to bf16 pairs into the swizzled K-major P tile (this half's keys)
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            float rowsum = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < kTcN / 32; ++c) {
-                float v[32];
-                tc::ld32(s_col + c * 32, v);
-                tc::wait_ld();
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {          // 4 chunks of 8 keys
-                    uint32_t pk[4];
+            for (int q8 = 0; q8 < 8; ++q8) {              // 8 chunks of 8 keys
+                uint32_t pk[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float p2[2];
-#pragma unroll
-                        for (int w = 0; w < 2; ++w) {
-                            const int e = q8 * 8 + 2 * u + w;
-                            float val = v[e] * scale_log2;
-                            if (!full_vis) {
-                                const int key = k0 + c * 32 + e;
-                                const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                                 (a.window <= 0 || key > pos - a.window);
-                                if (!vis) val = -INFINITY;
-                            }
-                            p2[w] = fast_exp2(val - mu);
-                        }
-                        rowsum += p2[0] + p2[1];
-                        pk[u] = pack2<false>(p2[0], p2[1]);
-                    }
-                    const int chunk = c * 4 + q8;          // 16-byte chunk (8 keys) in the row
-                    *reinterpret_cast<uint4*>(sP + (chunk >> 3) * C::kHalfBytes + sw128(r, chunk & 7)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                for (int u = 0; u < 4; ++u) {
+                    const float p0 = fast_exp2(x[q8 * 8 + 2 * u] - mu);
+                    const float p1 = fast_exp2(x[q8 * 8 + 2 * u + 1] - mu);
+                    s4[u] += p0 + p1;
+                    pk[u] = pack2<false>(p0, p1);
                 }
+                *reinterpret_cast<uint4*>(sP + half * C::kHalfBytes + sw128(r, q8)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_s_free[sb]);  // S buffer may be overwritten
-            l += rowsum;
+            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
             tc::fence_before_sync();
             __syncwarp();
@@ -442,21 +446,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done, (n_tiles - 1) & 1));
             tc::fence_after_sync();
         }
+        // every softmax thread reaches this exchange (failure or not; the wait is bounded)
+        s_red_sum[half][r] = l;
+        if (!__all_sync(0xFFFFFFFFu, pair_sync(2, 0))) ok = false;
+        const float l_row = l + s_red_sum[half ^ 1][r];
         if (!ok) {
             if (lane == 0) {
                 flag_error(a.err, PKV_DEVERR_TIMEOUT);
                 atomicOr(&s_fail, 1);
             }
         } else {
-            // epilogue: O / l -> bf16 rows; lse
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // epilogue: this half's O columns / l -> bf16; lse by half 0
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                                  (static_cast<size_t>(q0 + tok0 + t) * a.hq + kvh * G + r % G) * D;
+                                  (static_cast<size_t>(q0 + tok0 + t) * a.hq + kvh * G + r % G) * D +
+                                  half * (D / 2);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 float v[32];
                 if (n_tiles > 0) {
-                    tc::ld32(lane_base + C::kColO + c * 32, v);
+                    tc::ld32(lane_base + C::kColO + half * (D / 2) + c * 32, v);
                     tc::wait_ld();
                 } else {
 #pragma unroll
@@ -473,9 +482,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (row_ok && a.lse_out)
+            if (row_ok && a.lse_out && half == 0)
                 a.lse_out[static_cast<size_t>(q0 + tok0 + t) * a.hq + kvh * G + r % G] =
-                    l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+                    l_row > 0.f ? (m_used + __log2f(l_row)) * 0.6931471805599453f : -INFINITY;
         }
     }
 
