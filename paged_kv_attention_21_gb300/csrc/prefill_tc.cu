@@ -350,20 +350,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_s_free[sb]);  // S is in registers
+            // Row max.  Tiles wholly visible to the CTA (all but the diagonal and
+            // the window edge) take the short path: the max of the raw scores,
+            // scaled once.  Masked tiles scale and mask every score here, so the
+            // exponential pass below reads them ready.
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full_vis) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                float val = x[e] * scale_log2;
-                if (!full_vis) {
+                for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], x[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
                     const int key = kh + e;
                     const bool vis = key < kv_len && (!a.causal || key <= pos) &&
                                      (a.window <= 0 || key > pos - a.window);
-                    if (!vis) val = -INFINITY;
+                    x[e] = vis ? x[e] * scale_log2 : -INFINITY;
+                    m4[e & 3] = fmaxf(m4[e & 3], x[e]);
                 }
-                x[e] = val;
-                m4[e & 3] = fmaxf(m4[e & 3], val);
             }
             float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            if (full_vis) mx *= scale_log2;  // scale_log2 > 0: the max commutes with it
             s_red_max[sb][half][r] = mx;
             if (!__all_sync(0xFFFFFFFFu, pair_sync(sb, (j >> 1) & 1))) {
                 ok = false;
@@ -423,13 +429,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // to bf16 pairs into the swizzled K-major P tile (this half's keys)
             const float mu = m_used == -INFINITY ? 0.f : m_used;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            // p = 2^(score * scale - mu): one FMA and one exp2 per score on the
+            // short path (raw scores), one subtract on the masked path
+            const float sc = full_vis ? scale_log2 : 1.f;
 #pragma unroll
             for (int q8 = 0; q8 < 8; ++q8) {              // 8 chunks of 8 keys
                 uint32_t pk[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float p0 = fast_exp2(x[q8 * 8 + 2 * u] - mu);
-                    const float p1 = fast_exp2(x[q8 * 8 + 2 * u + 1] - mu);
+                    const float p0 = fast_exp2(fmaf(x[q8 * 8 + 2 * u], sc, -mu));
+                    const float p1 = fast_exp2(fmaf(x[q8 * 8 + 2 * u + 1], sc, -mu));
                     s4[u] += p0 + p1;
                     pk[u] = pack2<false>(p0, p1);
                 }
