@@ -8,25 +8,31 @@
 // position p_i = kv_len - q_len + i and attends keys t <= p_i (and
 // t > p_i - W with a window), gathered block by block through the block table.
 //
-// One CTA owns (sequence, KV head, query tile).  The tile packs QT = 128 / G
-// consecutive query tokens x the G heads of one KV group into M = 128 rows
-// (row r -> token r / G, head r % G), so each K/V tile read serves the whole
-// group.  Warp roles:
-//   warp 0      TMA producer: the Q tile once (3-D tensor map over q), then
-//               K and V tiles of 128 keys (8 blocks) into separate rings
-//               (2 stages each; K frees at S completion, V at PV completion);
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               S buffers, then O += P_{j-1} V_{j-1} into the TMEM O
-//               accumulator -- so S_{j+1} runs on the tensor pipe while the
-//               softmax warps work on S_j;
-//   warps 2..9  softmax, two threads per row (its TMEM lane; 64 key columns
-//               each, row maxima exchanged in shared memory): masked row max,
-//               lazy rescale of O only when the max grows by more than 2^8,
-//               P = 2^(x - m) (fp32 exp2, packed to bf16) written to shared
-//               memory in the 128-byte-swizzled K-major layout the MMA reads,
-//               and the final 1/l normalisation and bf16 store.
-// Operands: Q, K (K-major, SW128) and P (K-major, SW128) via shared-memory
-// descriptors; V is read MN-major (head_dim contiguous), as stored.
+// One CTA owns (sequence, KV head, pair of query tiles A and B).  A tile packs
+// QT = 128 / G consecutive query tokens x the G heads of one KV group into
+// M = 128 rows (row r -> token r / G, head r % G); the two tiles cover 2 QT
+// consecutive tokens and share every K/V tile the CTA reads, so each TMA box
+// feeds 256 query rows.  Warp roles:
+//   warp 0       TMA producer: both Q tiles once (3-D tensor map over q), then
+//                K and V tiles of 128 keys (8 blocks) into separate rings
+//                (2 stages each; K frees once both S MMAs are done, V once
+//                both PV MMAs are done);
+//   warp 1       MMA issuer (one thread), per KV tile j in the order
+//                S_A(j) | PV_B(j-1) | S_B(j) | PV_A(j), so that the tensor
+//                pipe works on one tile while the softmax warps of the other
+//                turn its S into P;
+//   warps 2..17  softmax, eight warps per Q tile, two threads per row (its
+//                TMEM lane; 64 key columns each, row maxima exchanged in
+//                shared memory): masked row max, lazy rescale of O only when
+//                the max grows by more than 2^8, P = 2^(x - m) (fp32 exp2,
+//                packed to bf16) written back into the tile's S columns of
+//                TMEM, and the final 1/l normalisation and bf16 store.
+// TMEM (512 columns): S_A | S_B | O_A | O_B.  P_X overwrites the first 64
+// columns of S_X, so S_X(j+1) may only overwrite those after PV_X(j) is done;
+// S is issued as two 64-key halves, the upper half first, so that this wait
+// overlaps the upper half's MMAs.  Operands: Q, K (K-major, SW128) via
+// shared-memory descriptors, P from TMEM, V read MN-major (head_dim
+// contiguous), as stored.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -38,7 +44,8 @@ namespace {
 constexpr int kTcM = 128;                         // query rows per tile
 constexpr int kTcN = 128;                         // keys per KV tile
 constexpr int kTcBlocks = kTcN / kBlockSize;      // 8 blocks per KV tile
-constexpr int kTcWarps = 10;  // producer, MMA issuer, 8 softmax warps (2 per row quadrant)
+constexpr int kTcQTiles = 2;                      // query tiles per CTA (A, B)
+constexpr int kTcWarps = 2 + 8 * kTcQTiles;       // producer, MMA issuer, 8 softmax warps per tile
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;         // log2 of the largest stale-max factor
 
@@ -46,22 +53,19 @@ template <int D>
 struct TcCfg {
     static constexpr int kHalves = D / 64;             // 64-column (128-byte) halves of a row
     static constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes
-    static constexpr int kQBytes = kHalves * kHalfBytes;
+    static constexpr int kQBytes = kHalves * kHalfBytes;  // one Q tile
     static constexpr int kKBytes = kHalves * kHalfBytes;  // 128 keys x D (K or V tile)
-    static constexpr int kPBytes = 2 * kHalfBytes;        // 128 rows x 128 keys
-    // K and V live in separate rings: a K stage frees as soon as its S = Q K^T
-    // is done, so K runs a full tile further ahead of the MMA than V.
     static constexpr int kKStages = 2;
     static constexpr int kVStages = 2;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffK = kOffP + kPBytes;
+    static constexpr int kOffK = kOffQ + kTcQTiles * kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
     static constexpr int kBodyBytes = kOffV + kVStages * kKBytes;
     // at least 120 KB so that one CTA owns an SM (and all 512 TMEM columns)
     static constexpr int kSmemBytes = (kBodyBytes + 1024 > 120 * 1024) ? kBodyBytes + 1024 : 120 * 1024;
-    static constexpr uint32_t kTmemCols = 512;            // S0 | S1 | O
-    static constexpr uint32_t kColO = 256;
+    static constexpr uint32_t kTmemCols = 512;            // S_A | S_B | O_A | O_B
+    static constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x * kTcN); }
+    static constexpr uint32_t col_o(int x) { return static_cast<uint32_t>(kTcQTiles * kTcN + x * D); }
 };
 
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
@@ -71,6 +75,32 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
+}
+
+// The KV tiles one query tile needs, as a range [lo, hi) of tile indices.
+struct TileSpan {
+    int tok0, ntok;      // first token (within the sequence) and token count
+    int pos_min, pos_max;
+    int lo, hi;          // absolute KV tile indices
+};
+
+__device__ __forceinline__ TileSpan tile_span(int tok0, int q_len, int QT, int kv_len, int causal,
+                                              int window) {
+    TileSpan t;
+    t.tok0 = tok0;
+    t.ntok = max(0, min(QT, q_len - tok0));
+    const int off = kv_len - q_len;
+    t.pos_min = off + tok0;
+    t.pos_max = off + tok0 + t.ntok - 1;
+    const int key_hi = causal ? min(t.pos_max, kv_len - 1) : kv_len - 1;
+    const int key_lo = window > 0 ? max(0, t.pos_min - window + 1) : 0;
+    if (t.ntok > 0 && key_hi >= key_lo) {
+        t.lo = key_lo / kTcN;
+        t.hi = key_hi / kTcN + 1;
+    } else {
+        t.lo = t.hi = 0;
+    }
+    return t;
 }
 
 template <int D>
@@ -83,19 +113,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t bar_q;
-    __shared__ __align__(8) uint64_t bar_k[3];
-    __shared__ __align__(8) uint64_t bar_k_empty[3];
-    __shared__ __align__(8) uint64_t bar_v[2];
-    __shared__ __align__(8) uint64_t bar_v_empty[2];
-    __shared__ __align__(8) uint64_t bar_s_full[2];
-    __shared__ __align__(8) uint64_t bar_s_free[2];
-    __shared__ __align__(8) uint64_t bar_p_full;
-    __shared__ __align__(8) uint64_t bar_o_done;
+    __shared__ __align__(8) uint64_t bar_k[C::kKStages];
+    __shared__ __align__(8) uint64_t bar_k_empty[C::kKStages];
+    __shared__ __align__(8) uint64_t bar_v[C::kVStages];
+    __shared__ __align__(8) uint64_t bar_v_empty[C::kVStages];
+    __shared__ __align__(8) uint64_t bar_s_full[kTcQTiles];
+    __shared__ __align__(8) uint64_t bar_p_full[kTcQTiles];
+    __shared__ __align__(8) uint64_t bar_o_done[kTcQTiles];
+    __shared__ __align__(8) uint64_t bar_pair[kTcQTiles][4][3];  // per tile and quadrant: parity 0/1, final
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    __shared__ float s_red_max[2][2][kTcM];  // [tile parity][column half][row]
-    __shared__ float s_red_sum[2][kTcM];     // [column half][row]
-    __shared__ __align__(8) uint64_t bar_pair[4][3];  // per quadrant: tile parity 0/1, final
+    __shared__ float s_red_max[kTcQTiles][2][2][kTcM];  // [tile][parity][column half][row]
+    __shared__ float s_red_sum[kTcQTiles][2][kTcM];     // [tile][column half][row]
 
     pdl_wait();
     pdl_launch_dependents();
@@ -116,17 +145,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         kv_len = cap;
     }
     const int ntiles_q = (q_len + QT - 1) / QT;
-    if (static_cast<int>(blockIdx.x) >= ntiles_q) return;
-    const int qt = ntiles_q - 1 - static_cast<int>(blockIdx.x);  // heaviest tiles first
-    const int tok0 = qt * QT;
-    const int ntok = min(QT, q_len - tok0);
-    const int off = kv_len - q_len;
-    const int pos_min = off + tok0;
-    const int pos_max = off + tok0 + ntok - 1;
-    const int key_hi = a.causal ? min(pos_max, kv_len - 1) : kv_len - 1;
-    const int key_lo = a.window > 0 ? max(0, pos_min - a.window + 1) : 0;
-    const int t_begin = key_lo / kTcN;
-    const int n_tiles = key_hi >= key_lo ? key_hi / kTcN + 1 - t_begin : 0;
+    const int npairs = (ntiles_q + kTcQTiles - 1) / kTcQTiles;
+    if (static_cast<int>(blockIdx.x) >= npairs) return;
+    const int pr = npairs - 1 - static_cast<int>(blockIdx.x);  // heaviest pairs first
+    TileSpan span[kTcQTiles];
+#pragma unroll
+    for (int x = 0; x < kTcQTiles; ++x)
+        span[x] = tile_span((pr * kTcQTiles + x) * QT, q_len, QT, kv_len, a.causal, a.window);
+    // the CTA's KV range is the union of the two tiles' ranges; j below counts
+    // KV tiles from t_begin, and tile x is active for j in [jlo[x], jhi[x])
+    int t_begin = 1 << 30, t_end = 0;
+#pragma unroll
+    for (int x = 0; x < kTcQTiles; ++x) {
+        if (span[x].hi > span[x].lo) {
+            t_begin = min(t_begin, span[x].lo);
+            t_end = max(t_end, span[x].hi);
+        }
+    }
+    const int n_tiles = t_end > 0 ? t_end - t_begin : 0;
+    int jlo[kTcQTiles], jhi[kTcQTiles];
+#pragma unroll
+    for (int x = 0; x < kTcQTiles; ++x) {
+        jlo[x] = span[x].hi > span[x].lo ? span[x].lo - t_begin : 0;
+        jhi[x] = span[x].hi > span[x].lo ? span[x].hi - t_begin : 0;
+    }
     const int nblk_seq = (kv_len + kBlockSize - 1) / kBlockSize;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -141,14 +183,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&bar_v[i], 1);
             mbar_init(&bar_v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_s_full[i], 1);
-            mbar_init(&bar_s_free[i], 8);
+        for (int x = 0; x < kTcQTiles; ++x) {
+            mbar_init(&bar_s_full[x], 1);
+            mbar_init(&bar_p_full[x], 8);
+            mbar_init(&bar_o_done[x], 1);
+            for (int qd = 0; qd < 4; ++qd)
+                for (int i = 0; i < 3; ++i) mbar_init(&bar_pair[x][qd][i], 64);
         }
-        mbar_init(&bar_p_full, 8);
-        for (int qd = 0; qd < 4; ++qd)
-            for (int i = 0; i < 3; ++i) mbar_init(&bar_pair[qd][i], 64);
-        mbar_init(&bar_o_done, 1);
         s_fail = 0;
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
@@ -164,32 +205,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = s_tmem;
 
-    uint8_t* sQ = smem + C::kOffQ;
-    uint8_t* sP = smem + C::kOffP;
     const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (n_tiles > 0) {
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar_q, C::kHalves * 64 * 2 * G * QT);
+                int nq = 0;
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(sQ + h * C::kHalfBytes, &qmap, &bar_q, h * 64, kvh * G, q0 + tok0);
+                for (int x = 0; x < kTcQTiles; ++x) nq += span[x].ntok > 0 ? 1 : 0;
+                mbar_arrive_expect_tx(&bar_q, nq * C::kHalves * 64 * 2 * G * QT);
+#pragma unroll
+                for (int x = 0; x < kTcQTiles; ++x) {
+                    if (span[x].ntok <= 0) continue;
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(smem + C::kOffQ + x * C::kQBytes + h * C::kHalfBytes, &qmap, &bar_q,
+                                    h * 64, kvh * G, q0 + span[x].tok0);
+                }
             }
-            // order of loads: K_0, K_1, V_0, K_2, V_1, ... -- K one tile ahead of V
-            int ids_prev = 0;
+            // order of loads: K_0, K_1, V_0, K_2, V_1, ... -- K one tile ahead of V.
+            // Block ids: lane l holds block l % 8 of tile l / 8 of a group of four
+            // tiles; the next group is read one group ahead, so the table read is
+            // never on the load path.  An id is checked when its group comes up.
+            const int blk_end = min(nblk_seq, (t_begin + n_tiles) * kTcBlocks);
+            auto read_ids = [&](int grp) -> int {
+                const int blk = (t_begin + grp * 4) * kTcBlocks + lane;
+                return blk < blk_end ? __ldg(bt + blk) : 0;
+            };
+            auto check_ids = [&](int v) -> int {
+                if (v < 0 || v >= a.num_blocks) {
+                    flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                    v = 0;
+                }
+                return v;
+            };
+            int ids_cur = check_ids(read_ids(0));
+            int ids_next = read_ids(1);
+            int ids_old = 0;  // the group before ids_cur (V lags K by one tile)
             for (int j = 0; j <= n_tiles; ++j) {
-                int ids_cur = 0;
+                bool switched = false;
                 if (j < n_tiles) {
-                    const int blk0 = (t_begin + j) * kTcBlocks;
-                    if (lane < kTcBlocks && blk0 + lane < nblk_seq) {
-                        ids_cur = bt[blk0 + lane];
-                        if (ids_cur < 0 || ids_cur >= a.num_blocks) {
-                            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                            ids_cur = 0;
-                        }
+                    if (j > 0 && (j & 3) == 0) {
+                        ids_old = ids_cur;
+                        ids_cur = check_ids(ids_next);
+                        ids_next = read_ids((j >> 2) + 1);
+                        switched = true;
                     }
+                    const int blk0 = (t_begin + j) * kTcBlocks;
                     const int st = j % C::kKStages;
                     int ok = 1;
                     if (lane == 0) ok = mbar_wait(&bar_k_empty[st], ((j / C::kKStages) & 1) ^ 1) ? 1 : 0;
@@ -202,7 +265,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint8_t* sK = smem + C::kOffK + st * C::kKBytes;
                     int ids[kTcBlocks];
 #pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b) ids[b] = __shfl_sync(0xFFFFFFFFu, ids_cur, b);
+                    for (int b = 0; b < kTcBlocks; ++b)
+                        ids[b] = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + b);
                     if (lane == 0) {
                         fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&bar_k[st], nvalid * kBlockSize * D * 2);
@@ -229,9 +293,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int blk0 = (t_begin + i) * kTcBlocks;
                     const int nvalid = min(kTcBlocks, nblk_seq - blk0);
                     uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
+                    const int src = switched ? ids_old : ids_cur;
                     int ids[kTcBlocks];
 #pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b) ids[b] = __shfl_sync(0xFFFFFFFFu, ids_prev, b);
+                    for (int b = 0; b < kTcBlocks; ++b)
+                        ids[b] = __shfl_sync(0xFFFFFFFFu, src, (i & 3) * kTcBlocks + b);
                     if (lane == 0) {
                         fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&bar_v[st], nvalid * kBlockSize * D * 2);
@@ -245,61 +311,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     }
                 }
-                ids_prev = ids_cur;
             }
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
-        constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN, false, false);
+        constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN / 2, false, false);  // one 64-key half
         constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTcM, D, false, true);
         bool ok = n_tiles > 0 ? mbar_wait(&bar_q, 0) : true;
         ok = __all_sync(0xFFFFFFFFu, ok);
-        for (int j = 0; ok && j <= n_tiles; ++j) {
-            if (j < n_tiles) {
-                const int st = j & 1;
-                const int ks = j % C::kKStages;
-                bool r1 = mbar_wait(&bar_k[ks], (j / C::kKStages) & 1);
-                bool r2 = mbar_wait(&bar_s_free[st], ((j >> 1) & 1) ^ 1);
-                if (!__all_sync(0xFFFFFFFFu, r1 && r2) || *reinterpret_cast<volatile int*>(&s_fail)) { ok = false; break; }
-                tc::fence_after_sync();
+        auto active = [&](int x, int j) { return j >= jlo[x] && j < jhi[x]; };
+        // S_x(j) = Q_x K_j^T, upper 64 keys first: they do not overlap P_x(j-1),
+        // so they go while PV_x(j-1) may still be reading P; then wait for PV_x(j-1)
+        // and write the lower half
+        auto issue_s = [&](int x, int j) -> bool {
+            const int ks = j % C::kKStages;
+            const uint8_t* sQ = smem + C::kOffQ + x * C::kQBytes;
+            const uint8_t* sK = smem + C::kOffK + ks * C::kKBytes;
+            for (int part = 1; part >= 0; --part) {
+                if (part == 0 && j > jlo[x]) {
+                    const bool r = mbar_wait(&bar_o_done[x], (j - 1 - jlo[x]) & 1);
+                    if (!__all_sync(0xFFFFFFFFu, r)) return false;
+                    tc::fence_after_sync();
+                }
                 if (lane == 0) {
-                    const uint8_t* sK = smem + C::kOffK + ks * C::kKBytes;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int h = kk >> 2;
                         const uint32_t ko = (kk & 3) * 32;
                         const uint64_t ad = tc::smem_desc(smem_u32(sQ + h * C::kHalfBytes) + ko, 16, 1024);
-                        const uint64_t bd = tc::smem_desc(smem_u32(sK + h * C::kHalfBytes) + ko, 16, 1024);
-                        tc::mma_bf16(tmem + st * kTcN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+                        const uint64_t bd = tc::smem_desc(
+                            smem_u32(sK + h * C::kHalfBytes + part * (kTcN / 2) * 128) + ko, 16, 1024);
+                        tc::mma_bf16(tmem + C::col_s(x) + part * (kTcN / 2), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
                     }
-                    tc::commit(&bar_s_full[st]);
-                    tc::commit(&bar_k_empty[ks]);  // this K tile is no longer needed
                 }
                 __syncwarp();
             }
-            if (j >= 1) {
-                const int i = j - 1;
-                const int st = i % C::kVStages;
-                bool r1 = mbar_wait(&bar_p_full, i & 1);
-                bool r2 = mbar_wait(&bar_v[st], (i / C::kVStages) & 1);
-                if (!__all_sync(0xFFFFFFFFu, r1 && r2) || *reinterpret_cast<volatile int*>(&s_fail)) { ok = false; break; }
-                tc::fence_after_sync();
-                if (lane == 0) {
-                    const uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
+            if (lane == 0) tc::commit(&bar_s_full[x]);
+            __syncwarp();
+            return true;
+        };
+        // O_x += P_x(j) V_j with P read from the first 64 columns of S_x
+        auto issue_pv = [&](int x, int j) -> bool {
+            const int vs = j % C::kVStages;
+            const bool r1 = mbar_wait(&bar_p_full[x], (j - jlo[x]) & 1);
+            const bool r2 = mbar_wait(&bar_v[vs], (j / C::kVStages) & 1);
+            if (!__all_sync(0xFFFFFFFFu, r1 && r2)) return false;
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint8_t* sV = smem + C::kOffV + vs * C::kKBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kTcN / 16; ++kk) {
-                        const int h = kk >> 2;
-                        const uint32_t ko = (kk & 3) * 32;
-                        const uint64_t ad = tc::smem_desc(smem_u32(sP + h * C::kHalfBytes) + ko, 16, 1024);
-                        // V, MN-major: 16 keys per k-step = 2 groups of 8 rows (SBO 1024);
-                        // the two 64-column halves of head_dim are C::kHalfBytes apart (LBO)
-                        const uint64_t bd = tc::smem_desc(smem_u32(sV) + kk * 2048, C::kHalfBytes, 1024);
-                        tc::mma_bf16(tmem + C::kColO, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::commit(&bar_o_done);
-                    tc::commit(&bar_v_empty[st]);
+                for (int kk = 0; kk < kTcN / 16; ++kk) {
+                    // P column group kk holds keys 64 c + 32 h + 16 s with h = kk / 4,
+                    // c = (kk / 2) % 2, s = kk % 2 (the softmax layout below).
+                    // V, MN-major: 16 keys per k-step = 2 groups of 8 rows (SBO 1024);
+                    // the two 64-column halves of head_dim are C::kHalfBytes apart (LBO)
+                    const int vrow = 64 * ((kk >> 1) & 1) + 32 * (kk >> 2) + 16 * (kk & 1);
+                    const uint64_t bd = tc::smem_desc(smem_u32(sV) + vrow * 128, C::kHalfBytes, 1024);
+                    tc::mma_bf16_tmem_a(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, bd, kIdescPV,
+                                        (j > jlo[x] || kk > 0) ? 1u : 0u);
                 }
+                tc::commit(&bar_o_done[x]);
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; ok && j <= n_tiles; ++j) {
+            if (j < n_tiles) {
+                const int ks = j % C::kKStages;
+                const bool r = mbar_wait(&bar_k[ks], (j / C::kKStages) & 1);
+                if (!__all_sync(0xFFFFFFFFu, r) || *reinterpret_cast<volatile int*>(&s_fail)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                if (active(0, j) && !issue_s(0, j)) { ok = false; break; }
+                if (!active(1, j)) {
+                    if (lane == 0) tc::commit(&bar_k_empty[ks]);
+                    __syncwarp();
+                }
+            }
+            if (j >= 1 && active(1, j - 1)) {
+                if (!issue_pv(1, j - 1)) { ok = false; break; }
+                if (lane == 0) tc::commit(&bar_v_empty[(j - 1) % C::kVStages]);
                 __syncwarp();
+            }
+            if (j < n_tiles) {
+                if (active(1, j)) {
+                    if (!issue_s(1, j)) { ok = false; break; }
+                    if (lane == 0) tc::commit(&bar_k_empty[j % C::kKStages]);  // K_j no longer needed
+                    __syncwarp();
+                }
+                if (active(0, j)) {
+                    if (!issue_pv(0, j)) { ok = false; break; }
+                    if (!active(1, j)) {
+                        if (lane == 0) tc::commit(&bar_v_empty[j % C::kVStages]);
+                        __syncwarp();
+                    }
+                }
             }
         }
         if (!ok && lane == 0) {
@@ -308,74 +416,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // -------------------------------------------------------------- softmax
-        // Two warps share each row quadrant: warp w (2..9) reads TMEM lanes of
-        // quadrant w % 4 and owns key columns [64h, 64h + 64) and O columns
-        // [h D/2, (h+1) D/2) with h = (w - 2) / 4.  The pair exchanges row maxima
-        // through shared memory on a named barrier; row sums stay per half.
+        // Warp w (2..17) serves query tile x = (w - 2) / 8 and reads TMEM lane
+        // quadrant w % 4; two warps share each quadrant.  Half h = ((w - 2) / 4) % 2
+        // owns the S columns 64 c + 32 h + [0, 32) for c = 0, 1 (keys k0 + the
+        // same offsets) and O columns [h D/2, (h+1) D/2).  The pair exchanges row
+        // maxima through shared memory; row sums stay per half.  Scores are
+        // streamed from TMEM twice (max, then exponentials): P for chunk c goes
+        // to columns 32 h + 16 c + [0, 16), which this half has already read, so
+        // P_x fills columns [0, 64) of S_x.
+        const int sw = warp - 2;
+        const int x = sw >> 3;                     // query tile
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = (warp - 2) >> 2;          // key / O column half
+        const int half = (sw >> 2) & 1;            // key / O column half
         const int r = quad * 32 + lane;            // the row this thread owns
         const int t = r / G;
-        const bool row_ok = r < QT * G && t < ntok;
-        const int pos = off + tok0 + t;
+        const TileSpan sp = x ? span[1] : span[0];
+        const bool row_ok = r < QT * G && t < sp.ntok;
+        const int pos = sp.pos_min + t;
+        const int j0 = x ? jlo[1] : jlo[0];
+        const int nx = x ? jhi[1] - jlo[1] : jhi[0] - jlo[0];
         const float scale_log2 = a.sm_scale * 1.4426950408889634f;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        const int sm_tid = (warp - 2) * 32 + lane;  // 0..255
+        const uint32_t s_base = lane_base + C::col_s(x);
+        const int grp_tid = (sw & 7) * 32 + lane;  // 0..255 within the tile's softmax group
         // the two warps of this quadrant meet on an mbarrier (bounded wait):
         // slot 0/1 for the per-tile max exchange (by tile parity), 2 at the end
         auto pair_sync = [&](int slot, uint32_t parity) {
-            mbar_arrive(&bar_pair[quad][slot]);
-            return mbar_wait(&bar_pair[quad][slot], parity);
+            mbar_arrive(&bar_pair[x][quad][slot]);
+            return mbar_wait(&bar_pair[x][quad][slot], parity);
         };
         float m_used = -INFINITY;
         float l = 0.f;                             // this half's share of the row sum
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
+        for (int i = 0; i < nx; ++i) {
+            const int j = j0 + i;
             const int k0 = (t_begin + j) * kTcN;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_s_full[sb], (j >> 1) & 1)) ||
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_s_full[x], i & 1)) ||
                 *reinterpret_cast<volatile int*>(&s_fail)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            const uint32_t s_col = lane_base + sb * kTcN + half * 64;
-            const int kh = k0 + half * 64;          // first key of this half
-            const bool full_vis = (!a.causal || k0 + kTcN - 1 <= pos_min) && (k0 + kTcN <= kv_len) &&
-                                  (a.window <= 0 || k0 > pos_max - a.window);
-            float x[64];
-            tc::ld32(s_col, *reinterpret_cast<float(*)[32]>(x));
-            tc::ld32(s_col + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-            tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_s_free[sb]);  // S is in registers
+            const bool full_vis = (!a.causal || k0 + kTcN - 1 <= sp.pos_min) && (k0 + kTcN <= kv_len) &&
+                                  (a.window <= 0 || k0 > sp.pos_max - a.window);
             // Row max.  Tiles wholly visible to the CTA (all but the diagonal and
-            // the window edge) take the short path: the max of the raw scores,
-            // scaled once.  Masked tiles scale and mask every score here, so the
-            // exponential pass below reads them ready.
+            // the window edge) take the max of the raw scores, scaled once;
+            // masked tiles scale and mask every score.
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (full_vis) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], x[e]);
-            } else {
+            for (int c = 0; c < 2; ++c) {
+                float xs[32];
+                tc::ld32(s_base + 64 * c + 32 * half, xs);
+                tc::wait_ld();
+                if (full_vis) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const int key = kh + e;
-                    const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                     (a.window <= 0 || key > pos - a.window);
-                    x[e] = vis ? x[e] * scale_log2 : -INFINITY;
-                    m4[e & 3] = fmaxf(m4[e & 3], x[e]);
+                    for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], xs[e]);
+                } else {
+                    const int kb = k0 + 64 * c + 32 * half;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = kb + e;
+                        const bool vis = key < kv_len && (!a.causal || key <= pos) &&
+                                         (a.window <= 0 || key > pos - a.window);
+                        m4[e & 3] = fmaxf(m4[e & 3], vis ? xs[e] * scale_log2 : -INFINITY);
+                    }
                 }
             }
             float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             if (full_vis) mx *= scale_log2;  // scale_log2 > 0: the max commutes with it
-            s_red_max[sb][half][r] = mx;
-            if (!__all_sync(0xFFFFFFFFu, pair_sync(sb, (j >> 1) & 1))) {
+            s_red_max[x][i & 1][half][r] = mx;
+            if (!__all_sync(0xFFFFFFFFu, pair_sync(i & 1, (i >> 1) & 1))) {
                 ok = false;
                 break;
             }
-            mx = fmaxf(mx, s_red_max[sb][half ^ 1][r]);
+            mx = fmaxf(mx, s_red_max[x][i & 1][half ^ 1][r]);
             // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + kRescaleThreshold ||
@@ -387,8 +501,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 l *= alpha;
             }
             // keys past kv_len in the last tile: zero their V rows so that a
-            // NaN in an unused slot never meets a zero weight in the MMA
-            if (k0 + kTcN > kv_len) {
+            // NaN in an unused slot never meets a zero weight in the MMA.  The
+            // tile whose PV reads V_j first does it (A when it uses V_j).
+            const bool zero_v = k0 + kTcN > kv_len && (x == 0 || j < jlo[0] || j >= jhi[0]);
+            if (zero_v) {
                 const int st = j % C::kVStages;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_v[st], (j / C::kVStages) & 1))) {
                     ok = false;
@@ -397,84 +513,93 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
                 const int first = max(0, kv_len - k0);
                 // 8 warps x 32 lanes zero rows [first, 128) of every half
-                for (int row = first + (sm_tid >> 3); row < kTcN; row += 32) {
+                for (int row = first + (grp_tid >> 3); row < kTcN; row += 32) {
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h)
-                        *reinterpret_cast<uint4*>(sV + h * C::kHalfBytes + row * 128 + (sm_tid & 7) * 16) =
+                        *reinterpret_cast<uint4*>(sV + h * C::kHalfBytes + row * 128 + (grp_tid & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
             }
-            // PV_{j-1} must be done before O is rescaled or P is overwritten
-            if (j > 0) {
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done, (j - 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                if (__any_sync(0xFFFFFFFFu, need)) {
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        float v[32];
-                        const uint32_t col = lane_base + C::kColO + half * (D / 2) + c * 32;
-                        tc::ld32(col, v);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                        tc::st32(col, v);
-                    }
-                    tc::wait_st();
-                }
-            }
-            // P = 2^(x - m) in fp32 (the row sum l stays exact to fp32), packed
-            // to bf16 pairs into the swizzled K-major P tile (this half's keys)
+            // P = 2^(x - m) in fp32 (the row sum l stays exact to fp32), packed to
+            // bf16 pairs (the lower key in the low half)
             const float mu = m_used == -INFINITY ? 0.f : m_used;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
-            // p = 2^(score * scale - mu): one FMA and one exp2 per score on the
-            // short path (raw scores), one subtract on the masked path
-            const float sc = full_vis ? scale_log2 : 1.f;
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {              // 8 chunks of 8 keys
-                uint32_t pk[4];
+            for (int c = 0; c < 2; ++c) {
+                float xs[32];
+                tc::ld32(s_base + 64 * c + 32 * half, xs);
+                tc::wait_ld();
+                uint32_t pk[16];
+                if (full_vis) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float p0 = fast_exp2(fmaf(x[q8 * 8 + 2 * u], sc, -mu));
-                    const float p1 = fast_exp2(fmaf(x[q8 * 8 + 2 * u + 1], sc, -mu));
-                    s4[u] += p0 + p1;
-                    pk[u] = pack2<false>(p0, p1);
+                    for (int u = 0; u < 16; ++u) {
+                        const float p0 = fast_exp2(fmaf(xs[2 * u], scale_log2, -mu));
+                        const float p1 = fast_exp2(fmaf(xs[2 * u + 1], scale_log2, -mu));
+                        s4[u & 3] += p0 + p1;
+                        pk[u] = pack2<false>(p0, p1);
+                    }
+                } else {
+                    const int kb = k0 + 64 * c + 32 * half;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        float pp[2];
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            const int key = kb + 2 * u + v;
+                            const bool vis = key < kv_len && (!a.causal || key <= pos) &&
+                                             (a.window <= 0 || key > pos - a.window);
+                            pp[v] = vis ? fast_exp2(fmaf(xs[2 * u + v], scale_log2, -mu)) : 0.f;
+                        }
+                        s4[u & 3] += pp[0] + pp[1];
+                        pk[u] = pack2<false>(pp[0], pp[1]);
+                    }
                 }
-                *reinterpret_cast<uint4*>(sP + half * C::kHalfBytes + sw128(r, q8)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                tc::st16u(s_base + 32 * half + 16 * c, pk);
             }
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-            fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
+            // PV_x(j-1) is done (S_x(j) was issued after it), so O may be rescaled
+            if (i > 0 && __any_sync(0xFFFFFFFFu, need)) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    float v[32];
+                    const uint32_t col = lane_base + C::col_o(x) + half * (D / 2) + c * 32;
+                    tc::ld32(col, v);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                    tc::st32(col, v);
+                }
+            }
+            tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_p_full);
+            if (lane == 0) mbar_arrive(&bar_p_full[x]);
         }
-        if (ok && n_tiles > 0) {
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done, (n_tiles - 1) & 1));
+        if (ok && nx > 0) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done[x], (nx - 1) & 1));
             tc::fence_after_sync();
         }
         // every softmax thread reaches this exchange (failure or not; the wait is bounded)
-        s_red_sum[half][r] = l;
+        s_red_sum[x][half][r] = l;
         if (!__all_sync(0xFFFFFFFFu, pair_sync(2, 0))) ok = false;
-        const float l_row = l + s_red_sum[half ^ 1][r];
+        const float l_row = l + s_red_sum[x][half ^ 1][r];
         if (!ok) {
             if (lane == 0) {
                 flag_error(a.err, PKV_DEVERR_TIMEOUT);
                 atomicOr(&s_fail, 1);
             }
-        } else {
+        } else if (sp.ntok > 0) {
             // epilogue: this half's O columns / l -> bf16; lse by half 0
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                                  (static_cast<size_t>(q0 + tok0 + t) * a.hq + kvh * G + r % G) * D +
+                                  (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D +
                                   half * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 float v[32];
-                if (n_tiles > 0) {
-                    tc::ld32(lane_base + C::kColO + half * (D / 2) + c * 32, v);
+                if (nx > 0) {
+                    tc::ld32(lane_base + C::col_o(x) + half * (D / 2) + c * 32, v);
                     tc::wait_ld();
                 } else {
 #pragma unroll
@@ -492,7 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (row_ok && a.lse_out && half == 0)
-                a.lse_out[static_cast<size_t>(q0 + tok0 + t) * a.hq + kvh * G + r % G] =
+                a.lse_out[static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G] =
                     l_row > 0.f ? (m_used + __log2f(l_row)) * 0.6931471805599453f : -INFINITY;
         }
     }
@@ -521,7 +646,7 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs& a, const CUtensorMap& qmap, c
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(a.max_qtiles, a.hkv, a.num_seqs);
+    dim3 grid((a.max_qtiles + kTcQTiles - 1) / kTcQTiles, a.hkv, a.num_seqs);
     return launch_pdl(kern, grid, dim3(kTcThreads), C::kSmemBytes, stream, a, qmap, kmap, vmap);
 }
 
