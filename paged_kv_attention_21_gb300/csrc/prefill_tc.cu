@@ -28,9 +28,8 @@
 //                packed to bf16) written back into the tile's S columns of
 //                TMEM, and the final 1/l normalisation and bf16 store.
 // TMEM (512 columns): S_A | S_B | O_A | O_B.  P_X overwrites the first 64
-// columns of S_X, so S_X(j+1) may only overwrite those after PV_X(j) is done;
-// S is issued as two 64-key halves, the upper half first, so that this wait
-// overlaps the upper half's MMAs.  Operands: Q, K (K-major, SW128) via
+// columns of S_X, so S_X(j+1) is issued only after PV_X(j) is done; the other
+// tile's MMA sits between the two in the order above.  Operands: Q, K (K-major, SW128) via
 // shared-memory descriptors, P from TMEM, V read MN-major (head_dim
 // contiguous), as stored.
 #include "common.cuh"
@@ -315,38 +314,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
-        constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN / 2, false, false);  // one 64-key half
+        constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN, false, false);
         constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTcM, D, false, true);
         bool ok = n_tiles > 0 ? mbar_wait(&bar_q, 0) : true;
         ok = __all_sync(0xFFFFFFFFu, ok);
         auto active = [&](int x, int j) { return j >= jlo[x] && j < jhi[x]; };
-        // S_x(j) = Q_x K_j^T, upper 64 keys first: they do not overlap P_x(j-1),
-        // so they go while PV_x(j-1) may still be reading P; then wait for PV_x(j-1)
-        // and write the lower half
+        // S_x(j) = Q_x K_j^T once PV_x(j-1) is done (it reads P_x(j-1) from the
+        // columns S_x(j) overwrites).  A 128-key S is one N = 128 MMA per k-step:
+        // two N = 64 halves cost as much tensor time each as one N = 128.
         auto issue_s = [&](int x, int j) -> bool {
             const int ks = j % C::kKStages;
             const uint8_t* sQ = smem + C::kOffQ + x * C::kQBytes;
             const uint8_t* sK = smem + C::kOffK + ks * C::kKBytes;
-            for (int part = 1; part >= 0; --part) {
-                if (part == 0 && j > jlo[x]) {
-                    const bool r = mbar_wait(&bar_o_done[x], (j - 1 - jlo[x]) & 1);
-                    if (!__all_sync(0xFFFFFFFFu, r)) return false;
-                    tc::fence_after_sync();
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const int h = kk >> 2;
-                        const uint32_t ko = (kk & 3) * 32;
-                        const uint64_t ad = tc::smem_desc(smem_u32(sQ + h * C::kHalfBytes) + ko, 16, 1024);
-                        const uint64_t bd = tc::smem_desc(
-                            smem_u32(sK + h * C::kHalfBytes + part * (kTcN / 2) * 128) + ko, 16, 1024);
-                        tc::mma_bf16(tmem + C::col_s(x) + part * (kTcN / 2), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                }
-                __syncwarp();
+            if (j > jlo[x]) {
+                const bool r = mbar_wait(&bar_o_done[x], (j - 1 - jlo[x]) & 1);
+                if (!__all_sync(0xFFFFFFFFu, r)) return false;
+                tc::fence_after_sync();
             }
-            if (lane == 0) tc::commit(&bar_s_full[x]);
+            if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int h = kk >> 2;
+                    const uint32_t ko = (kk & 3) * 32;
+                    const uint64_t ad = tc::smem_desc(smem_u32(sQ + h * C::kHalfBytes) + ko, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(smem_u32(sK + h * C::kHalfBytes) + ko, 16, 1024);
+                    tc::mma_bf16(tmem + C::col_s(x), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&bar_s_full[x]);
+            }
             __syncwarp();
             return true;
         };
