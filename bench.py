@@ -46,6 +46,9 @@ def parse_args():
     p.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
                    help="workload: 2 Qwen2.5-3B decode (default), 3 Qwen3-4B decode+append, "
                         "4 Llama-3-8B mixed step, 5 FP8 two-layer decode")
+    p.add_argument("--part", choices=["step", "prefill"], default="step",
+                   help="step: the workload's whole step (default); prefill: the ragged causal "
+                        "prefill part of workload 4 alone, timed against the tensor-core peak")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU seconds the oracle baseline sample aims at")
@@ -100,6 +103,19 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel timed alone (the burst figure)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class ClockSampler:
@@ -494,11 +510,80 @@ def workload_config(W, extra=None):
     return cfg
 
 
+def main_prefill(args, rank, world, local):
+    """The prefill part of the Llama-3-8B-shaped mixed step on its own: 8 chunks
+    of 512 query tokens over cached prefixes U[0, 8192], 32/8 heads, D 128,
+    causal.  Each timed launch follows an L2 flush (a 256 MiB write)."""
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    P = PrefillPart(dev, rank)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        P.run()
+    torch.cuda.synchronize(dev)
+    K = max(1, args.steps)
+    times = []
+    sampler = ClockSampler(dev.index)
+    barrier(world)
+    for _ in range(K):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        P.run()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    ms = reduce_max(float(np.mean(times)), world)
+    flags = P.pkv.pkv_device_errors(reset=True)
+    if flags:
+        raise RuntimeError("device error word 0x%x after the prefill runs" % flags)
+    if rank != 0:
+        return
+    peak, kind = measured_tensor_peak()
+    tflops = P.flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "ragged causal chunked-prefill attention TFLOP/s on 1 GB300",
+        "value": round(tflops * world, 1),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) q/K/V, shared-prefix block tables",
+        "config": {"workload": P.spec.name, "num_q_heads": P.spec.num_q_heads,
+                   "num_kv_heads": P.spec.num_kv_heads, "head_dim": P.spec.head_dim,
+                   "q_tokens": P.tokens, "causal": True,
+                   "l2": "256 MiB write before every timed launch"},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "kernel": "prefill_tc_kernel (tcgen05, two query tiles per CTA)",
+                     "peak_source": "%s bf16_tflops (burst)" % kind,
+                     "algorithmic_flops_per_launch": int(P.flops),
+                     "avg_launch_ms": round(ms, 5),
+                     "p10_ms": round(float(np.percentile(times, 10)), 5),
+                     "p90_ms": round(float(np.percentile(times, 90)), 5)},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         return main_reference(args, rank, world, local)
+    if args.part == "prefill":
+        return main_prefill(args, rank, world, local)
     r = time_pkv(args, rank, world, local)
     if rank != 0:
         return

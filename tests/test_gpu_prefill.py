@@ -84,6 +84,23 @@ def test_prefill_masks(causal, window):
     assert_lse_close(lse, ref_lse, "prefill masks")
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (16, 2, 128), (64, 8, 64)])
+def test_short_multi_token_queries(hq, hkv, d):
+    """Speculative-verify shapes (infer-lab, "Technique" table: speculative
+    decoding): 2-8 new tokens per sequence after a long cached context, run
+    through the ragged prefill kernel and checked against the oracle."""
+    spec = _small(num_chunks=12, hq=hq, hkv=hkv, d=d, prefix_hi=3000, seed=11)
+    rng = np.random.default_rng(11)
+    q_lens = [int(v) for v in rng.integers(2, 9, 12)]
+    prefixes = [int(v) for v in np.repeat(rng.integers(100, 3001, 6), 2)]
+    pb = wl.make_prefill_batch(spec, "cpu", q_lens=q_lens, prefixes=prefixes)
+    out, lse = _gpu_prefill(spec, pb)
+    ref, ref_lse = _oracle_prefill(spec, pb)
+    assert_close(out, ref, "verify q_len 2-8, %d/%d/%d" % (hq, hkv, d))
+    assert_lse_close(lse, ref_lse, "verify")
+    assert pkv.pkv_device_errors() == 0
+
+
 def test_chunked_prefill_equals_one_shot():
     """infer-lab's invariant: chunked prefill == one-shot prefill.  The oracle
     holds it bit for bit; the kernel within the attention tolerance."""
