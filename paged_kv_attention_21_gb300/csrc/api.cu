@@ -91,11 +91,17 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
     const void* ptr;
     int64_t num_blocks;
-    int32_t hkv, d, fp8, dev;
+    int32_t hkv, d, fp8, dev, kind;
     bool operator==(const MapKey& o) const {
         return ptr == o.ptr && num_blocks == o.num_blocks && hkv == o.hkv && d == o.d &&
-               fp8 == o.fp8 && dev == o.dev;
+               fp8 == o.fp8 && dev == o.dev && kind == o.kind;
     }
+};
+
+// The two tiled views of a pool.
+enum MapKind {
+    kMapBlockRows = 0,  // {D, 16, Hkv, num_blocks}, box {inner, 16, 1, 1}
+    kMapTileRows = 1,   // bf16 only: {64, D/64, 16, Hkv, num_blocks}, box {64, D/64, 16, 1, 1}
 };
 
 struct MapEntry {
@@ -109,14 +115,19 @@ thread_local MapEntry g_maps[kMapCache];
 thread_local int g_maps_used = 0;
 thread_local uint64_t g_map_clock = 0;
 
-// The tiled view of one pool: dims (innermost first) {D, block_size, Hkv,
-// num_blocks}; box {inner, 16, 1, 1}.  bf16 rows are split into 64-element
-// boxes with the 128-byte swizzle; e4m3 rows are one unswizzled box.
-pkv_status pool_map(const void* pool, const pkv_cache_desc* desc, CUtensorMap* out) {
+// A tiled view of one pool.  kMapBlockRows: dims (innermost first) {D,
+// block_size, Hkv, num_blocks}, box {inner, 16, 1, 1}; bf16 rows are split
+// into 64-element boxes with the 128-byte swizzle, e4m3 rows are one
+// unswizzled box.  kMapTileRows (bf16): one box brings a whole (block, head)
+// tile, which costs the TMA unit about two thirds of two half-width boxes.
+pkv_status pool_map(const void* pool, const pkv_cache_desc* desc, CUtensorMap* out,
+                    MapKind kind = kMapBlockRows) {
     int dev = 0;
     cudaGetDevice(&dev);
-    const MapKey key{pool, desc->num_blocks, desc->num_kv_heads, desc->head_dim,
-                     desc->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 0, dev};
+    const int fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 0;
+    if (fp8) kind = kMapBlockRows;
+    const MapKey key{pool, desc->num_blocks, desc->num_kv_heads, desc->head_dim, fp8, dev,
+                     static_cast<int32_t>(kind)};
     for (int i = 0; i < g_maps_used; ++i) {
         if (g_maps[i].key == key) {
             g_maps[i].stamp = ++g_map_clock;
@@ -128,22 +139,35 @@ pkv_status pool_map(const void* pool, const pkv_cache_desc* desc, CUtensorMap* o
     if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const pkv::BoxShape box = pkv::kv_box_shape(desc->head_dim, key.fp8);
     const cuuint64_t elem = key.fp8 ? 1 : 2;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(desc->head_dim),
-                                static_cast<cuuint64_t>(desc->block_size),
-                                static_cast<cuuint64_t>(desc->num_kv_heads),
-                                static_cast<cuuint64_t>(desc->num_blocks)};
-    const cuuint64_t strides[3] = {dims[0] * elem, dims[0] * dims[1] * elem,
-                                   dims[0] * dims[1] * dims[2] * elem};
-    const cuuint32_t boxdim[4] = {static_cast<cuuint32_t>(box.inner),
-                                  static_cast<cuuint32_t>(desc->block_size), 1, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const cuuint64_t D = static_cast<cuuint64_t>(desc->head_dim);
+    const cuuint64_t rows = static_cast<cuuint64_t>(desc->block_size);
+    const cuuint64_t hkv = static_cast<cuuint64_t>(desc->num_kv_heads);
+    const cuuint64_t nb = static_cast<cuuint64_t>(desc->num_blocks);
     CUtensorMap map;
-    CUresult r = fn(&map,
-                    key.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                    const_cast<void*>(pool), dims, strides, boxdim, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    box.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (kind == kMapTileRows) {
+        // one box per (block, head): 16 rows x D/64 slices of 128 bytes, so a
+        // row's slices sit side by side (row r, slice h at 128 (r D/64 + h)),
+        // each swizzled by its 128-byte unit index
+        const cuuint64_t dims[5] = {64, D / 64, rows, hkv, nb};
+        const cuuint64_t strides[4] = {64 * elem, D * elem, rows * D * elem, hkv * rows * D * elem};
+        const cuuint32_t boxdim[5] = {64, static_cast<cuuint32_t>(D / 64),
+                                      static_cast<cuuint32_t>(rows), 1, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims, strides,
+               boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {D, rows, hkv, nb};
+        const cuuint64_t strides[3] = {D * elem, D * rows * elem, D * rows * hkv * elem};
+        const cuuint32_t boxdim[4] = {static_cast<cuuint32_t>(box.inner),
+                                      static_cast<cuuint32_t>(rows), 1, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = fn(&map, key.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void*>(pool), dims, strides, boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               box.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
     int slot = 0;
     if (g_maps_used < kMapCache) {
@@ -389,9 +413,9 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
             return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, ws.total);
     }
     CUtensorMap kmap, vmap;
-    st = pool_map(k_cache, desc, &kmap);
+    st = pool_map(k_cache, desc, &kmap, kMapTileRows);
     if (st != PKV_OK) return st;
-    st = pool_map(v_cache, desc, &vmap);
+    st = pool_map(v_cache, desc, &vmap, kMapTileRows);
     if (st != PKV_OK) return st;
     pkv::DecodeArgs a{};
     a.q = q;
@@ -739,9 +763,9 @@ extern "C" pkv_status pkv_decode_attention_static(
     st = static_scratch(&scratch);
     if (st != PKV_OK) return st;
     CUtensorMap kmap, vmap;
-    st = pool_map(k_cache, desc, &kmap);
+    st = pool_map(k_cache, desc, &kmap, kMapTileRows);
     if (st != PKV_OK) return st;
-    st = pool_map(v_cache, desc, &vmap);
+    st = pool_map(v_cache, desc, &vmap, kMapTileRows);
     if (st != PKV_OK) return st;
     uint8_t* wsb = static_cast<uint8_t*>(scratch);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -48,10 +48,8 @@ struct DecodeCfg {
     static constexpr int kElem = kFp8 ? 1 : 2;
     static constexpr int kTileBytes = kBlockSize * D * kElem;  // one block of one head
     static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
-    // bf16: 128-byte swizzled boxes of 64 elements; fp8: one unswizzled box
-    static constexpr int kBoxInner = kFp8 ? D : 64;
-    static constexpr int kBoxes = D / kBoxInner;
-    static constexpr int kBoxBytes = kBlockSize * kBoxInner * kElem;
+    // bf16: one 5-D box per tile (16 rows x D/64 swizzled 128-byte slices);
+    // fp8: one unswizzled 4-D box of 16 rows x D bytes
     static constexpr int kConvBytes = kFp8 ? 2 * kBlockSize * D * 2 : 0;  // f16 K + V
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
@@ -61,8 +59,20 @@ struct DecodeCfg {
     static constexpr int kSmemBytes = kBodyBytes + 1024;  // + alignment slack
 };
 
-// f16 staging of an fp8 tile: src [16][D] bytes (row-major) -> dst [D/64][16][64]
-// f16 with the 128-byte swizzle, the layout the bf16 path gets from TMA.
+// Byte offset of 16-byte chunk `chunk` (0 .. D/8 - 1) of row r in a 16 x D
+// 16-bit tile as it sits in shared memory: row r's D/64 slices of 128 bytes
+// are side by side (unit u = r D/64 + chunk / 8), and each unit's chunks are
+// swizzled by u % 8 -- the layout the 128-byte-swizzled 5-D TMA box writes
+// on a 1024-byte aligned tile.  Eight rows at one chunk fall in at most two
+// bank groups' worth of conflicts (D = 128) or none (D = 64).
+template <int D>
+__device__ __forceinline__ uint32_t kv_off(int r, int chunk) {
+    const int u = r * (D / 64) + (chunk >> 3);
+    return static_cast<uint32_t>(u * 128 + (((chunk & 7) ^ (u & 7)) << 4));
+}
+
+// f16 staging of an fp8 tile: src [16][D] bytes (row-major) -> dst in the
+// kv_off layout, the one the bf16 path gets from TMA.
 template <int D>
 __device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, int lane) {
     constexpr int kChunksPerRow = D / 16;
@@ -84,12 +94,19 @@ __device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* ds
             h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
         }
         const int d0 = cc * 2;  // destination 16-byte chunk (8 f16) index in the row
-        *reinterpret_cast<uint4*>(dst + (d0 >> 3) * 2048 + sw128(r, d0 & 7)) =
-            make_uint4(h[0], h[1], h[2], h[3]);
-        const int d1 = d0 + 1;
-        *reinterpret_cast<uint4*>(dst + (d1 >> 3) * 2048 + sw128(r, d1 & 7)) =
-            make_uint4(h[4], h[5], h[6], h[7]);
+        *reinterpret_cast<uint4*>(dst + kv_off<D>(r, d0)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + kv_off<D>(r, d0 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
+}
+
+// One (block, head) tile of K or V into shared memory.
+template <bool kFp8>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int kvh,
+                                          int block) {
+    if constexpr (kFp8)
+        tma_load_4d(dst, map, bar, 0, 0, kvh, block);
+    else
+        tma_load_5d(dst, map, bar, 0, 0, 0, kvh, block);
 }
 
 template <int D, bool kFp8>
@@ -172,11 +189,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             uint8_t* kdst = wbase + st * C::kStageBytes;
             uint8_t* vdst = kdst + C::kTileBytes;
             mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
-#pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx) {
-                tma_load_4d(kdst + bx * C::kBoxBytes, &kmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
-                tma_load_4d(vdst + bx * C::kBoxBytes, &vmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
-            }
+            load_tile<kFp8>(kdst, &kmap, &bars[warp][st], kvh, pb);
+            load_tile<kFp8>(vdst, &vmap, &bars[warp][st], kvh, pb);
         }
     }
 
@@ -244,8 +258,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int chunk = 2 * kk + csel;
                 uint32_t b00, b01, b10, b11;
-                ldmatrix_x4(b00, b01, b10, b11,
-                            kaddr + (chunk >> 3) * 2048 + sw128(tok, chunk & 7));
+                ldmatrix_x4(b00, b01, b10, b11, kaddr + kv_off<D>(tok, chunk));
                 mma_16816<kFp8>(sacc[0], qa[kk], b00, b01);
                 mma_16816<kFp8>(sacc[1], qa[kk], b10, b11);
             }
@@ -322,8 +335,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             for (int j = 0; j < D / 16; ++j) {
                 const int chunk = 2 * j + csel;
                 uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(v0, v1, v2, v3,
-                                  vaddr + (chunk >> 3) * 2048 + sw128(tok, chunk & 7));
+                ldmatrix_x4_trans(v0, v1, v2, v3, vaddr + kv_off<D>(tok, chunk));
                 v0 &= keep_lo;
                 v2 &= keep_lo;
                 v1 &= keep_hi;
@@ -341,11 +353,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             uint8_t* kdst = wbase + st * C::kStageBytes;
             uint8_t* vdst = kdst + C::kTileBytes;
             mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
-#pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx) {
-                tma_load_4d(kdst + bx * C::kBoxBytes, &kmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
-                tma_load_4d(vdst + bx * C::kBoxBytes, &vmap, &bars[warp][st], bx * C::kBoxInner, 0, kvh, pb);
-            }
+            load_tile<kFp8>(kdst, &kmap, &bars[warp][st], kvh, pb);
+            load_tile<kFp8>(vdst, &vmap, &bars[warp][st], kvh, pb);
         }
     }
     if (failed) {
