@@ -392,32 +392,42 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     }
     __syncthreads();
     const bool cta_failed = s_flag != 0;
-    const float vs = kFp8 ? a.v_scale[kvh] : 1.f;
     const size_t pair = static_cast<size_t>(seq) * a.hkv + kvh;
+    // per row, once: the warps' weights 2^(m_w - M) / L (v_scale folded in)
+    // replace s_m, and the row's lse goes to s_l[0]
+    if (threadIdx.x < 16) {
+        const int r = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][r]);
+        float f[kWarps];
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            f[w] = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
+            L += f[w] * s_l[w][r];
+        }
+        const float inv = L > 0.f ? (kFp8 ? a.v_scale[kvh] : 1.f) / L : 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s_m[w][r] = f[w] * inv;
+        s_l[0][r] = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
     if (!cta_failed) {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
             const int r = idx / D;
             const int d = idx % D;
-            float M = -INFINITY;
+            float ov = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][r]);
-            float L = 0.f, acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
-                L += f * s_l[w][r];
-                acc += f * comb[(w * 16 + r) * C::kCombStride + d];
-            }
-            const float ov = acc / L * vs;
-            const float lse = (M + __log2f(L)) * 0.6931471805599453f;
+            for (int w = 0; w < kWarps; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
             if (nsplit == 1) {
                 static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d] =
                     __float2bfloat16_rn(ov);
-                if (a.lse_out && d == 0) a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] = lse;
+                if (a.lse_out && d == 0) a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] = s_l[0][r];
             } else {
                 const size_t prow = (pair * a.max_splits + split) * G + r;
                 a.part_o[prow * D + d] = ov;
-                if (d == 0) a.part_lse[prow] = lse;
+                if (d == 0) a.part_lse[prow] = s_l[0][r];
             }
         }
     }

@@ -70,6 +70,41 @@ def test_odd_groups_and_lengths():
         _check_batch(spec, b, on_device(b), chunks=(0, 1, 2))
 
 
+@pytest.mark.parametrize("lens", [(1,), (16,) * 512, (5, 700, 16, 17, 1, 300, 33, 4000),
+                                  tuple(range(1, 514))])
+def test_automatic_plan_edges(lens):
+    """Batches at the edges of the automatic split plan: a single key, 512
+    one-block sequences, a mix of very short and long contexts, and 513
+    sequences of every length from 1 to 513."""
+    import dataclasses
+    spec = dataclasses.replace(wl.scaled(wl.QWEN25_3B, batch=len(lens)), fixed_lens=lens,
+                               ctx_lo=min(lens), ctx_hi=max(lens), seed=77)
+    b = wl.make_decode_batch(spec, "cpu")
+    _check_batch(spec, b, on_device(b), chunks=(0,))
+
+
+def test_sequence_without_keys():
+    """A sequence whose device-side length is 0 gets o = 0 and lse = -inf;
+    the others are unchanged."""
+    spec = wl.scaled(wl.QWEN3_4B, batch=9, ctx_hi=600, seed=5)
+    b = wl.make_decode_batch(spec, "cpu")
+    d = on_device(b)
+    desc = desc_for(spec, b.k_cache, b.tables_host)
+    ks, vs = _scales(b)
+    lens = b.lens_host.copy()
+    lens[3] = 0
+    d["context_lens"] = torch.from_numpy(lens).to(DEV)
+    out, lse, _ = gpu_decode(desc, d, b.max_context_len, spec.sm_scale)
+    keep = [i for i in range(len(lens)) if i != 3]
+    ref, ref_lse = oracle_decode(spec, u16(b.q[keep]), pool_np(b.k_cache), pool_np(b.v_cache),
+                                 b.tables_host[keep], b.lens_host[keep])
+    assert_close(out[keep], ref, "other sequences")
+    assert_lse_close(lse[keep], ref_lse, "other sequences")
+    assert torch.count_nonzero(out[3].float()).item() == 0
+    assert bool(torch.all(torch.isinf(lse[3]) & (lse[3] < 0)))
+    assert pkv.pkv_device_errors() == 0
+
+
 def test_poisoned_unused_slots_do_not_change_the_output():
     spec = wl.scaled(wl.QWEN25_3B, batch=6, ctx_hi=700)
     b = wl.make_decode_batch(spec, "cpu")
