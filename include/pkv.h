@@ -224,6 +224,43 @@ pkv_status pkv_merge_states(const float *o_parts, const float *lse_parts, int32_
                             int32_t num_rows, int32_t num_heads, int32_t head_dim, void *out,
                             float *lse_out, pkv_stream_t stream);
 
+/* ---- f2: cascade (shared-prefix) decode --------------------------------
+ * Decode for batches whose sequences share cached prefixes (infer-lab,
+ * "Technique" table: RadixAttention prefix caching, and its invariant
+ * "prefix-cached == uncached"; llm-infer, "What It Does": prefix caching for
+ * prompts that share leading blocks).  Sequences come in groups of
+ * consecutive indices; sequence s of group g attends the keys of its group's
+ * prefix (prefix_lens[g] tokens through prefix_tables[g]) followed by the
+ * keys of its own suffix (suffix_lens[s] tokens through suffix_tables[s]):
+ *   o = softmax(sm_scale * q k^T) v over prefix and suffix keys together,
+ * the same result as pkv_decode_attention over the concatenated table.  The
+ * group's queries attend the prefix in one pass that reads each prefix block
+ * once for the whole group; the suffixes go through the split-KV decode;
+ * the two (o, lse) states merge as in pkv_merge_states.
+ *   q, out    : bf16 [num_seqs][Hq][D].  lse_out: fp32 [num_seqs][Hq], nullable.
+ *   group_indptr (device) / group_indptr_host (host): int32 [num_groups+1],
+ *               0 = group_indptr[0] <= ... <= group_indptr[num_groups] = num_seqs.
+ *   prefix_tables: int32 [num_groups][max_blocks_per_seq]; prefix_lens (device)
+ *               and prefix_lens_host: int32 [num_groups], tokens in [0, table capacity].
+ *   suffix_tables: int32 [num_seqs][max_blocks_per_seq]; suffix_lens: int32
+ *               [num_seqs], each in [1, max_suffix_len] (the new token is in the suffix).
+ *   workspace : >= pkv_cascade_workspace_size(...) bytes, 256-byte aligned,
+ *               zero-filled before its first use (it holds the decode tickets).
+ * bf16 pools only (PKV_ERR_UNSUPPORTED for e4m3); no sliding window. */
+pkv_status pkv_cascade_decode(const pkv_cache_desc *desc, const void *q, const void *k_cache,
+                              const void *v_cache, int32_t num_groups, const int32_t *group_indptr,
+                              const int32_t *group_indptr_host, const int32_t *prefix_tables,
+                              const int32_t *prefix_lens, const int32_t *prefix_lens_host,
+                              int32_t num_seqs, const int32_t *suffix_tables,
+                              const int32_t *suffix_lens, int32_t max_suffix_len, float sm_scale,
+                              void *out, float *lse_out, void *workspace, size_t workspace_bytes,
+                              pkv_stream_t stream);
+
+/* Host: workspace bytes pkv_cascade_decode needs (planning uses the current
+ * device's SM count); 0 for invalid arguments. */
+size_t pkv_cascade_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
+                                  int32_t max_suffix_len);
+
 /* ---- decode with no workspace argument (no counterpart on the pages) ---
  * The same computation as pkv_decode_attention, for callers that cannot
  * allocate device memory at the point of the call -- for example code that

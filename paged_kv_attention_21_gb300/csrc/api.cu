@@ -666,6 +666,174 @@ pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_
     return PKV_OK;
 }
 
+// ---------------------------------------------------- cascade decode (f2) --
+//
+// The queries of a group of consecutive sequences that share a cached prefix
+// attend that prefix in one pass of the prefill kernel (not causal: every
+// query sees the whole prefix), which reads each prefix block once for the
+// whole group; each sequence's own suffix goes through the decode kernel;
+// the two fp32 (o, lse) states merge exactly as split-KV partials do.
+
+namespace {
+struct CascadeWs {
+    size_t o, lse, dec, dec_bytes, total;
+};
+CascadeWs cascade_ws_layout(const pkv_cache_desc* d, int num_seqs, int max_suffix_len, int sms) {
+    CascadeWs w{};
+    const size_t rows = size_t(num_seqs) * d->num_q_heads;
+    w.o = 0;
+    w.lse = align256(2 * rows * d->head_dim * sizeof(float));
+    w.dec = w.lse + align256(2 * rows * sizeof(float));
+    int c = 0, sp = 0;
+    w.dec_bytes = 0;
+    if (plan_decode(d, num_seqs, std::max(max_suffix_len, 1), -1, sms, 0, &c, &sp) == PKV_OK)
+        w.dec_bytes = decode_ws_layout(d, num_seqs, sp).total;
+    w.total = w.dec + w.dec_bytes;
+    return w;
+}
+}  // namespace
+
+size_t pkv_cascade_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_suffix_len) {
+    if (check_desc(desc) != PKV_OK || num_seqs <= 0 || max_suffix_len < 1) return 0;
+    int sms = 0;
+    if (device_state(nullptr, &sms) != PKV_OK) return 0;
+    return cascade_ws_layout(desc, num_seqs, max_suffix_len, sms).total;
+}
+
+pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                              const void* v_cache, int32_t num_groups, const int32_t* group_indptr,
+                              const int32_t* group_indptr_host, const int32_t* prefix_tables,
+                              const int32_t* prefix_lens, const int32_t* prefix_lens_host,
+                              int32_t num_seqs, const int32_t* suffix_tables,
+                              const int32_t* suffix_lens, int32_t max_suffix_len, float sm_scale,
+                              void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                              pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (desc->kv_dtype != PKV_KV_BF16) return fail(PKV_ERR_UNSUPPORTED, "cascade decode reads bf16 pools only");
+    if (num_seqs < 0 || num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range", num_seqs);
+    if (num_seqs == 0) return PKV_OK;
+    if (num_groups < 1 || num_groups > num_seqs)
+        return fail(PKV_ERR_INVALID_ARG, "num_groups %d outside [1, num_seqs]", num_groups);
+    if (!q || !k_cache || !v_cache || !group_indptr || !group_indptr_host || !prefix_tables || !prefix_lens ||
+        !prefix_lens_host || !suffix_tables || !suffix_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
+    const int cap = desc->max_blocks_per_seq * desc->block_size;
+    if (max_suffix_len < 1 || max_suffix_len > cap)
+        return fail(PKV_ERR_INVALID_ARG, "max_suffix_len %d outside [1, %d]", max_suffix_len, cap);
+    if (group_indptr_host[0] != 0 || group_indptr_host[num_groups] != num_seqs)
+        return fail(PKV_ERR_INVALID_ARG, "group_indptr_host must run from 0 to num_seqs");
+    int max_group = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        const int n = group_indptr_host[g + 1] - group_indptr_host[g];
+        if (n < 0) return fail(PKV_ERR_INVALID_ARG, "group_indptr_host decreases at %d", g);
+        max_group = std::max(max_group, n);
+        if (prefix_lens_host[g] < 0 || prefix_lens_host[g] > cap)
+            return fail(PKV_ERR_INVALID_ARG, "group %d: prefix length %d outside [0, %d]", g, prefix_lens_host[g], cap);
+    }
+    uint32_t* err = nullptr;
+    int sms = 0;
+    st = device_state(&err, &sms);
+    if (st != PKV_OK) return st;
+    const CascadeWs ws = cascade_ws_layout(desc, num_seqs, max_suffix_len, sms);
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", ws.total);
+    if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (workspace_bytes < ws.total)
+        return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, ws.total);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    float* o_parts = reinterpret_cast<float*>(wsb + ws.o);    // [2][num_seqs][Hq][D]
+    float* lse_parts = reinterpret_cast<float*>(wsb + ws.lse);  // [2][num_seqs][Hq]
+    const size_t rows = size_t(num_seqs) * desc->num_q_heads;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int G = desc->num_q_heads / desc->num_kv_heads;
+
+    // part 0: every group's queries over its shared prefix
+    {
+        const int QT = pkv::prefill_tc_q_tile(G);
+        CUtensorMap kmap, vmap, qmap;
+        st = pool_map(k_cache, desc, &kmap);
+        if (st != PKV_OK) return st;
+        st = pool_map(v_cache, desc, &vmap);
+        if (st != PKV_OK) return st;
+        st = q_map(q, num_seqs, desc, G, QT, &qmap);
+        if (st != PKV_OK) return st;
+        pkv::PrefillArgs a{};
+        a.q = q;
+        a.out = nullptr;
+        a.out_f32 = o_parts;
+        a.lse_out = lse_parts;
+        a.qo_indptr = group_indptr;
+        a.kv_lens = prefix_lens;
+        a.block_tables = prefix_tables;
+        a.err = err;
+        a.num_seqs = num_groups;
+        a.hq = desc->num_q_heads;
+        a.hkv = desc->num_kv_heads;
+        a.group = G;
+        a.d = desc->head_dim;
+        a.mbps = desc->max_blocks_per_seq;
+        a.causal = 0;
+        a.window = -1;
+        a.max_qtiles = (max_group + QT - 1) / QT;
+        a.q_tile = QT;
+        a.total_q = num_seqs;
+        a.num_blocks = desc->num_blocks;
+        a.sm_scale = sm_scale;
+        if (a.max_qtiles > 0) {
+            cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
+        }
+    }
+    // part 1: each sequence over its own suffix
+    {
+        int chunk = 0, splits = 0;
+        st = plan_decode(desc, num_seqs, max_suffix_len, -1, sms, 0, &chunk, &splits);
+        if (st != PKV_OK) return st;
+        const DecodeWs dws = decode_ws_layout(desc, num_seqs, splits);
+        CUtensorMap kmap, vmap;
+        st = pool_map(k_cache, desc, &kmap, kMapTileRows);
+        if (st != PKV_OK) return st;
+        st = pool_map(v_cache, desc, &vmap, kMapTileRows);
+        if (st != PKV_OK) return st;
+        uint8_t* dwb = wsb + ws.dec;
+        pkv::DecodeArgs a{};
+        a.q = q;
+        a.out = nullptr;
+        a.out_f32 = o_parts + rows * desc->head_dim;
+        a.lse_out = lse_parts + rows;
+        a.block_tables = suffix_tables;
+        a.context_lens = suffix_lens;
+        a.counters = dws.total ? reinterpret_cast<uint32_t*>(dwb + dws.counters) : nullptr;
+        a.part_lse = dws.total ? reinterpret_cast<float*>(dwb + dws.lse) : nullptr;
+        a.part_o = dws.total ? reinterpret_cast<float*>(dwb + dws.o) : nullptr;
+        a.err = err;
+        a.num_seqs = num_seqs;
+        a.hq = desc->num_q_heads;
+        a.hkv = desc->num_kv_heads;
+        a.group = G;
+        a.d = desc->head_dim;
+        a.mbps = desc->max_blocks_per_seq;
+        a.window = -1;
+        a.chunk_blocks = chunk;
+        a.max_splits = splits;
+        a.max_ctx = max_suffix_len;
+        a.fp8 = 0;
+        a.num_blocks = desc->num_blocks;
+        a.sm_scale = sm_scale;
+        cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
+    }
+    // the two states, merged per (sequence, head)
+    pkv::MergeArgs m{o_parts, lse_parts, out, lse_out, 2, num_seqs, desc->num_q_heads, desc->head_dim};
+    cudaError_t e = pkv::launch_merge(m, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cascade merge launch");
+    return PKV_OK;
+}
+
 pkv_status pkv_device_errors(uint32_t* flags_out, int32_t reset) {
     g_last_error[0] = 0;
     if (!flags_out) return fail(PKV_ERR_INVALID_ARG, "flags_out is NULL");

@@ -143,9 +143,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     const int lo = (a.window > 0 && ctx > a.window) ? ctx - a.window : 0;
     if (ctx <= 0) {  // no visible key: o = 0, lse = -inf
         if (split == 0) {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
-                               (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
-            for (int i = threadIdx.x; i < G * D; i += kThreads) o[i] = __float2bfloat16_rn(0.f);
+            const size_t o0 = (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
+            for (int i = threadIdx.x; i < G * D; i += kThreads) {
+                if (a.out_f32)
+                    a.out_f32[o0 + i] = 0.f;
+                else
+                    static_cast<__nv_bfloat16*>(a.out)[o0 + i] = __float2bfloat16_rn(0.f);
+            }
             if (a.lse_out && threadIdx.x < G)
                 a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + threadIdx.x] = -INFINITY;
         }
@@ -421,8 +425,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
             if (nsplit == 1) {
-                static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d] =
-                    __float2bfloat16_rn(ov);
+                const size_t oi = (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d;
+                if (a.out_f32)
+                    a.out_f32[oi] = ov;
+                else
+                    static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(ov);
                 if (a.lse_out && d == 0) a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] = s_l[0][r];
             } else {
                 const size_t prow = (pair * a.max_splits + split) * G + r;
@@ -509,10 +516,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         }
         const float W = rowW[r];
         const float inv = W > 0.f ? 1.f / W : 0.f;
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
-                            (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + c4 * 4;
-        *reinterpret_cast<uint2*>(ob) =
-            make_uint2(pack2<false>(acc.x * inv, acc.y * inv), pack2<false>(acc.z * inv, acc.w * inv));
+        const size_t oi = (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + c4 * 4;
+        if (a.out_f32) {
+            *reinterpret_cast<float4*>(a.out_f32 + oi) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else {
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
+                make_uint2(pack2<false>(acc.x * inv, acc.y * inv), pack2<false>(acc.z * inv, acc.w * inv));
+        }
         if (a.lse_out && c4 == 0)
             a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] =
                 W > 0.f ? rowM[r] + __logf(W) : -INFINITY;

@@ -63,6 +63,7 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 struct DecodeArgs {
     const void* q;
     void* out;
+    float* out_f32;  // non-null: fp32 output (an (o, lse) state to merge) instead of bf16 out
     float* lse_out;
     const int32_t* block_tables;
     const int32_t* context_lens;
@@ -83,6 +84,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CU
 struct PrefillArgs {
     const void* q;
     void* out;
+    float* out_f32;  // non-null: fp32 output (an (o, lse) state to merge) instead of bf16 out
     float* lse_out;
     const int32_t* qo_indptr;
     const int32_t* kv_lens;

@@ -585,11 +585,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 atomicOr(&s_fail, 1);
             }
         } else if (sp.ntok > 0) {
-            // epilogue: this half's O columns / l -> bf16; lse by half 0
+            // epilogue: this half's O columns / l -> bf16 (or fp32); lse by half 0
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                                  (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D +
-                                  half * (D / 2);
+            const size_t orow0 = (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D + half * (D / 2);
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + orow0;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 float v[32];
@@ -600,7 +599,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0.f;
                 }
-                if (row_ok) {
+                if (row_ok && a.out_f32) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(a.out_f32 + orow0 + c * 32 + e) =
+                            make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+                } else if (row_ok) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         *reinterpret_cast<uint4*>(orow + c * 32 + e) =
