@@ -79,13 +79,13 @@ def _load():
         lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
         lib.orc_rope_table.argtypes = [f32, i32, i32, P]
         lib.orc_rope_table.restype = None
-        lib.orc_append_rope.argtypes = [i32, i32, i32, i32, i32, i64, i32, P, P, P, P, P, i32,
-                                        P, P, i32, P, P, P, P, i32]
+        lib.orc_append_rope.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32, P, P, P, P, P,
+                                        i32, P, P, i32, P, P, P, P, i32]
         lib.orc_append_rope.restype = ctypes.c_int
         lib.orc_gather_kv.argtypes = [i32, i32, i32, i32, i64, i32, P, P, P, i32, P]
         lib.orc_gather_kv.restype = ctypes.c_int
         lib.orc_paged_attention.argtypes = [i32, i32, i32, i32, i32, i64, i32, P, P, P, P, P,
-                                            i32, P, P, P, f32, i32, i32, P, P, i32, i32]
+                                            i32, P, P, P, f32, i32, i32, i32, P, P, P, i32, i32]
         lib.orc_paged_attention.restype = ctypes.c_int
         lib.orc_copy_blocks.argtypes = [P, i64, i64, P, P, i32]
         lib.orc_copy_blocks.restype = ctypes.c_int
@@ -148,7 +148,7 @@ def rope_table(theta: float, rotary_dim: int, max_pos: int) -> np.ndarray:
 
 def append_rope(*, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, k_cache, v_cache,
                 block_tables, token_to_seq, positions, k_new, v_new, q=None, cos_sin=None,
-                k_scale=None, v_scale=None):
+                k_scale=None, v_scale=None, ring_blocks=0):
     """Host append + RoPE.  Mutates k_cache / v_cache (numpy, uint16 for bf16
     or uint8 for e4m3, shape [num_blocks][Hkv][bs][D]) and returns the rotated
     q (a new uint16 array) or None."""
@@ -166,7 +166,7 @@ def append_rope(*, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, k_
     vs = None if v_scale is None else _c(v_scale, np.float32)
     max_pos = 0 if cs is None else cs.shape[0]
     rc = lib.orc_append_rope(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype,
-                             k_cache.shape[0], mbps, _ptr(k_cache), _ptr(v_cache), _ptr(ks),
+                             k_cache.shape[0], mbps, int(ring_blocks), _ptr(k_cache), _ptr(v_cache), _ptr(ks),
                              _ptr(vs), _ptr(bt), num_seqs, _ptr(tts), _ptr(pos), len(pos),
                              _ptr(kn), _ptr(vn), _ptr(qo), _ptr(cs), max_pos)
     if rc != 0:
@@ -204,7 +204,8 @@ def gather_kv(cache, block_tables, lens, *, block_size):
 
 def paged_attention(*, q, k_cache, v_cache, block_tables, qo_indptr, kv_lens, num_q_heads,
                     num_kv_heads, sm_scale, causal=True, window=-1, kv_dtype=KV_BF16,
-                    k_scale=None, v_scale=None, precision=32, nthreads=1, with_lse=True):
+                    k_scale=None, v_scale=None, precision=32, nthreads=1, with_lse=True,
+                    ring_blocks=0, sinks=None):
     """Ragged softmax attention over the paged cache.
 
     q: uint16 bf16 bits [T][Hq][D].  Returns (out fp32 [T][Hq][D], lse fp32
@@ -226,7 +227,9 @@ def paged_attention(*, q, k_cache, v_cache, block_tables, qo_indptr, kv_lens, nu
     rc = lib.orc_paged_attention(num_q_heads, hkv, d, bs, kv_dtype, nb, bt.shape[1],
                                  _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs), _ptr(bt),
                                  len(kl), _ptr(qo), _ptr(kl), _ptr(q), float(sm_scale),
-                                 int(causal), int(window), _ptr(out), _ptr(lse), int(precision),
+                                 int(causal), int(window), int(ring_blocks),
+                                 _ptr(None if sinks is None else _c(sinks, np.float32)),
+                                 _ptr(out), _ptr(lse), int(precision),
                                  int(nthreads))
     if rc != 0:
         raise ValueError("oracle paged_attention failed (rc=%d)" % rc)

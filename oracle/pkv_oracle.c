@@ -165,12 +165,14 @@ static void rope_rotate(const uint16_t *x, int D, const float *cs, float *outv) 
 /* Writes each new token's K and V into its slot of the paged cache and
  * rotates q in place.  Token i belongs to sequence token_to_seq[i] and sits
  * at position positions[i]; its slot is block block_tables[s][p / bs],
- * row p % bs.  K is rotated (when cos_sin != NULL) then rounded to bf16, or
+ * row p % bs -- or, with a ring of ring_blocks > 0 blocks per sequence (the
+ * sliding-window cache of RustInfer's "Status"), block
+ * block_tables[s][(p / bs) % ring_blocks].  K is rotated (when cos_sin != NULL) then rounded to bf16, or
  * divided by k_scale[h] and encoded as e4m3.  V is copied (bf16) or divided
  * by v_scale[h] and encoded.  Returns 0, or -1 on an out-of-range index (no
  * write happens for that token). */
 int orc_append_rope(int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t kv_dtype,
-                    int64_t num_blocks, int32_t max_blocks_per_seq,
+                    int64_t num_blocks, int32_t max_blocks_per_seq, int32_t ring_blocks,
                     void *k_cache, void *v_cache, const float *k_scale, const float *v_scale,
                     const int32_t *block_tables, int32_t num_seqs,
                     const int32_t *token_to_seq, const int32_t *positions, int32_t num_tokens,
@@ -182,9 +184,10 @@ int orc_append_rope(int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t kv_d
     for (int32_t i = 0; i < num_tokens; ++i) {
         int32_t s = token_to_seq[i];
         int32_t p = positions[i];
-        if (s < 0 || s >= num_seqs || p < 0 || p / bs >= max_blocks_per_seq ||
+        int32_t b = ring_blocks > 0 ? (p / bs) % ring_blocks : p / bs;
+        if (s < 0 || s >= num_seqs || p < 0 || b >= max_blocks_per_seq ||
             (cos_sin && p >= max_pos)) { rc = -1; continue; }
-        int32_t blk = block_tables[(size_t)s * max_blocks_per_seq + p / bs];
+        int32_t blk = block_tables[(size_t)s * max_blocks_per_seq + b];
         if (blk < 0 || (int64_t)blk >= num_blocks) { rc = -1; continue; }
         int32_t slot = p % bs;
         const float *cs = cos_sin ? cos_sin + (size_t)p * (D / 2) * 2 : NULL;
@@ -277,6 +280,8 @@ typedef struct {
     const uint16_t *q;
     float sm_scale;
     int32_t causal, window, precision;
+    int32_t ring_blocks;     /* > 0: key t sits in table entry (t / bs) % ring_blocks */
+    const float *sinks;      /* nullable: per query head sink logit */
     float *out, *lse;
     const int32_t *tok_seq; /* query token -> sequence, filled by the caller */
     int64_t units;          /* num_q_tokens * Hq */
@@ -288,7 +293,8 @@ typedef struct {
  * with the per-head scale for e4m3). */
 static float kv_elem(const attn_job *J, const void *cache, const float *scale,
                      int32_t s, int32_t t, int32_t h, int32_t d, int *err) {
-    int32_t blk = J->block_tables[(size_t)s * J->max_blocks_per_seq + t / J->bs];
+    int32_t b = J->ring_blocks > 0 ? (t / J->bs) % J->ring_blocks : t / J->bs;
+    int32_t blk = J->block_tables[(size_t)s * J->max_blocks_per_seq + b];
     if (blk < 0 || (int64_t)blk >= J->num_blocks) { *err = 1; return 0.0f; }
     size_t idx = (((size_t)blk * J->Hkv + h) * J->bs + (t % J->bs)) * J->D + d;
     if (J->kv_dtype == ORC_KV_BF16) return orc_bf16_to_f32(((const uint16_t *)cache)[idx]);
@@ -299,7 +305,9 @@ static float kv_elem(const attn_job *J, const void *cache, const float *scale,
  * definition over the keys the mask leaves visible.
  *   l_t = sm_scale * sum_d q[d] k_t[d]
  *   m = max_t l_t,  e_t = exp(l_t - m),  L = sum_t e_t
- *   o = (sum_t e_t v_t) / L,  lse = m + ln L                                 */
+ *   o = (sum_t e_t v_t) / L,  lse = m + ln L
+ * With a sink logit s for the head (a softmax entry whose value is zero):
+ *   m = max(s, max_t l_t),  L = exp(s - m) + sum_t e_t.                      */
 static void attend_one_f32(attn_job *J, int64_t unit, float *logit, float *acc) {
     int32_t i = (int32_t)(unit / J->Hq);
     int32_t h = (int32_t)(unit % J->Hq);
@@ -316,9 +324,10 @@ static void attend_one_f32(attn_job *J, int64_t unit, float *logit, float *acc) 
     const uint16_t *qv = J->q + ((size_t)i * J->Hq + h) * J->D;
     float *o = J->out + ((size_t)i * J->Hq + h) * J->D;
     int err = 0;
+    const float sink = J->sinks ? J->sinks[h] : -INFINITY;
     if (hi < lo) {
         for (int d = 0; d < J->D; ++d) o[d] = 0.0f;
-        if (J->lse) J->lse[(size_t)i * J->Hq + h] = -INFINITY;
+        if (J->lse) J->lse[(size_t)i * J->Hq + h] = sink;
         return;
     }
     int32_t n = hi - lo + 1;
@@ -330,7 +339,8 @@ static void attend_one_f32(attn_job *J, int64_t unit, float *logit, float *acc) 
     }
     float m = logit[0];
     for (int32_t t = 1; t < n; ++t) if (logit[t] > m) m = logit[t];
-    float L = 0.0f;
+    if (sink > m) m = sink;
+    float L = sink == -INFINITY ? 0.0f : expf(sink - m);
     for (int32_t t = 0; t < n; ++t) { logit[t] = expf(logit[t] - m); L += logit[t]; }
     for (int d = 0; d < J->D; ++d) acc[d] = 0.0f;
     for (int32_t t = 0; t < n; ++t)
@@ -358,9 +368,10 @@ static void attend_one_f64(attn_job *J, int64_t unit, double *logit, double *acc
     const uint16_t *qv = J->q + ((size_t)i * J->Hq + h) * J->D;
     float *o = J->out + ((size_t)i * J->Hq + h) * J->D;
     int err = 0;
+    const double sink = J->sinks ? (double)J->sinks[h] : -INFINITY;
     if (hi < lo) {
         for (int d = 0; d < J->D; ++d) o[d] = 0.0f;
-        if (J->lse) J->lse[(size_t)i * J->Hq + h] = -INFINITY;
+        if (J->lse) J->lse[(size_t)i * J->Hq + h] = (float)sink;
         return;
     }
     int32_t n = hi - lo + 1;
@@ -373,7 +384,8 @@ static void attend_one_f64(attn_job *J, int64_t unit, double *logit, double *acc
     }
     double m = logit[0];
     for (int32_t t = 1; t < n; ++t) if (logit[t] > m) m = logit[t];
-    double L = 0.0;
+    if (sink > m) m = sink;
+    double L = sink == -INFINITY ? 0.0 : exp(sink - m);
     for (int32_t t = 0; t < n; ++t) { logit[t] = exp(logit[t] - m); L += logit[t]; }
     for (int d = 0; d < J->D; ++d) acc[d] = 0.0;
     for (int32_t t = 0; t < n; ++t)
@@ -388,6 +400,7 @@ static void *attn_worker(void *arg) {
     attn_job *J = (attn_job *)arg;
     int32_t max_len = 0;
     for (int32_t s = 0; s < J->num_seqs; ++s) if (J->kv_lens[s] > max_len) max_len = J->kv_lens[s];
+    if (J->window > 0 && J->window < max_len) max_len = J->window;
     size_t n = (size_t)(max_len > 0 ? max_len : 1);
     if (J->precision == 64) {
         double *logit = (double *)malloc(sizeof(double) * n);
@@ -409,8 +422,11 @@ static void *attn_worker(void *arg) {
  * [qo_indptr[s], qo_indptr[s+1]) and kv_lens[s] cached keys; its query i sits
  * at position kv_lens[s] - q_len + (i - qo_indptr[s]).  Decode is the case
  * q_len = 1 for every sequence.  q: bf16 [T][Hq][D]; out: fp32 [T][Hq][D];
- * lse (nullable): fp32 [T][Hq].  Units (token, head) are spread over
- * nthreads threads; the result does not depend on nthreads.
+ * lse (nullable): fp32 [T][Hq].  ring_blocks > 0: the sequence's cache is a
+ * ring of that many blocks (key t in table entry (t / bs) % ring_blocks); a
+ * window is then required and its keys must fit the ring.  sinks (nullable):
+ * fp32 [Hq] sink logits.  Units (token, head) are spread over nthreads
+ * threads; the result does not depend on nthreads.
  * Returns 0; -1 on a bad argument; 1 if a block id was out of range. */
 int orc_paged_attention(int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t kv_dtype,
                         int64_t num_blocks, int32_t max_blocks_per_seq,
@@ -419,12 +435,17 @@ int orc_paged_attention(int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t 
                         const int32_t *block_tables, int32_t num_seqs,
                         const int32_t *qo_indptr, const int32_t *kv_lens,
                         const uint16_t *q, float sm_scale, int32_t causal, int32_t window,
+                        int32_t ring_blocks, const float *sinks,
                         float *out, float *lse, int32_t precision, int32_t nthreads) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || bs <= 0 || num_seqs < 0) return -1;
+    if (ring_blocks < 0 || ring_blocks > max_blocks_per_seq) return -1;
+    /* a window spans at most (window - 1 + bs - 1) / bs + 1 blocks */
+    if (ring_blocks > 0 && (window <= 0 || (window - 1 + bs - 1) / bs + 1 > ring_blocks)) return -1;
     int32_t T = qo_indptr[num_seqs];
     for (int32_t s = 0; s < num_seqs; ++s) {
         if (qo_indptr[s + 1] < qo_indptr[s]) return -1;
-        if (kv_lens[s] < 0 || (kv_lens[s] + bs - 1) / bs > max_blocks_per_seq) return -1;
+        if (kv_lens[s] < 0 || (ring_blocks == 0 && (kv_lens[s] + bs - 1) / bs > max_blocks_per_seq))
+            return -1;
     }
     int32_t *tok_seq = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
     if (!tok_seq) return -2;
@@ -444,6 +465,7 @@ int orc_paged_attention(int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t 
         J->block_tables = block_tables; J->num_seqs = num_seqs;
         J->qo_indptr = qo_indptr; J->kv_lens = kv_lens; J->q = q; J->sm_scale = sm_scale;
         J->causal = causal; J->window = window; J->precision = precision;
+        J->ring_blocks = ring_blocks; J->sinks = sinks;
         J->out = out; J->lse = lse; J->tok_seq = tok_seq; J->units = units;
         J->begin = units * w / nthreads;
         J->end = units * (w + 1) / nthreads;

@@ -530,3 +530,94 @@ def test_copy_blocks_matches_numpy_assignment():
     ref[dst] = ref[src]
     oracle.copy_blocks(pool, src, dst)
     assert np.array_equal(pool, ref)
+
+
+# ---------------------------------------------- sinks and the ring cache --
+
+def test_sinks_equal_softmax_with_an_extra_zero_value_entry():
+    """A sink logit s joins the softmax with a zero value vector: scipy's
+    softmax / logsumexp over [logits, s] in float64, dropping the sink's row."""
+    rng = np.random.default_rng(30)
+    hq, hkv, d = 8, 2, 64
+    case = PagedCase(rng, [1, 40, 130], hq, hkv, d)
+    sinks = np.array([-3.0, 0.0, 1.5, 4.0, -np.inf, 2.0, 8.0, -1.0], np.float32)
+    sm = 0.125
+    out, lse = oracle.paged_attention(**case.oracle_kwargs(), sm_scale=sm, sinks=sinks)
+    G = hq // hkv
+    for s in range(3):
+        K, V = case.k_f64(s), case.v_f64(s)
+        qv = bits_to_f64(case.q[s])
+        for h in range(hq):
+            logits = np.append(sm * (K[:, h // G, :] @ qv[h]), float(sinks[h]))
+            p = scipy.special.softmax(logits)
+            ref = p[:-1] @ V[:, h // G, :]
+            assert np.abs(out[s, h] - ref).max() < 2e-6
+            assert abs(lse[s, h] - scipy.special.logsumexp(logits)) < 2e-5
+
+
+def test_sink_of_minus_infinity_changes_no_bit_and_a_large_sink_takes_the_mass():
+    rng = np.random.default_rng(31)
+    case = PagedCase(rng, [50, 7], 4, 2, 32)
+    o0, l0 = oracle.paged_attention(**case.oracle_kwargs(), sm_scale=0.2)
+    o1, l1 = oracle.paged_attention(**case.oracle_kwargs(), sm_scale=0.2,
+                                    sinks=np.full(4, -np.inf, np.float32))
+    assert np.array_equal(o0.view(np.uint32), o1.view(np.uint32))
+    assert np.array_equal(l0.view(np.uint32), l1.view(np.uint32))
+    o2, l2 = oracle.paged_attention(**case.oracle_kwargs(), sm_scale=0.2,
+                                    sinks=np.full(4, 60.0, np.float32))
+    assert np.abs(o2).max() < 1e-9  # every key weighs about e^-60 against the sink
+    assert np.abs(l2 - 60.0).max() < 1e-5
+
+
+def _ring_from_linear(case, ring):
+    """A ring pool of `ring` blocks per sequence holding, in entry b % ring,
+    the last logical block b that maps there (numpy copies)."""
+    B = len(case.lens)
+    nb = B * ring
+    k = np.zeros((nb,) + case.k_cache.shape[1:], case.k_cache.dtype)
+    v = np.zeros_like(k)
+    tabs = np.full((B, ring), -1, np.int32)
+    for s in range(B):
+        tabs[s] = np.arange(ring) + s * ring
+        for b in range((int(case.lens[s]) + BS - 1) // BS):
+            k[tabs[s, b % ring]] = case.k_cache[case.tables[s, b]]
+            v[tabs[s, b % ring]] = case.v_cache[case.tables[s, b]]
+    return k, v, tabs
+
+
+@pytest.mark.parametrize("window,ring", [(128, 9), (40, 4), (16, 2)])
+def test_ring_cache_equals_the_linear_cache_over_the_window(window, ring):
+    rng = np.random.default_rng(32 + window)
+    case = PagedCase(rng, [1, 15, 16, 17, 130, 700, 1031], 8, 2, 64)
+    o_lin, l_lin = oracle.paged_attention(**case.oracle_kwargs(), sm_scale=0.125, window=window)
+    k, v, tabs = _ring_from_linear(case, ring)
+    kw = case.oracle_kwargs()
+    kw.update(k_cache=k, v_cache=v, block_tables=tabs)
+    o_ring, l_ring = oracle.paged_attention(**kw, sm_scale=0.125, window=window, ring_blocks=ring)
+    assert np.array_equal(o_lin.view(np.uint32), o_ring.view(np.uint32))
+    assert np.array_equal(l_lin.view(np.uint32), l_ring.view(np.uint32))
+    ref, _ = dense_reference(case, 0.125, window=window)
+    assert np.abs(o_ring - ref).max() < 2e-6
+    # a ring too small for the window is refused
+    with pytest.raises(Exception):
+        oracle.paged_attention(**kw, sm_scale=0.125, window=window + BS, ring_blocks=ring)
+
+
+def test_ring_append_writes_entry_block_mod_ring():
+    rng = np.random.default_rng(33)
+    hkv, d, ring, n = 2, 32, 3, 100
+    kc = np.zeros((ring, hkv, BS, d), np.uint16)
+    vc = np.zeros_like(kc)
+    tab = np.array([[2, 0, 1]], np.int32)
+    kn = bf16_bits(rng.standard_normal((n, hkv, d)))
+    vn = bf16_bits(rng.standard_normal((n, hkv, d)))
+    for p in range(n):
+        oracle.append_rope(num_q_heads=hkv, num_kv_heads=hkv, head_dim=d, block_size=BS,
+                           kv_dtype=oracle.KV_BF16, k_cache=kc, v_cache=vc, block_tables=tab,
+                           token_to_seq=[0], positions=[p], k_new=kn[p:p + 1], v_new=vn[p:p + 1],
+                           ring_blocks=ring)
+    for p in range(n):
+        b = p // BS
+        if b >= (n - 1) // BS - ring + 1:  # not yet overwritten by a later block
+            assert np.array_equal(kc[tab[0, b % ring], :, p % BS], kn[p])
+            assert np.array_equal(vc[tab[0, b % ring], :, p % BS], vn[p])
