@@ -70,7 +70,13 @@ typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
 
 /* Shape of one paged KV pool pair (K and V share it).
  * Supported: head_dim 64 or 128; block_size 16; num_q_heads a multiple of
- * num_kv_heads with group size num_q_heads / num_kv_heads <= 16. */
+ * num_kv_heads with group size num_q_heads / num_kv_heads <= 16.
+ * ring_blocks > 0 makes every sequence's cache a ring of that many blocks, as
+ * for a sliding-window layer (RustInfer, "Status": SWA with a 128-token ring
+ * cache): token p lives in block block_tables[s][(p / block_size) % ring_blocks],
+ * so a sequence's window of W keys needs ring_blocks >= ceil((W - 1) / 16) + 1
+ * (9 for W = 128) however long it grows.  Append and decode (with a window)
+ * honour it; prefill, gather and cascade decode refuse a ring (PKV_ERR_UNSUPPORTED). */
 typedef struct {
     int32_t num_q_heads;
     int32_t num_kv_heads;
@@ -79,6 +85,7 @@ typedef struct {
     int32_t kv_dtype;            /* pkv_kv_dtype */
     int32_t max_blocks_per_seq;  /* row length of block_tables (int32 [num_seqs][this]) */
     int64_t num_blocks;          /* blocks in each pool */
+    int32_t ring_blocks;         /* 0: linear tables; > 0: ring of this many blocks (<= max_blocks_per_seq) */
 } pkv_cache_desc;
 
 /* Bytes of one pool (K or V): num_blocks * Hkv * block_size * head_dim * elem.
@@ -87,8 +94,8 @@ uint64_t pkv_cache_bytes(const pkv_cache_desc *desc);
 
 /* ---- a1: fused KV append + RoPE (llm-infer, "What It Does") ------------
  * For each new token i (0 <= i < num_tokens): s = token_to_seq[i],
- * p = positions[i]; slot = block block_tables[s][p / block_size], row
- * p % block_size.  For every KV head h:
+ * p = positions[i]; slot = block block_tables[s][p / block_size] (entry
+ * (p / block_size) % ring_blocks with a ring), row p % block_size.  For every KV head h:
  *   K row = RoPE(k_new[i][h], p) rounded to bf16 (RNE), or for e4m3
  *           RNE-satfinite(RoPE(k_new[i][h], p) / k_scale[h]);
  *   V row = v_new[i][h] copied, or RNE-satfinite(v_new[i][h] / v_scale[h]).
@@ -146,16 +153,22 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc *desc, void *k_cache, void *v_ca
  *   o = softmax(sm_scale * q k^T) v over the visible keys, lse = ln sum exp.
  * Visible keys: t < context_lens[s]; with window > 0 also
  * t > context_lens[s] - 1 - window.  e4m3 pools read k = code * k_scale[h],
- * v = code * v_scale[h].
+ * v = code * v_scale[h].  With sinks (RustInfer, "Status": SWA operators
+ * with attention sinks) query head h has a sink logit sinks[h] that joins
+ * the softmax with a zero value: o = sum_t e^{l_t} v_t / (e^{sinks[h]} +
+ * sum_t e^{l_t}), lse = ln(e^{sinks[h]} + sum_t e^{l_t}).
  * The KV range of each (sequence, KV head) is cut into chunks of whole
  * blocks (pkv_decode_plan); every chunk runs as one CTA whose warps share
  * the G query heads of the group; partial (o, lse) states go to the
  * workspace and the last chunk to finish merges them in the same launch.
  *   q        : bf16 [num_seqs][Hq][D].      out: bf16 [num_seqs][Hq][D].
  *   lse_out  : fp32 [num_seqs][Hq], nullable.
- *   context_lens : int32 [num_seqs], each in [1, max_blocks_per_seq*bs].
+ *   context_lens : int32 [num_seqs], each in [1, max_blocks_per_seq*bs]
+ *              (any length >= 1 with a ring cache).
  *   max_context_len : host, >= every context_lens[s]; sizes the plan.
- *   window   : <= 0 for full attention.
+ *   window   : <= 0 for full attention; required (> 0, and covered by the
+ *              ring) when desc->ring_blocks > 0.
+ *   sinks    : fp32 [Hq] sink logits in the units of sm_scale * q.k, or NULL.
  *   chunk_blocks : blocks per chunk; 0 lets the planner choose
  *              (pkv_decode_plan), else 1..128.
  *   workspace: >= pkv_decode_workspace_size(...) bytes, 256-byte aligned,
@@ -167,8 +180,9 @@ pkv_status pkv_decode_attention(const pkv_cache_desc *desc, const void *q,
                                 const float *k_scale, const float *v_scale,
                                 const int32_t *block_tables, const int32_t *context_lens,
                                 int32_t num_seqs, int32_t max_context_len, float sm_scale,
-                                int32_t window, int32_t chunk_blocks, void *out, float *lse_out,
-                                void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+                                int32_t window, const float *sinks, int32_t chunk_blocks,
+                                void *out, float *lse_out, void *workspace,
+                                size_t workspace_bytes, pkv_stream_t stream);
 
 /* Host: workspace bytes pkv_decode_attention needs for this shape and
  * chunk_blocks (0 = planned; planning uses the current device's SM count).
@@ -288,8 +302,8 @@ pkv_status pkv_decode_attention_static(const pkv_cache_desc *desc, const void *q
                                        const float *k_scale, const float *v_scale,
                                        const int32_t *block_tables, const int32_t *context_lens,
                                        int32_t num_seqs, int32_t max_context_len, float sm_scale,
-                                       int32_t window, int32_t chunk_blocks, void *out,
-                                       float *lse_out, pkv_stream_t stream);
+                                       int32_t window, const float *sinks, int32_t chunk_blocks,
+                                       void *out, float *lse_out, pkv_stream_t stream);
 
 /* ---- diagnostics --------------------------------------------------------- */
 

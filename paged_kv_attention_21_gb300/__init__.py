@@ -45,15 +45,15 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int64)]
+                ("num_blocks", ctypes.c_int64), ("ring_blocks", ctypes.c_int32)]
 
 
 def make_desc(*, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
-              kv_dtype=KV_BF16, block_size=16) -> CacheDesc:
+              kv_dtype=KV_BF16, block_size=16, ring_blocks=0) -> CacheDesc:
     if isinstance(kv_dtype, str):
         kv_dtype = KV_FP8_E4M3 if kv_dtype.startswith("fp8") else KV_BF16
     return CacheDesc(int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-                     int(kv_dtype), int(max_blocks_per_seq), int(num_blocks))
+                     int(kv_dtype), int(max_blocks_per_seq), int(num_blocks), int(ring_blocks))
 
 
 _lock = threading.Lock()
@@ -81,7 +81,7 @@ def load_library():
             "pkv_append_rope": (ctypes.c_int, [D, P, P, P, P, P, i32, P, P, i32, P, P, P, P, i32, P]),
             "pkv_rope_cos_sin_table": (ctypes.c_int, [f32, i32, i32, P]),
             "pkv_gather_kv": (ctypes.c_int, [D, P, P, P, P, i32, i64, P, P]),
-            "pkv_decode_attention": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32, i32,
+            "pkv_decode_attention": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32, i32, P,
                                                     i32, P, P, P, ctypes.c_size_t, P]),
             "pkv_decode_workspace_size": (ctypes.c_size_t, [D, i32, i32, i32, i32]),
             "pkv_decode_plan": (ctypes.c_int, [D, i32, i32, i32, i32, P, P]),
@@ -90,7 +90,7 @@ def load_library():
                                                             ctypes.c_size_t, P]),
             "pkv_prefill_workspace_size": (ctypes.c_size_t, [D, i32, i32]),
             "pkv_decode_attention_static": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32,
-                                                           i32, i32, P, P, P]),
+                                                           i32, P, i32, P, P, P]),
             "pkv_merge_states": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, P, P]),
             "pkv_cascade_workspace_size": (ctypes.c_size_t, [D, i32, i32]),
             "pkv_cascade_decode": (ctypes.c_int, [D, P, P, P, i32, P, P, P, P, P, i32, P, P, i32, f32,
@@ -190,24 +190,26 @@ def pkv_decode_plan(desc, num_seqs, max_context_len, window=-1, num_sms=0):
 
 def pkv_decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
                          sm_scale, out, lse=None, workspace=None, window=-1, chunk_blocks=0,
-                         k_scale=None, v_scale=None, stream=None):
+                         k_scale=None, v_scale=None, sinks=None, stream=None):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().pkv_decode_attention(
         ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
         _ptr(block_tables), _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len),
-        float(sm_scale), int(window), int(chunk_blocks), _ptr(out), _ptr(lse), _ptr(workspace),
-        ws_bytes, _stream(stream)))
+        float(sm_scale), int(window), _ptr(sinks), int(chunk_blocks), _ptr(out), _ptr(lse),
+        _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pkv_decode_attention_static(desc, q, k_cache, v_cache, block_tables, context_lens,
                                 max_context_len, sm_scale, out, lse=None, window=-1,
-                                chunk_blocks=0, k_scale=None, v_scale=None, stream=None):
+                                chunk_blocks=0, k_scale=None, v_scale=None, sinks=None,
+                                stream=None):
     """Decode for callers that cannot allocate: no workspace argument, the
     library's fixed 16 MiB device scratch instead (see include/pkv.h)."""
     _check(load_library().pkv_decode_attention_static(
         ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
         _ptr(block_tables), _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len),
-        float(sm_scale), int(window), int(chunk_blocks), _ptr(out), _ptr(lse), _stream(stream)))
+        float(sm_scale), int(window), _ptr(sinks), int(chunk_blocks), _ptr(out), _ptr(lse),
+        _stream(stream)))
 
 
 def pkv_prefill_workspace_size(desc, num_seqs, total_q_tokens) -> int:

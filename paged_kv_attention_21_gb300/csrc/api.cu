@@ -212,6 +212,27 @@ pkv_status check_desc(const pkv_cache_desc* d) {
         return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld out of range", (long long)d->num_blocks);
     if (d->max_blocks_per_seq <= 0)
         return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if (d->ring_blocks < 0 || d->ring_blocks > d->max_blocks_per_seq)
+        return fail(PKV_ERR_INVALID_ARG, "ring_blocks %d outside [0, max_blocks_per_seq = %d]", d->ring_blocks,
+                    d->max_blocks_per_seq);
+    return PKV_OK;
+}
+
+// Decode over a ring cache needs a window whose keys the ring holds: the
+// window spans at most ceil((W - 1) / 16) + 1 blocks.  Also the bound on
+// max_context_len: the table capacity, or none with a ring.
+pkv_status check_ring_window(const pkv_cache_desc* d, int window, int max_context_len) {
+    if (d->ring_blocks > 0) {
+        if (window <= 0) return fail(PKV_ERR_INVALID_ARG, "a ring cache needs a sliding window");
+        if ((window - 1 + d->block_size - 1) / d->block_size + 1 > d->ring_blocks)
+            return fail(PKV_ERR_INVALID_ARG, "window %d needs more than ring_blocks = %d blocks", window,
+                        d->ring_blocks);
+        if (max_context_len < 1) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d < 1", max_context_len);
+        return PKV_OK;
+    }
+    if (max_context_len < 1 || max_context_len > d->max_blocks_per_seq * d->block_size)
+        return fail(PKV_ERR_INVALID_ARG, "max_context_len %d outside [1, %d]", max_context_len,
+                    d->max_blocks_per_seq * d->block_size);
     return PKV_OK;
 }
 
@@ -380,8 +401,9 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
                                 const void* v_cache, const float* k_scale, const float* v_scale,
                                 const int32_t* block_tables, const int32_t* context_lens,
                                 int32_t num_seqs, int32_t max_context_len, float sm_scale,
-                                int32_t window, int32_t chunk_blocks, void* out, float* lse_out,
-                                void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+                                int32_t window, const float* sinks, int32_t chunk_blocks, void* out,
+                                float* lse_out, void* workspace, size_t workspace_bytes,
+                                pkv_stream_t stream) {
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
@@ -392,9 +414,8 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
         return fail(PKV_ERR_INVALID_ARG, "null device pointer");
     const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
     if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
-    if (max_context_len < 1 || max_context_len > desc->max_blocks_per_seq * desc->block_size)
-        return fail(PKV_ERR_INVALID_ARG, "max_context_len %d outside [1, %d]", max_context_len,
-                    desc->max_blocks_per_seq * desc->block_size);
+    st = check_ring_window(desc, window, max_context_len);
+    if (st != PKV_OK) return st;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
     if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
@@ -425,6 +446,8 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
     a.context_lens = context_lens;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.sinks = sinks;
+    a.ring = desc->ring_blocks;
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     a.counters = ws.total ? reinterpret_cast<uint32_t*>(wsb + ws.counters) : nullptr;
     a.part_lse = ws.total ? reinterpret_cast<float*>(wsb + ws.lse) : nullptr;
@@ -473,6 +496,7 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     (void)workspace_bytes;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
+    if (desc->ring_blocks > 0) return fail(PKV_ERR_UNSUPPORTED, "prefill reads linear tables (no ring cache)");
     if (desc->kv_dtype != PKV_KV_BF16)
         return fail(PKV_ERR_UNSUPPORTED, "prefill reads bf16 pools only");
     if (num_seqs < 0 || num_seqs > 65535)
@@ -581,6 +605,7 @@ pkv_status pkv_append_rope(const pkv_cache_desc* desc, void* k_cache, void* v_ca
     a.d = desc->head_dim;
     a.mbps = desc->max_blocks_per_seq;
     a.max_pos = rope_max_pos;
+    a.ring = desc->ring_blocks;
     a.num_blocks = desc->num_blocks;
     a.fp8 = fp8 ? 1 : 0;
     a.err = err;
@@ -595,6 +620,7 @@ pkv_status pkv_gather_kv(const pkv_cache_desc* desc, const void* cache, const in
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
+    if (desc->ring_blocks > 0) return fail(PKV_ERR_UNSUPPORTED, "gather reads linear tables (no ring cache)");
     if (num_seqs < 0 || total_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative count");
     if (num_seqs == 0 || total_tokens == 0) return PKV_OK;
     if (!cache || !block_tables || !context_lens || !cu_context_lens || !out)
@@ -711,6 +737,7 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
+    if (desc->ring_blocks > 0) return fail(PKV_ERR_UNSUPPORTED, "cascade decode reads linear tables (no ring cache)");
     if (desc->kv_dtype != PKV_KV_BF16) return fail(PKV_ERR_UNSUPPORTED, "cascade decode reads bf16 pools only");
     if (num_seqs < 0 || num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range", num_seqs);
     if (num_seqs == 0) return PKV_OK;
@@ -897,7 +924,8 @@ extern "C" pkv_status pkv_decode_attention_static(
     const pkv_cache_desc* desc, const void* q, const void* k_cache, const void* v_cache,
     const float* k_scale, const float* v_scale, const int32_t* block_tables,
     const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float sm_scale,
-    int32_t window, int32_t chunk_blocks, void* out, float* lse_out, pkv_stream_t stream) {
+    int32_t window, const float* sinks, int32_t chunk_blocks, void* out, float* lse_out,
+    pkv_stream_t stream) {
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
@@ -908,9 +936,8 @@ extern "C" pkv_status pkv_decode_attention_static(
         return fail(PKV_ERR_INVALID_ARG, "null device pointer");
     const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
     if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
-    if (max_context_len < 1 || max_context_len > desc->max_blocks_per_seq * desc->block_size)
-        return fail(PKV_ERR_INVALID_ARG, "max_context_len %d outside [1, %d]", max_context_len,
-                    desc->max_blocks_per_seq * desc->block_size);
+    st = check_ring_window(desc, window, max_context_len);
+    if (st != PKV_OK) return st;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
     if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
@@ -951,6 +978,8 @@ extern "C" pkv_status pkv_decode_attention_static(
     a.context_lens = context_lens;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.sinks = sinks;
+    a.ring = desc->ring_blocks;
     a.counters = ws.total ? reinterpret_cast<uint32_t*>(wsb + ws.counters) : nullptr;
     a.part_lse = ws.total ? reinterpret_cast<float*>(wsb + ws.lse) : nullptr;
     a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;

@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(256) append_rope_kernel(AppendArgs a) {
 
     const int s = a.token_to_seq[i];
     const int p = a.positions[i];
-    const bool ok = s >= 0 && s < a.num_seqs && p >= 0 && p / kBlockSize < a.mbps &&
+    const int tb = a.ring > 0 ? (p / kBlockSize) % a.ring : p / kBlockSize;  // table entry
+    const bool ok = s >= 0 && s < a.num_seqs && p >= 0 && tb < a.mbps &&
                     (a.cos_sin == nullptr || p < a.max_pos);
     if (!ok) {
         if (lane == 0) flag_error(a.err, PKV_DEVERR_POSITION);
@@ -71,7 +72,7 @@ __global__ void __launch_bounds__(256) append_rope_kernel(AppendArgs a) {
     };
 
     if (r < a.hkv) {
-        const int blk = a.block_tables[static_cast<size_t>(s) * a.mbps + p / kBlockSize];
+        const int blk = a.block_tables[static_cast<size_t>(s) * a.mbps + tb];
         if (blk < 0 || blk >= a.num_blocks) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
             return;

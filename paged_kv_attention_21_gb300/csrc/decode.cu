@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                     static_cast<__nv_bfloat16*>(a.out)[o0 + i] = __float2bfloat16_rn(0.f);
             }
             if (a.lse_out && threadIdx.x < G)
-                a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + threadIdx.x] = -INFINITY;
+                a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + threadIdx.x] =
+                    a.sinks ? a.sinks[kvh * G + threadIdx.x] : -INFINITY;
         }
         return;
     }
@@ -176,7 +177,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
     int phys = 0;
     if (lane < my_n) {
-        phys = bt[b0 + warp + lane * kWarps];
+        const int lb = b0 + warp + lane * kWarps;  // logical block
+        phys = bt[a.ring > 0 ? lb % a.ring : lb];
         if (phys < 0 || phys >= a.num_blocks) {
             flag_error(a.err, PKV_DEVERR_BLOCK_ID);
             phys = 0;  // read a valid block; the output is flagged invalid
@@ -411,10 +413,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             f[w] = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
             L += f[w] * s_l[w][r];
         }
-        const float inv = L > 0.f ? (kFp8 ? a.v_scale[kvh] : 1.f) / L : 0.f;
+        float inv = L > 0.f ? (kFp8 ? a.v_scale[kvh] : 1.f) / L : 0.f;
+        float lse = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
+        if (a.sinks && nsplit == 1 && r < G) {
+            // the sink joins the normaliser: lse' = ln(e^lse + e^s), o scaled by e^(lse - lse')
+            const float sk = a.sinks[kvh * G + r];
+            const float hi = fmaxf(lse, sk);
+            const float lse2 = hi == -INFINITY ? -INFINITY : hi + __logf(__expf(lse - hi) + __expf(sk - hi));
+            inv *= lse == -INFINITY ? 0.f : __expf(lse - lse2);
+            lse = lse2;
+        }
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) s_m[w][r] = f[w] * inv;
-        s_l[0][r] = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
+        s_l[0][r] = lse;
     }
     __syncthreads();
     if (!cta_failed) {
@@ -471,6 +482,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
 #pragma unroll
         for (int off = 1; off < 8; off <<= 1) W += __shfl_xor_sync(0xFFFFFFFFu, W, off);
         if (sub == 0) {
+            // a sink joins the normaliser (M is finite: every split has keys)
+            if (a.sinks && r < G) W += __expf(a.sinks[kvh * G + r] - M);
             rowM[r] = M;
             rowW[r] = W;
         }

@@ -24,6 +24,7 @@ struct AppendArgs {
     int32_t num_seqs, num_tokens, hq, hkv, d, mbps, max_pos;
     int64_t num_blocks;
     int32_t fp8;
+    int32_t ring;  // > 0: table entry (p / 16) % ring
     uint32_t* err;
 };
 cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream);
@@ -69,12 +70,14 @@ struct DecodeArgs {
     const int32_t* context_lens;
     const float* k_scale;
     const float* v_scale;
+    const float* sinks;   // nullable: fp32 [hq] sink logits
     uint32_t* counters;   // [num_seqs * hkv], zero on entry and exit
     float* part_lse;      // [num_seqs * hkv * max_splits * group]
     float* part_o;        // [num_seqs * hkv * max_splits * group * d]
     uint32_t* err;
     int32_t num_seqs, hq, hkv, group, d, mbps, window, chunk_blocks, max_splits, fp8;
     int32_t max_ctx;  // host bound on context_lens: the split plan covers up to it
+    int32_t ring;     // > 0: logical block b is table entry b % ring
     int64_t num_blocks;
     float sm_scale;
 };

@@ -80,7 +80,7 @@ def test_invalid_arguments_return_status_before_any_device_work(lib):
     ]
     # null desc
     st = lib.pkv_decode_attention(None, fake, fake, fake, None, None, fake, fake, 1, 10, 0.1, -1,
-                                  0, fake, None, None, 0, None)
+                                  None, 0, fake, None, None, 0, None)
     assert st == 1 and "desc" in pkv.pkv_last_error()
     bad = [
         (_desc(num_q_heads=15), 1, "multiple"),
@@ -92,34 +92,34 @@ def test_invalid_arguments_return_status_before_any_device_work(lib):
     ]
     for d, code, word in bad:
         st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,
-                                      10, 0.1, -1, 0, fake, None, None, 0, None)
+                                      10, 0.1, -1, None, 0, fake, None, None, 0, None)
         assert st == code, (word, st)
         assert word in pkv.pkv_last_error()
     d = _desc()
     # context longer than the table can hold
     st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,
-                                  256 * 16 + 1, 0.1, -1, 0, fake, None, None, 0, None)
+                                  256 * 16 + 1, 0.1, -1, None, 0, fake, None, None, 0, None)
     assert st == 1 and "max_context_len" in pkv.pkv_last_error()
     # e4m3 without scales
     d8 = _desc(kv_dtype=pkv.KV_FP8_E4M3)
     st = lib.pkv_decode_attention(ctypes.byref(d8), fake, fake, fake, None, None, fake, fake, 1,
-                                  10, 0.1, -1, 0, fake, None, None, 0, None)
+                                  10, 0.1, -1, None, 0, fake, None, None, 0, None)
     assert st == 1 and "scale" in pkv.pkv_last_error()
     # null pointers
     st = lib.pkv_decode_attention(ctypes.byref(d), None, fake, fake, None, None, fake, fake, 1,
-                                  10, 0.1, -1, 0, fake, None, None, 0, None)
+                                  10, 0.1, -1, None, 0, fake, None, None, 0, None)
     assert st == 1
     # misaligned q
     st = lib.pkv_decode_attention(ctypes.byref(d), P(0x10002), fake, fake, None, None, fake, fake,
-                                  1, 10, 0.1, -1, 0, fake, None, None, 0, None)
+                                  1, 10, 0.1, -1, None, 0, fake, None, None, 0, None)
     assert st == 1 and "aligned" in pkv.pkv_last_error()
     # bad sm_scale
     st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,
-                                  10, float("nan"), -1, 0, fake, None, None, 0, None)
+                                  10, float("nan"), -1, None, 0, fake, None, None, 0, None)
     assert st == 1
     # zero sequences: a no-op, OK
     st = lib.pkv_decode_attention(ctypes.byref(d), None, None, None, None, None, None, None, 0,
-                                  10, 0.1, -1, 0, None, None, None, 0, None)
+                                  10, 0.1, -1, None, 0, None, None, None, 0, None)
     assert st == 0
     # prefill: e4m3 pools unsupported; kv_len < q_len rejected
     st = lib.pkv_prefill_attention_ragged(ctypes.byref(d8), fake, fake, fake, fake, None, None,
@@ -141,6 +141,20 @@ def test_invalid_arguments_return_status_before_any_device_work(lib):
     assert st == 1
     st = lib.pkv_rope_cos_sin_table(1e4, 63, 10, fake)
     assert st == 1
+    # ring cache: bounded by the table row, needs a window it can hold; prefill refuses it
+    st = lib.pkv_decode_attention(ctypes.byref(_desc(max_blocks_per_seq=8, ring_blocks=9)), fake, fake,
+                                  fake, None, None, fake, fake, 1, 10, 0.1, 128, None, 0, fake, None,
+                                  None, 0, None)
+    assert st == 1 and "ring_blocks" in pkv.pkv_last_error()
+    dr = _desc(ring_blocks=9)
+    for window in (-1, 0, 145):
+        st = lib.pkv_decode_attention(ctypes.byref(dr), fake, fake, fake, None, None, fake, fake, 1,
+                                      100000, 0.1, window, None, 0, fake, None, None, 0, None)
+        assert st == 1 and "window" in pkv.pkv_last_error(), window
+    st = lib.pkv_prefill_attention_ragged(ctypes.byref(dr), fake, fake, fake, fake, None, None,
+                                          fake, fake, 1, 4, None, None, 0.1, 1, -1, fake, None,
+                                          None, 0, None)
+    assert st == 2 and "ring" in pkv.pkv_last_error()
 
 
 def test_planner_fills_the_gpu_and_respects_limits(lib):
