@@ -305,6 +305,22 @@ DecodeWs decode_ws_layout(const pkv_cache_desc* d, int num_seqs, int splits) {
     return w;
 }
 
+// FP8 prefill staging: a bf16 copy of every visible block of the batch,
+// block j of sequence s at s * max_blocks_per_seq + j, and its table.
+struct PrefillStageWs {
+    size_t tables, k, v, total;
+};
+PrefillStageWs prefill_stage_ws(const pkv_cache_desc* d, int num_seqs) {
+    PrefillStageWs w{};
+    const size_t blocks = size_t(num_seqs) * d->max_blocks_per_seq;
+    const size_t block_bytes = size_t(d->num_kv_heads) * d->block_size * d->head_dim * 2;
+    w.tables = 0;
+    w.k = align256(blocks * sizeof(int32_t));
+    w.v = w.k + align256(blocks * block_bytes);
+    w.total = w.v + align256(blocks * block_bytes);
+    return w;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -473,10 +489,9 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
 
 size_t pkv_prefill_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,
                                   int32_t total_q_tokens) {
-    (void)desc;
-    (void)num_seqs;
     (void)total_q_tokens;
-    return 0;
+    if (check_desc(desc) != PKV_OK || num_seqs <= 0 || desc->kv_dtype != PKV_KV_FP8_E4M3) return 0;
+    return prefill_stage_ws(desc, num_seqs).total;
 }
 
 pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* q,
@@ -490,15 +505,11 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
                                         float* lse_out, void* workspace,
                                         size_t workspace_bytes, pkv_stream_t stream) {
     g_last_error[0] = 0;
-    (void)k_scale;
-    (void)v_scale;
-    (void)workspace;
-    (void)workspace_bytes;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (desc->ring_blocks > 0) return fail(PKV_ERR_UNSUPPORTED, "prefill reads linear tables (no ring cache)");
-    if (desc->kv_dtype != PKV_KV_BF16)
-        return fail(PKV_ERR_UNSUPPORTED, "prefill reads bf16 pools only");
+    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
     if (num_seqs < 0 || num_seqs > 65535)
         return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
     if (total_q_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "total_q_tokens < 0");
@@ -532,18 +543,55 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     uint32_t* err = nullptr;
     st = device_state(&err, nullptr);
     if (st != PKV_OK) return st;
+    // e4m3 pools: the batch's visible blocks are staged as bf16 (exact) in the
+    // workspace, and the kernel reads the staged pool with the scales folded in
+    pkv_cache_desc staged = *desc;
+    const void* kpool = k_cache;
+    const void* vpool = v_cache;
+    const int32_t* tables = block_tables;
+    if (fp8) {
+        const PrefillStageWs sw = prefill_stage_ws(desc, num_seqs);
+        if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", sw.total);
+        if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        if (workspace_bytes < sw.total)
+            return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, sw.total);
+        uint8_t* wsb = static_cast<uint8_t*>(workspace);
+        pkv::StageArgs g{};
+        g.k_cache = static_cast<const uint8_t*>(k_cache);
+        g.v_cache = static_cast<const uint8_t*>(v_cache);
+        g.block_tables = block_tables;
+        g.kv_lens = kv_lens;
+        g.k_stage = reinterpret_cast<uint16_t*>(wsb + sw.k);
+        g.v_stage = reinterpret_cast<uint16_t*>(wsb + sw.v);
+        g.stage_tables = reinterpret_cast<int32_t*>(wsb + sw.tables);
+        g.num_seqs = num_seqs;
+        g.mbps = desc->max_blocks_per_seq;
+        g.hkv = desc->num_kv_heads;
+        g.d = desc->head_dim;
+        g.num_blocks = desc->num_blocks;
+        g.err = err;
+        cudaError_t e = pkv::launch_stage_fp8(g, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "FP8 staging launch");
+        staged.kv_dtype = PKV_KV_BF16;
+        staged.num_blocks = static_cast<int64_t>(num_seqs) * desc->max_blocks_per_seq;
+        kpool = g.k_stage;
+        vpool = g.v_stage;
+        tables = g.stage_tables;
+    }
     CUtensorMap kmap, vmap;
-    st = pool_map(k_cache, desc, &kmap);
+    st = pool_map(kpool, &staged, &kmap);
     if (st != PKV_OK) return st;
-    st = pool_map(v_cache, desc, &vmap);
+    st = pool_map(vpool, &staged, &vmap);
     if (st != PKV_OK) return st;
     pkv::PrefillArgs a{};
+    a.k_scale = fp8 ? k_scale : nullptr;
+    a.v_scale = fp8 ? v_scale : nullptr;
     a.q = q;
     a.out = out;
     a.lse_out = lse_out;
     a.qo_indptr = qo_indptr;
     a.kv_lens = kv_lens;
-    a.block_tables = block_tables;
+    a.block_tables = tables;
     a.err = err;
     a.num_seqs = num_seqs;
     a.hq = desc->num_q_heads;
@@ -556,7 +604,7 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     a.max_qtiles = max_qtiles;
     a.q_tile = QT;
     a.total_q = total_q_tokens;
-    a.num_blocks = desc->num_blocks;
+    a.num_blocks = staged.num_blocks;
     a.sm_scale = sm_scale;
     CUtensorMap qmap;
     st = q_map(q, total_q_tokens, desc, G, QT, &qmap);

@@ -52,6 +52,23 @@ struct CopyArgs {
 };
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 
+// e4m3 -> bf16 staging of the visible blocks of a batch (FP8 prefill): block
+// j < ceil(kv_lens[s] / 16) of sequence s goes to staging block s * mbps + j,
+// and the staging table gets that id.  Exact: every e4m3 code is a bf16 value.
+struct StageArgs {
+    const uint8_t* k_cache;   // e4m3 pools
+    const uint8_t* v_cache;
+    const int32_t* block_tables;
+    const int32_t* kv_lens;
+    uint16_t* k_stage;        // bf16 staging pools [num_seqs * mbps][Hkv][16][D]
+    uint16_t* v_stage;
+    int32_t* stage_tables;    // [num_seqs][mbps]
+    int32_t num_seqs, mbps, hkv, d;
+    int64_t num_blocks;
+    uint32_t* err;
+};
+cudaError_t launch_stage_fp8(const StageArgs& a, cudaStream_t stream);
+
 struct MergeArgs {
     const float* o_parts;
     const float* lse_parts;
@@ -86,6 +103,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CU
 
 struct PrefillArgs {
     const void* q;
+    const float* k_scale;  // nullable: per KV head, folded into the logit scale (staged FP8 pools)
+    const float* v_scale;  // nullable: per KV head, folded into the output
     void* out;
     float* out_f32;  // non-null: fp32 output (an (o, lse) state to merge) instead of bf16 out
     float* lse_out;

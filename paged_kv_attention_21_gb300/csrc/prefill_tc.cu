@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int pos = sp.pos_min + t;
         const int j0 = x ? jlo[1] : jlo[0];
         const int nx = x ? jhi[1] - jlo[1] : jhi[0] - jlo[0];
-        const float scale_log2 = a.sm_scale * 1.4426950408889634f;
+        const float scale_log2 = a.sm_scale * 1.4426950408889634f * (a.k_scale ? a.k_scale[kvh] : 1.f);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const uint32_t s_base = lane_base + C::col_s(x);
         const int grp_tid = (sw & 7) * 32 + lane;  // 0..255 within the tile's softmax group
@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         } else if (sp.ntok > 0) {
             // epilogue: this half's O columns / l -> bf16 (or fp32); lse by half 0
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            const float inv = l_row > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / l_row : 0.f;
             const size_t orow0 = (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D + half * (D / 2);
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + orow0;
 #pragma unroll

@@ -121,11 +121,11 @@ def test_invalid_arguments_return_status_before_any_device_work(lib):
     st = lib.pkv_decode_attention(ctypes.byref(d), None, None, None, None, None, None, None, 0,
                                   10, 0.1, -1, None, 0, None, None, None, 0, None)
     assert st == 0
-    # prefill: e4m3 pools unsupported; kv_len < q_len rejected
+    # prefill: e4m3 pools need their scales; kv_len < q_len rejected
     st = lib.pkv_prefill_attention_ragged(ctypes.byref(d8), fake, fake, fake, fake, None, None,
                                           fake, fake, 1, 4, None, None, 0.1, 1, -1, fake, None,
                                           None, 0, None)
-    assert st == 2
+    assert st == 1 and "scale" in pkv.pkv_last_error()
     qo = np.array([0, 4], np.int32)
     kl = np.array([3], np.int32)
     st = lib.pkv_prefill_attention_ragged(ctypes.byref(d), fake, fake, fake, fake, None, None,

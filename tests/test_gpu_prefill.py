@@ -186,3 +186,34 @@ def test_mixed_step_workload_full_size():
     assert_close(out[torch.from_numpy(rows).to(DEV)], ref, "mixed-step prefill")
     assert_lse_close(lse[torch.from_numpy(rows).to(DEV)], ref_lse, "mixed-step prefill")
     assert pkv.pkv_device_errors() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d,window", [(32, 8, 128, -1), (64, 8, 64, -1), (16, 2, 128, 128),
+                                             (64, 8, 64, 128)])
+def test_fp8_prefill_matches_oracle(hq, hkv, d, window):
+    """Ragged causal prefill over e4m3 pools with per-head scales (InferX, "The
+    kernels underneath": FP8 KV cache): against the oracle on the same codes."""
+    from tests._cases import PagedCase
+    rng = np.random.default_rng(80 + d + hq + (window > 0))
+    case = PagedCase(rng, [300, 1000, 77, 520, 1], hq, hkv, d, q_lens=[64, 200, 77, 1, 1], fp8=True)
+    sm = 1.0 / np.sqrt(d)
+    desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=case.num_blocks,
+                         max_blocks_per_seq=case.mbps, kv_dtype=pkv.KV_FP8_E4M3)
+    T = int(case.qo[-1])
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    q = t(case.q).view(torch.int16).view(torch.bfloat16) if case.q.dtype == np.uint16 else t(case.q)
+    out = torch.full((T, hq, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, hq), float("nan"), device=DEV)
+    ws = torch.zeros(max(pkv.pkv_prefill_workspace_size(desc, len(case.lens), T), 256), dtype=torch.uint8,
+                     device=DEV)
+    for _ in range(2):  # the staging workspace is reused
+        pkv.pkv_prefill_attention_ragged(desc, q, t(case.qo), t(case.k_cache), t(case.v_cache), t(case.tables),
+                                         t(case.lens), sm, out, lse, qo_indptr_host=case.qo,
+                                         kv_lens_host=case.lens, window=window, workspace=ws,
+                                         k_scale=t(case.k_scale), v_scale=t(case.v_scale))
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle.paged_attention(**case.oracle_kwargs(), sm_scale=sm, causal=True, window=window,
+                                              nthreads=NTHREADS)
+        assert_close(out, ref, "fp8 prefill %d/%d/%d" % (hq, hkv, d))
+        assert_lse_close(lse, ref_lse, "fp8 prefill")
+    assert pkv.pkv_device_errors() == 0
