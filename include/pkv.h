@@ -209,8 +209,13 @@ pkv_status pkv_decode_plan(const pkv_cache_desc *desc, int32_t num_seqs,
  *   qo_indptr: int32 [num_seqs + 1] (device).  kv_lens: int32 [num_seqs].
  *   qo_indptr_host, kv_lens_host: host copies (nullable, used for planning
  *              and validation only; they must match the device arrays).
- *   workspace: >= pkv_prefill_workspace_size(...) bytes (0 today; may be NULL).
- * bf16 pools only. */
+ *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL): k = code * k_scale[h],
+ *              v = code * v_scale[h] (InferX, "The kernels underneath": FP8 KV cache).
+ *   workspace: >= pkv_prefill_workspace_size(...) bytes, 256-byte aligned; 0
+ *              (may be NULL) for bf16 pools.  For e4m3 pools it holds a bf16
+ *              copy of the batch's visible blocks (exact: every e4m3 code is a
+ *              bf16 value), staged by the call before the attention kernel.
+ * No ring cache (PKV_ERR_UNSUPPORTED). */
 pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *q,
                                         const int32_t *qo_indptr, const void *k_cache,
                                         const void *v_cache, const float *k_scale,
@@ -222,7 +227,8 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *
                                         float *lse_out, void *workspace,
                                         size_t workspace_bytes, pkv_stream_t stream);
 
-/* Host: workspace bytes pkv_prefill_attention_ragged needs. */
+/* Host: workspace bytes pkv_prefill_attention_ragged needs: 0 for bf16 pools;
+ * for e4m3, a staging copy of num_seqs * max_blocks_per_seq blocks in bf16. */
 size_t pkv_prefill_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
                                   int32_t total_q_tokens);
 
