@@ -4,10 +4,11 @@
 Default workload: the Qwen2.5-3B-shaped decode layer -- 64 sequences, 16
 query / 2 KV heads, head_dim 128, block_size 16, bf16 KV ~ N(0,1), context
 lengths uniform in [256, 4096], blocks scattered over a 40,000-block pool.
-One step is one pass of the whole hot path over one batch: the fused append
-of each sequence's new token with RoPE (theta 1e6) at position ctx-1, then
+One step is one pass of the whole hot path over one batch, in one launch
+per layer (pkv_decode_step): the append of each sequence's new token with
+RoPE (theta 1e6) at position ctx-1 and the rotation of q, fused into
 split-KV GQA decode attention with its planner, block-table gather and
-in-launch merge.  Four batches over disjoint regions of the pool (572 MB of
+in-launch merge (``--two-launch`` runs append and decode as two launches).  Four batches over disjoint regions of the pool (572 MB of
 K/V, more than the 129 MB L2) rotate step by step, so no step finds its K/V
 in L2.  The timed steps replay a CUDA graph of the step sequence.
 
@@ -50,6 +51,9 @@ def parse_args():
                    help="step: the workload's whole step (default); prefill: the ragged causal "
                         "prefill part of workload 4 alone, timed against the tensor-core peak")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--two-launch", action="store_true",
+                   help="run append and decode as two launches per layer instead of the "
+                        "fused decode step")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU seconds the oracle baseline sample aims at")
     return p.parse_args()
@@ -192,8 +196,9 @@ class DecodeWorkload:
     """A decode workload: instances over disjoint regions of one pool (per
     layer), each with its own device workspace-free inputs."""
 
-    def __init__(self, config, dev, rank):
+    def __init__(self, config, dev, rank, fused=True):
         import paged_kv_attention_21_gb300 as pkv
+        self.fused = fused
         from paged_kv_attention_21_gb300 import workloads as wl
         self.pkv = pkv
         spec = wl.CONFIGS[config]
@@ -264,6 +269,19 @@ class DecodeWorkload:
         n = 0
         for li, (layer, w) in enumerate(zip(self.layers, self.windows)):
             b = layer[i]
+            if self.fused:
+                # one launch: append + RoPE of the new token, q rotation, decode
+                if ev_pairs is not None:
+                    ev_pairs[li][0].record()
+                pkv.pkv_decode_step(self.desc, b.q, b.k_new, b.v_new, b.k_cache, b.v_cache,
+                                    b.block_tables, b.context_lens, self.max_ctx,
+                                    self.spec.sm_scale, self.out, self.lse, self.ws,
+                                    cos_sin=self.table, window=w, k_scale=b.k_scale,
+                                    v_scale=b.v_scale)
+                if ev_pairs is not None:
+                    ev_pairs[li][1].record()
+                n += 1
+                continue
             pkv.pkv_append_rope(self.desc, b.k_cache, b.v_cache, b.block_tables, self.seq_ids,
                                 self.pos[i], b.k_new, b.v_new, q=b.q, cos_sin=self.table,
                                 k_scale=b.k_scale, v_scale=b.v_scale)
@@ -317,7 +335,7 @@ def time_pkv(args, rank, world, local):
     import paged_kv_attention_21_gb300 as pkv
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    W = DecodeWorkload(args.config, dev, rank)
+    W = DecodeWorkload(args.config, dev, rank, fused=not args.two_launch)
     K, Wm = args.steps, max(3, args.warmup)
     R = 64 if W.n_inst > 1 else 8          # steps per captured graph
     R = max(W.n_inst, min(R, K))
@@ -392,18 +410,20 @@ def time_pkv(args, rank, world, local):
 
 def time_e2e(W, dev, steps):
     """The same step through the public API with host buffers: each step
-    copies its inputs from pinned host memory, runs append + decode, and
-    reads the output back to the host."""
+    copies its inputs from pinned host memory, runs the decode step (append +
+    decode), and reads the output back to the host."""
     pkv = W.pkv
     host = []
     for b, pos in zip(W.insts, W.pos):
         h = {k: getattr(b, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "block_tables",
                                                            "context_lens")}
-        h["pos"] = pos.cpu().pin_memory()
+        if not W.fused:  # the two-launch path takes explicit positions
+            h["pos"] = pos.cpu().pin_memory()
         host.append(h)
     devbuf = {k: torch.empty_like(getattr(W.insts[0], k)) for k in
               ("q", "k_new", "v_new", "block_tables", "context_lens")}
-    devbuf["pos"] = torch.empty_like(W.pos[0])
+    if not W.fused:
+        devbuf["pos"] = torch.empty_like(W.pos[0])
     out_h = torch.empty(W.out.shape, dtype=W.out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
     d2h = out_h.numel() * out_h.element_size()
@@ -415,6 +435,13 @@ def time_e2e(W, dev, steps):
             devbuf[k].copy_(v, non_blocking=True)
         for layer, w in zip(W.layers, W.windows):
             b = layer[i % W.n_inst]
+            if W.fused:
+                pkv.pkv_decode_step(W.desc, devbuf["q"], devbuf["k_new"], devbuf["v_new"],
+                                    b.k_cache, b.v_cache, devbuf["block_tables"],
+                                    devbuf["context_lens"], W.max_ctx, W.spec.sm_scale, W.out,
+                                    None, W.ws, cos_sin=W.table, window=w, k_scale=b.k_scale,
+                                    v_scale=b.v_scale)
+                continue
             pkv.pkv_append_rope(W.desc, b.k_cache, b.v_cache, devbuf["block_tables"], W.seq_ids,
                                 devbuf["pos"], devbuf["k_new"], devbuf["v_new"], q=devbuf["q"],
                                 cos_sin=W.table, k_scale=b.k_scale, v_scale=b.v_scale)
@@ -502,7 +529,10 @@ def workload_config(W, extra=None):
            if W.n_inst > 1 else "K/V per step (%.1f GB) far exceeds the 129 MB L2" %
                                  (W.kv_bytes(0) / 1e9),
            "parallelism": "replicas: independent batches per GPU, no collective",
-           "step": "append+RoPE of the new token, then split-KV decode (one CUDA graph)"}
+           "step": ("one launch per layer: append+RoPE of the new token fused into split-KV "
+                    "decode (pkv_decode_step), replayed as a CUDA graph" if W.fused else
+                    "append+RoPE of the new token, then split-KV decode: two launches per "
+                    "layer, replayed as a CUDA graph")}
     if W.prefill is not None:
         cfg["step"] += " + ragged causal prefill of 8x512 tokens over shared prefixes"
     if extra:
@@ -610,15 +640,17 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": decode_traffic_per_launch(args.config),
-                     "kernel": "decode_kernel (split-KV GQA decode, merge fused)",
+                     "kernel": ("decode_kernel (append+RoPE, split-KV GQA decode and merge, "
+                                "one launch)" if W.fused else
+                                "decode_kernel (split-KV GQA decode, merge fused)"),
                      "peak_source": "%s hbm_gbs" % peak_kind,
                      "algorithmic_bytes_per_launch": int(r["dom_bytes"]),
                      "avg_launch_ms": round(r["dom_ms"], 5)},
         "e2e": {"value": round(r["e2e_val"], 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"],
                 "steps": r["e2e"]["steps"],
-                "note": "public API per step: pinned H2D of the step's inputs, append+decode, "
-                        "D2H of the output, host sync"},
+                "note": "public API per step: pinned H2D of the step's inputs, the decode "
+                        "step (append+RoPE+decode), D2H of the output, host sync"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }

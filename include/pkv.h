@@ -184,6 +184,33 @@ pkv_status pkv_decode_attention(const pkv_cache_desc *desc, const void *q,
                                 void *out, float *lse_out, void *workspace,
                                 size_t workspace_bytes, pkv_stream_t stream);
 
+/* ---- a1 + a3-a7 fused: one decode step of one layer (llm-infer, "What It
+ * Does": KV writes and fused RoPE inside the decode step).  Equal, bit for
+ * bit in the cache and in out / lse, to
+ *   pkv_append_rope(token_to_seq[s] = s, positions[s] = context_lens[s] - 1,
+ *                   k_new, v_new, q_inout = a copy of q, rope_cos_sin)
+ * followed by pkv_decode_attention over that rotated copy -- in one launch:
+ * the CTA that loads a sequence's last block writes the new K/V rows into it
+ * first, and every CTA rotates its own query rows.  q itself is only read
+ * (not rotated in place).
+ *   k_new, v_new : bf16 [num_seqs][Hkv][D], the new token's K (before RoPE)
+ *                  and V; context_lens[s] already counts that token.
+ *   rope_cos_sin : fp32 [rope_max_pos][D/2][2] (pkv_rope_cos_sin_table), or
+ *                  NULL (no rotation); rope_max_pos >= max_context_len.
+ *   k_cache, v_cache : written (one row per sequence and KV head), then read.
+ * A sequence with context_lens[s] == 0 appends nothing.  Two sequences'
+ * new tokens must not share a slot.  Every other argument, the workspace
+ * (pkv_decode_workspace_size) and the errors are those of
+ * pkv_decode_attention. */
+pkv_status pkv_decode_step(const pkv_cache_desc *desc, const void *q, const void *k_new,
+                           const void *v_new, const float *rope_cos_sin, int32_t rope_max_pos,
+                           void *k_cache, void *v_cache, const float *k_scale,
+                           const float *v_scale, const int32_t *block_tables,
+                           const int32_t *context_lens, int32_t num_seqs,
+                           int32_t max_context_len, float sm_scale, int32_t window,
+                           const float *sinks, int32_t chunk_blocks, void *out, float *lse_out,
+                           void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
 /* Host: workspace bytes pkv_decode_attention needs for this shape and
  * chunk_blocks (0 = planned; planning uses the current device's SM count).
  * 0 when no workspace is needed (every sequence fits one chunk) or the

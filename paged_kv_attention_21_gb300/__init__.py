@@ -83,6 +83,8 @@ def load_library():
             "pkv_gather_kv": (ctypes.c_int, [D, P, P, P, P, i32, i64, P, P]),
             "pkv_decode_attention": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32, i32, P,
                                                     i32, P, P, P, ctypes.c_size_t, P]),
+            "pkv_decode_step": (ctypes.c_int, [D, P, P, P, P, i32, P, P, P, P, P, P, i32, i32, f32,
+                                               i32, P, i32, P, P, P, ctypes.c_size_t, P]),
             "pkv_decode_workspace_size": (ctypes.c_size_t, [D, i32, i32, i32, i32]),
             "pkv_decode_plan": (ctypes.c_int, [D, i32, i32, i32, i32, P, P]),
             "pkv_prefill_attention_ragged": (ctypes.c_int, [D, P, P, P, P, P, P, P, P, i32, i32,
@@ -197,6 +199,22 @@ def pkv_decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, 
         _ptr(block_tables), _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len),
         float(sm_scale), int(window), _ptr(sinks), int(chunk_blocks), _ptr(out), _ptr(lse),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_decode_step(desc, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                    max_context_len, sm_scale, out, lse=None, workspace=None, cos_sin=None,
+                    window=-1, chunk_blocks=0, k_scale=None, v_scale=None, sinks=None, stream=None):
+    """One decode step of one layer in one launch: append each sequence's new
+    token (k_new, v_new; RoPE'd with cos_sin) at context_lens - 1, rotate q
+    (read only), and attend -- as pkv_append_rope then pkv_decode_attention."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    max_pos = 0 if cos_sin is None else int(cos_sin.shape[0])
+    _check(load_library().pkv_decode_step(
+        ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cos_sin), max_pos,
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+        _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len), float(sm_scale),
+        int(window), _ptr(sinks), int(chunk_blocks), _ptr(out), _ptr(lse), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def pkv_decode_attention_static(desc, q, k_cache, v_cache, block_tables, context_lens,

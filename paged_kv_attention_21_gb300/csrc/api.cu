@@ -189,6 +189,7 @@ constexpr int kMaxGroup = 16;
 constexpr int kMaxChunk = 128;   // blocks per decode CTA (32 per warp)
 constexpr int kMinChunk = 32;
 constexpr int kMaxSplits = 512;
+constexpr int kClusterSplits = 4;  // the decode kernel's cluster-merge limit
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -277,6 +278,12 @@ pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, in
         chunk = std::max(kMinChunk, std::min(kMaxChunk, chunk));
         chunk = std::max(chunk, (mb + kMaxSplits - 1) / kMaxSplits);  // bound the split count
         if (chunk > mb) chunk = mb;
+        // 2..4 chunks per sequence merge in a thread-block cluster, without
+        // the workspace round trip; a plan of 5..8 takes 4 longer chunks
+        // instead when they fit one CTA
+        const int s = (mb + chunk - 1) / chunk;
+        if (s > kClusterSplits && s <= 2 * kClusterSplits && (mb + kClusterSplits - 1) / kClusterSplits <= kMaxChunk)
+            chunk = (mb + kClusterSplits - 1) / kClusterSplits;
     }
     const int splits = (mb + chunk - 1) / chunk;
     if (splits > kMaxSplits)
@@ -413,13 +420,24 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,
     return decode_ws_layout(desc, num_seqs, s).total;
 }
 
-pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const void* k_cache,
-                                const void* v_cache, const float* k_scale, const float* v_scale,
-                                const int32_t* block_tables, const int32_t* context_lens,
-                                int32_t num_seqs, int32_t max_context_len, float sm_scale,
-                                int32_t window, const float* sinks, int32_t chunk_blocks, void* out,
-                                float* lse_out, void* workspace, size_t workspace_bytes,
-                                pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The new token of a decode step (pkv_decode_step); null for plain decode.
+struct StepIn {
+    const void* k_new;
+    const void* v_new;
+    const float* cos_sin;
+    int32_t max_pos;
+};
+
+pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                       const void* v_cache, const float* k_scale, const float* v_scale,
+                       const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+                       int32_t max_context_len, float sm_scale, int32_t window, const float* sinks,
+                       int32_t chunk_blocks, void* out, float* lse_out, void* workspace,
+                       size_t workspace_bytes, pkv_stream_t stream, const StepIn* step) {
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
@@ -435,6 +453,18 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
     if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
+    if (step) {
+        if (!step->k_new || !step->v_new) return fail(PKV_ERR_INVALID_ARG, "k_new / v_new is NULL");
+        if (!aligned(step->k_new, 16) || !aligned(step->v_new, 16))
+            return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+        if (step->cos_sin) {
+            if (!aligned(step->cos_sin, 16)) return fail(PKV_ERR_INVALID_ARG, "rope_cos_sin must be 16-byte aligned");
+            // the new token sits at context_lens[s] - 1 <= max_context_len - 1
+            if (step->max_pos < max_context_len)
+                return fail(PKV_ERR_INVALID_ARG, "rope_max_pos %d < max_context_len %d", step->max_pos,
+                            max_context_len);
+        }
+    }
     uint32_t* err = nullptr;
     int sms = 0;
     st = device_state(&err, &sms);
@@ -482,9 +512,45 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const
     a.fp8 = fp8 ? 1 : 0;
     a.num_blocks = desc->num_blocks;
     a.sm_scale = sm_scale;
+    if (step) {
+        a.k_new = step->k_new;
+        a.v_new = step->v_new;
+        a.cos_sin = step->cos_sin;
+        a.k_pool = const_cast<void*>(k_cache);
+        a.v_pool = const_cast<void*>(v_cache);
+    }
     cudaError_t e = pkv::launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (e != cudaSuccess) return cuda_fail(e, step ? "decode step launch" : "decode launch");
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_decode_attention(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                                const void* v_cache, const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                int32_t num_seqs, int32_t max_context_len, float sm_scale,
+                                int32_t window, const float* sinks, int32_t chunk_blocks, void* out,
+                                float* lse_out, void* workspace, size_t workspace_bytes,
+                                pkv_stream_t stream) {
+    return decode_impl(desc, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                       max_context_len, sm_scale, window, sinks, chunk_blocks, out, lse_out, workspace,
+                       workspace_bytes, stream, nullptr);
+}
+
+pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, const void* k_new,
+                           const void* v_new, const float* rope_cos_sin, int32_t rope_max_pos,
+                           void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+                           int32_t max_context_len, float sm_scale, int32_t window, const float* sinks,
+                           int32_t chunk_blocks, void* out, float* lse_out, void* workspace,
+                           size_t workspace_bytes, pkv_stream_t stream) {
+    const StepIn step{k_new, v_new, rope_cos_sin, rope_max_pos};
+    return decode_impl(desc, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                       max_context_len, sm_scale, window, sinks, chunk_blocks, out, lse_out, workspace,
+                       workspace_bytes, stream, &step);
 }
 
 size_t pkv_prefill_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,

@@ -18,10 +18,20 @@
 //     O[16 x D] += P[16 x 16] . V
 // so ONE read of each K/V block serves the whole GQA group.  At the end the
 // 4 warps combine in shared memory; a chunk that is its sequence's only one
-// writes bf16 output, otherwise it writes an fp32 (o, lse) partial to the
-// workspace and takes a ticket; the last chunk to arrive merges
+// writes bf16 output.  Otherwise the chunks' fp32 (o_i, lse_i) states merge
 //     M = max lse_i, w_i = exp(lse_i - M), o = sum w_i o_i / sum w_i
-// and resets the ticket, all in the same launch.
+// in the same launch, one of two ways:
+//   * plans of 2..4 chunks launch every (sequence, KV head) as a thread-block
+//     cluster: each chunk keeps its state in shared memory, and after a
+//     cluster barrier every chunk merges a slice of the output by reading its
+//     peers' states through distributed shared memory -- no global round
+//     trip, no fence;
+//   * larger plans write the states to the workspace and take a ticket; the
+//     last chunk to arrive merges and resets the ticket.
+//
+// Decode step (fused append): with k_new set, the warp that loads a
+// sequence's last block first writes the new token's K (RoPE) and V rows into
+// it, and every CTA rotates its q rows, so append and attention are one launch.
 //
 // e4m3 pools: the TMA loads fp8 bytes, each warp converts the tile to f16
 // (exact) in shared memory and runs the f16 MMA; k_scale folds into the
@@ -39,6 +49,9 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
+// Plans of 2..4 chunks per sequence merge inside a cluster (larger clusters
+// measured slower than the ticket merge: co-scheduling them leaves slots idle).
+constexpr int kMaxClusterSplits = 4;
 
 template <int D, bool kFp8>
 struct DecodeCfg {
@@ -109,7 +122,71 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
         tma_load_5d(dst, map, bar, 0, 0, 0, kvh, block);
 }
 
+// Fused append: one warp writes sequence seq's new token (position p) for KV
+// head kvh into row p % 16 of physical block blk -- K rotated (RoPE, when
+// cos_sin is set) and rounded to bf16 or quantised to e4m3, V copied or
+// quantised -- with the same arithmetic as the standalone append kernel, then
+// fences the writes against the TMA reads of that block that follow.
+// Lane l owns the rotation pairs (j, j + D/2) for j in [l PPL, (l+1) PPL).
 template <int D, bool kFp8>
+__device__ __forceinline__ void append_new_token(const DecodeArgs& a, int seq, int kvh, int blk, int p,
+                                                 int lane) {
+    constexpr int HALF = D / 2;
+    constexpr int PPL = HALF / 32;
+    const int j0 = lane * PPL;
+    const size_t src = (static_cast<size_t>(seq) * a.hkv + kvh) * D;
+    const size_t dst = ((static_cast<size_t>(blk) * a.hkv + kvh) * kBlockSize + p % kBlockSize) * D;
+    const __nv_bfloat16* kx = static_cast<const __nv_bfloat16*>(a.k_new) + src;
+    const __nv_bfloat16* vx = static_cast<const __nv_bfloat16*>(a.v_new) + src;
+    float lo[PPL], hi[PPL];
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        const float av = __bfloat162float(kx[j0 + k]);
+        const float bv = __bfloat162float(kx[HALF + j0 + k]);
+        if (a.cos_sin) {
+            const float c = a.cos_sin[(static_cast<size_t>(p) * HALF + j0 + k) * 2];
+            const float sn = a.cos_sin[(static_cast<size_t>(p) * HALF + j0 + k) * 2 + 1];
+            lo[k] = __fsub_rn(__fmul_rn(av, c), __fmul_rn(bv, sn));
+            hi[k] = __fadd_rn(__fmul_rn(bv, c), __fmul_rn(av, sn));
+        } else {
+            lo[k] = av;
+            hi[k] = bv;
+        }
+    }
+    if constexpr (!kFp8) {
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(a.k_pool) + dst;
+        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(a.v_pool) + dst;
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            kc[j0 + k] = __float2bfloat16_rn(lo[k]);
+            kc[HALF + j0 + k] = __float2bfloat16_rn(hi[k]);
+            vc[j0 + k] = vx[j0 + k];
+            vc[HALF + j0 + k] = vx[HALF + j0 + k];
+        }
+    } else {
+        uint8_t* kc = static_cast<uint8_t*>(a.k_pool) + dst;
+        uint8_t* vc = static_cast<uint8_t*>(a.v_pool) + dst;
+        const float ks = a.k_scale[kvh];
+        const float vs = a.v_scale[kvh];
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            kc[j0 + k] = __nv_cvt_float_to_fp8(__fdiv_rn(lo[k], ks), __NV_SATFINITE, __NV_E4M3);
+            kc[HALF + j0 + k] = __nv_cvt_float_to_fp8(__fdiv_rn(hi[k], ks), __NV_SATFINITE, __NV_E4M3);
+            vc[j0 + k] = __nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(vx[j0 + k]), vs), __NV_SATFINITE,
+                                               __NV_E4M3);
+            vc[HALF + j0 + k] = __nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(vx[HALF + j0 + k]), vs),
+                                                      __NV_SATFINITE, __NV_E4M3);
+        }
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+}
+
+// kCluster: the chunks of one (sequence, KV head) form a thread-block cluster
+// (grid x = cluster x = max_splits, so a chunk's cluster rank is blockIdx.x)
+// and merge through distributed shared memory; otherwise through the
+// workspace and a ticket.
+template <int D, bool kFp8, bool kCluster>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                                                           const __grid_constant__ CUtensorMap kmap,
                                                           const __grid_constant__ CUtensorMap vmap) {
@@ -133,12 +210,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     const int lane = threadIdx.x & 31;
     const int G = a.group;
 
+    // Without a window a chunk's blocks do not depend on the context length:
+    // read this warp's block ids (lane k: the k-th one) while the length is
+    // still in flight.  Entries past the sequence's end are read but unused.
+    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
+    int phys = 0;
+    if (a.window <= 0) {
+        const int lb = split * a.chunk_blocks + warp + lane * kWarps;
+        if (lane * kWarps < a.chunk_blocks && lb < a.mbps) phys = bt[lb];
+    }
     int ctx = a.context_lens[seq];
     // the split plan (and the workspace) covers contexts up to max_ctx, which
     // the host checked against the table capacity
+    bool clamped = false;
     if (ctx > a.max_ctx) {
         if (threadIdx.x == 0 && split == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
         ctx = a.max_ctx;
+        clamped = true;
     }
     const int lo = (a.window > 0 && ctx > a.window) ? ctx - a.window : 0;
     if (ctx <= 0) {  // no visible key: o = 0, lse = -inf
@@ -174,17 +262,30 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     __syncthreads();
 
     // Physical block ids of this warp's blocks: lane k holds the k-th one.
-    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
-    int phys = 0;
+    bool bad_id = false;
     if (lane < my_n) {
         const int lb = b0 + warp + lane * kWarps;  // logical block
-        phys = bt[a.ring > 0 ? lb % a.ring : lb];
+        if (a.window > 0) phys = bt[a.ring > 0 ? lb % a.ring : lb];
         if (phys < 0 || phys >= a.num_blocks) {
             flag_error(a.err, PKV_DEVERR_BLOCK_ID);
             phys = 0;  // read a valid block; the output is flagged invalid
+            bad_id = true;
         }
     }
     uint8_t* wbase = smem + warp * C::kWarpBytes;
+
+    // Fused append: the warp that loads the sequence's last block writes the
+    // new token into it first -- before its prologue when that block is one
+    // of the first NSTAGE, else right after (the refill that loads it comes later).
+    const int k_last = (last_blk - b0) / kWarps;
+    const bool appender = a.k_new != nullptr && !clamped && split == nsplit - 1 &&
+                          warp == (last_blk - b0) % kWarps;
+    auto append = [&]() {
+        const int pb = __shfl_sync(0xFFFFFFFFu, phys, k_last & 31);
+        const bool bad = __shfl_sync(0xFFFFFFFFu, bad_id, k_last & 31);
+        if (!bad) append_new_token<D, kFp8>(a, seq, kvh, pb, ctx - 1, lane);
+    };
+    if (appender && k_last < C::kStages) append();
     // Lane 0 issues the prologue; the shuffle reads lane k's id from lane 0's
     // point of view, so every lane takes part in it.
 #pragma unroll
@@ -199,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             load_tile<kFp8>(vdst, &vmap, &bars[warp][st], kvh, pb);
         }
     }
+    if (appender && k_last >= C::kStages) append();
 
     // Q fragments (A operand, rows = heads of the group, zero-padded to 16).
     const int g0 = lane >> 2;
@@ -215,9 +317,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                 const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
                 uint32_t v = 0;
                 if (row < G) v = *reinterpret_cast<const uint32_t*>(qb + row * D + col);
-                if constexpr (kFp8) v = pack2<true>(bf16_lo(v), bf16_hi(v));
                 qa[kk][part] = v;
             }
+        }
+        if (a.k_new != nullptr && a.cos_sin != nullptr && !clamped) {
+            // decode step: rotate q at the new token's position, rounded to
+            // bf16 as the standalone append rounds it.  Column c of k-step kk
+            // pairs with column c + D/2, held by the same lane in k-step
+            // kk + KSTEPS/2; columns c, c+1 sit in one register.
+            const float* cs = a.cos_sin + static_cast<size_t>(ctx - 1) * (D / 2) * 2;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS / 2; ++kk) {
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
+                    const float4 t = *reinterpret_cast<const float4*>(cs + col * 2);  // c, s of col, col+1
+                    const uint32_t va = qa[kk][part];
+                    const uint32_t vb = qa[kk + KSTEPS / 2][part];
+                    const float a0 = bf16_lo(va), a1 = bf16_hi(va);
+                    const float b0v = bf16_lo(vb), b1v = bf16_hi(vb);
+                    const float lo0 = __fsub_rn(__fmul_rn(a0, t.x), __fmul_rn(b0v, t.y));
+                    const float hi0 = __fadd_rn(__fmul_rn(b0v, t.x), __fmul_rn(a0, t.y));
+                    const float lo1 = __fsub_rn(__fmul_rn(a1, t.z), __fmul_rn(b1v, t.w));
+                    const float hi1 = __fadd_rn(__fmul_rn(b1v, t.z), __fmul_rn(a1, t.w));
+                    qa[kk][part] = pack2<false>(lo0, lo1);
+                    qa[kk + KSTEPS / 2][part] = pack2<false>(hi0, hi1);
+                }
+            }
+        }
+        if constexpr (kFp8) {
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                for (int part = 0; part < 4; ++part)
+                    qa[kk][part] = pack2<true>(bf16_lo(qa[kk][part]), bf16_hi(qa[kk][part]));
         }
     }
     float scale_log2 = a.sm_scale * 1.4426950408889634f;
@@ -414,7 +547,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             L += f[w] * s_l[w][r];
         }
         float inv = L > 0.f ? (kFp8 ? a.v_scale[kvh] : 1.f) / L : 0.f;
-        float lse = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
+        // a failed chunk's state is excluded from the merge by lse = -inf
+        float lse = L > 0.f && !cta_failed ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
         if (a.sinks && nsplit == 1 && r < G) {
             // the sink joins the normaliser: lse' = ln(e^lse + e^s), o scaled by e^(lse - lse')
             const float sk = a.sinks[kvh * G + r];
@@ -442,6 +576,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                 else
                     static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(ov);
                 if (a.lse_out && d == 0) a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] = s_l[0][r];
+            } else if (kCluster) {
+                // this chunk's state stays in shared memory, in place of warp 0's rows
+                comb[r * C::kCombStride + d] = ov;
             } else {
                 const size_t prow = (pair * a.max_splits + split) * G + r;
                 a.part_o[prow * D + d] = ov;
@@ -450,6 +587,76 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         }
     }
     if (nsplit == 1) return;
+
+    if constexpr (kCluster) {
+        // ---- cluster merge: chunk c of the pair holds o_c (rows of warp 0's
+        // slice of comb) and lse_c (s_l[0]) in its shared memory
+        cluster_sync();
+        float* wts = comb + 16 * C::kCombStride;  // warp 1's slice, free now: [chunk][16]
+        float* rowM = wts + kMaxClusterSplits * 16;
+        float* rowW = rowM + 16;
+        if (threadIdx.x < 16) {
+            const int r = threadIdx.x;
+            float l[kMaxClusterSplits];
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterSplits; ++c) {
+                l[c] = c < nsplit ? ld_cluster_f32(cluster_map(smem_u32(&s_l[0][r]), c)) : -INFINITY;
+                M = fmaxf(M, l[c]);
+            }
+            float W = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterSplits; ++c) {
+                const float wv = l[c] == -INFINITY ? 0.f : __expf(l[c] - M);
+                wts[c * 16 + r] = wv;
+                W += wv;
+            }
+            if (a.sinks && r < G && M != -INFINITY) W += __expf(a.sinks[kvh * G + r] - M);
+            rowM[r] = M;
+            rowW[r] = W;
+        }
+        __syncthreads();
+        // this chunk merges its share of the G x D output, in float4 slots
+        constexpr int kSlotsPerRow = D / 4;
+        const int total = G * kSlotsPerRow;
+        const int s_lo = split * total / nsplit;
+        const int s_hi = (split + 1) * total / nsplit;
+        for (int slot = s_lo + threadIdx.x; slot < s_hi; slot += kThreads) {
+            const int r = slot / kSlotsPerRow;
+            const int c4 = slot % kSlotsPerRow;
+            const uint32_t local = smem_u32(comb + r * C::kCombStride + c4 * 4);
+            float4 v[kMaxClusterSplits];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterSplits; ++c)
+                if (c < nsplit) v[c] = ld_cluster_f32x4(cluster_map(local, c));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < kMaxClusterSplits; ++c) {
+                const float w = wts[c * 16 + r];
+                if (c < nsplit && w != 0.f) {
+                    acc.x += w * v[c].x;
+                    acc.y += w * v[c].y;
+                    acc.z += w * v[c].z;
+                    acc.w += w * v[c].w;
+                }
+            }
+            const float W = rowW[r];
+            const float inv = W > 0.f ? 1.f / W : 0.f;
+            const size_t oi = (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + c4 * 4;
+            if (a.out_f32) {
+                *reinterpret_cast<float4*>(a.out_f32 + oi) =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            } else {
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
+                    make_uint2(pack2<false>(acc.x * inv, acc.y * inv), pack2<false>(acc.z * inv, acc.w * inv));
+            }
+            if (a.lse_out && c4 == 0)
+                a.lse_out[static_cast<size_t>(seq) * a.hq + kvh * G + r] =
+                    W > 0.f ? rowM[r] + __logf(W) : -INFINITY;
+        }
+        cluster_sync();  // no chunk exits while a peer may still read its shared memory
+        return;
+    }
 
     // ---- ticket: the last chunk of this (sequence, KV head) merges
     __threadfence();
@@ -548,21 +755,24 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
                             cudaStream_t stream) {
     using C = DecodeCfg<D, kFp8>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
-    auto kern = decode_kernel<D, kFp8>;
+    static_assert((kMaxClusterSplits + 2) * 16 <= 16 * C::kCombStride, "cluster merge scratch");
+    const bool cluster = a.max_splits >= 2 && a.max_splits <= kMaxClusterSplits;
+    auto kern = cluster ? decode_kernel<D, kFp8, true> : decode_kernel<D, kFp8, false>;
     // The shared-memory opt-in is a per-device function attribute: set it on
     // the first launch on each device (never inside a stream capture).
-    static bool attr_set[64] = {};
+    static bool attr_set[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[cluster][dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[cluster][dev] = true;
     }
     dim3 grid(a.max_splits, a.hkv, a.num_seqs);
-    return launch_pdl(kern, grid, dim3(kThreads), C::kSmemBytes, stream, a, kmap, vmap);
+    return launch_pdl_cluster(kern, grid, dim3(kThreads), C::kSmemBytes, stream,
+                              cluster ? static_cast<unsigned>(a.max_splits) : 1u, a, kmap, vmap);
 }
 
 }  // namespace

@@ -97,6 +97,15 @@ struct DecodeArgs {
     int32_t ring;     // > 0: logical block b is table entry b % ring
     int64_t num_blocks;
     float sm_scale;
+    // Fused append (decode step): when k_new is set, every sequence's new
+    // token (position context_lens[s] - 1) is written into its cache row by
+    // the warp that loads that block, before the load; cos_sin (nullable)
+    // rotates it and q.
+    const void* k_new;      // bf16 [num_seqs][hkv][d]
+    const void* v_new;      // bf16 [num_seqs][hkv][d]
+    const float* cos_sin;   // fp32 [max_pos][d/2][2]
+    void* k_pool;           // the pools the tensor maps view, written
+    void* v_pool;
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);

@@ -157,6 +157,26 @@ def test_invalid_arguments_return_status_before_any_device_work(lib):
     assert st == 2 and "ring" in pkv.pkv_last_error()
 
 
+def test_decode_step_validates_its_new_token_arguments(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    d = _desc()
+
+    def step(k_new, v_new, cos_sin, max_pos, max_ctx=100):
+        return lib.pkv_decode_step(ctypes.byref(d), fake, k_new, v_new, cos_sin, max_pos, fake, fake,
+                                   None, None, fake, fake, 1, max_ctx, 0.1, -1, None, 0, fake, None,
+                                   None, 0, None)
+
+    assert step(None, fake, None, 0) == 1 and "k_new" in pkv.pkv_last_error()
+    assert step(fake, None, None, 0) == 1 and "v_new" in pkv.pkv_last_error()
+    assert step(P(0x10008), fake, None, 0) == 1 and "aligned" in pkv.pkv_last_error()
+    # the table must cover the new token's position max_context_len - 1
+    assert step(fake, fake, fake, 99) == 1 and "rope_max_pos" in pkv.pkv_last_error()
+    # the shared checks of decode still apply
+    assert step(fake, fake, fake, 4097, max_ctx=256 * 16 + 1) == 1
+    assert "max_context_len" in pkv.pkv_last_error()
+
+
 def test_planner_fills_the_gpu_and_respects_limits(lib):
     sms = 152
     # (Hq, Hkv, D, dtype, B, max_ctx, window)

@@ -1,0 +1,189 @@
+"""GPU parity of the fused decode step (llm-infer, "What It Does": KV writes
+and fused RoPE inside the decode step): one launch appends every sequence's
+new token (RoPE'd K, V; e4m3 quantised for FP8 pools), rotates q and attends.
+
+Checked three ways on the same seeded bytes:
+  * the cache after the step equals the oracle's append, byte for byte;
+  * out / lse match the oracle's attention over that cache with the oracle's
+    rotated q, within the attention tolerance;
+  * out / lse / cache equal, bit for bit, the two-launch path (append with an
+    in-place q rotation, then plain decode) -- the fusion changes no
+    arithmetic."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_21_gb300 as pkv
+from tests._cases import BS, PagedCase, bf16_bits
+from tests._gpu import DEV, NTHREADS, assert_close, assert_lse_close, pool_np
+
+pytestmark = pytest.mark.gpu
+
+LENS = [1, 2, 15, 16, 17, 33, 64, 65, 129, 700, 2049, 4100]
+
+
+def _pool(bits):
+    t = torch.from_numpy(np.ascontiguousarray(bits))
+    if bits.dtype == np.uint16:
+        return t.view(torch.int16).view(torch.bfloat16).to(DEV)
+    return t.to(DEV)
+
+
+def _dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _setup(seed, lens, hq, hkv, d, fp8, rope):
+    rng = np.random.default_rng(seed)
+    case = PagedCase(rng, lens, hq, hkv, d, fp8=fp8)
+    B = len(lens)
+    k_new = bf16_bits(rng.standard_normal((B, hkv, d)).astype(np.float32))
+    v_new = bf16_bits(rng.standard_normal((B, hkv, d)).astype(np.float32))
+    table = oracle.rope_table(1e6, d, int(max(lens))) if rope else None
+    return case, k_new, v_new, table
+
+
+def _oracle_step(case, k_new, v_new, table, tables, k_cache, v_cache, window, ring=0, sinks=None):
+    """Oracle: append at position len - 1 (rotating q), then attention."""
+    B = len(case.lens)
+    kc, vc = k_cache.copy(), v_cache.copy()
+    q_rot = oracle.append_rope(num_q_heads=case.hq, num_kv_heads=case.hkv, head_dim=case.d,
+                               block_size=BS, kv_dtype=1 if case.fp8 else 0, k_cache=kc, v_cache=vc,
+                               block_tables=tables, token_to_seq=np.arange(B, dtype=np.int32),
+                               positions=(case.lens - 1).astype(np.int32), k_new=k_new, v_new=v_new,
+                               q=case.q, cos_sin=table, k_scale=case.k_scale, v_scale=case.v_scale,
+                               ring_blocks=ring)
+    ref, ref_lse = oracle.paged_attention(q=q_rot, k_cache=kc, v_cache=vc, block_tables=tables,
+                                          qo_indptr=np.arange(B + 1), kv_lens=case.lens,
+                                          num_q_heads=case.hq, num_kv_heads=case.hkv,
+                                          sm_scale=1 / math.sqrt(case.d), window=window,
+                                          kv_dtype=1 if case.fp8 else 0, k_scale=case.k_scale,
+                                          v_scale=case.v_scale, ring_blocks=ring, sinks=sinks,
+                                          nthreads=NTHREADS)
+    return kc, vc, ref, ref_lse
+
+
+def _gpu(case, k_new, v_new, table, tables, k_cache, v_cache, window, chunk, fused, ring=0,
+         sinks=None):
+    B = len(case.lens)
+    desc = pkv.make_desc(num_q_heads=case.hq, num_kv_heads=case.hkv, head_dim=case.d,
+                         num_blocks=k_cache.shape[0], max_blocks_per_seq=tables.shape[1],
+                         kv_dtype=1 if case.fp8 else 0, ring_blocks=ring)
+    max_ctx = int(case.lens.max())
+    kd, vd = _pool(k_cache), _pool(v_cache)
+    q = _pool(case.q)
+    out = torch.full((B, case.hq, case.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, case.hq), float("nan"), device=DEV)
+    ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, window, chunk), 256),
+                     dtype=torch.uint8, device=DEV)
+    lens = _dev(case.lens)
+    tabs = _dev(tables)
+    ks, vs, sk = _dev(case.k_scale), _dev(case.v_scale), _dev(sinks)
+    cs = _dev(table)
+    if fused:
+        q_before = q.clone()
+        pkv.pkv_decode_step(desc, q, _pool(k_new), _pool(v_new), kd, vd, tabs, lens, max_ctx,
+                            1 / math.sqrt(case.d), out, lse, ws, cos_sin=cs, window=window,
+                            chunk_blocks=chunk, k_scale=ks, v_scale=vs, sinks=sk)
+        torch.cuda.synchronize()
+        assert torch.equal(q, q_before), "the decode step must not modify q"
+    else:
+        pkv.pkv_append_rope(desc, kd, vd, tabs, _dev(np.arange(B, dtype=np.int32)),
+                            _dev((case.lens - 1).astype(np.int32)), _pool(k_new), _pool(v_new), q=q,
+                            cos_sin=cs, k_scale=ks, v_scale=vs)
+        pkv.pkv_decode_attention(desc, q, kd, vd, tabs, lens, max_ctx, 1 / math.sqrt(case.d), out, lse,
+                                 ws, window=window, chunk_blocks=chunk, k_scale=ks, v_scale=vs,
+                                 sinks=sk)
+        torch.cuda.synchronize()
+    assert pkv.pkv_device_errors() == 0
+    assert int(ws[:4 * B * case.hkv].view(torch.int32).abs().sum().item()) == 0, "tickets not reset"
+    return out, lse, kd, vd
+
+
+@pytest.mark.parametrize("hq,hkv,d,fp8", [(16, 2, 128, False), (32, 8, 128, False), (8, 2, 64, False),
+                                          (64, 8, 64, True), (16, 2, 128, True)])
+@pytest.mark.parametrize("rope", [True, False])
+def test_decode_step_matches_oracle_and_two_launch_path(hq, hkv, d, fp8, rope):
+    case, k_new, v_new, table = _setup(80 + d + hq + fp8, LENS, hq, hkv, d, fp8, rope)
+    kc, vc, ref, ref_lse = _oracle_step(case, k_new, v_new, table, case.tables, case.k_cache,
+                                        case.v_cache, -1)
+    for chunk in (0, 1, 3):
+        out, lse, kd, vd = _gpu(case, k_new, v_new, table, case.tables, case.k_cache, case.v_cache,
+                                -1, chunk, fused=True)
+        assert np.array_equal(pool_np(kd), kc), "K cache after the step differs from the oracle's append"
+        assert np.array_equal(pool_np(vd), vc), "V cache after the step differs from the oracle's append"
+        assert_close(out, ref, "decode step %d/%d/%d fp8=%d chunk %d" % (hq, hkv, d, fp8, chunk))
+        assert_lse_close(lse, ref_lse, "decode step lse")
+        out2, lse2, kd2, vd2 = _gpu(case, k_new, v_new, table, case.tables, case.k_cache, case.v_cache,
+                                    -1, chunk, fused=False)
+        assert torch.equal(out, out2) and torch.equal(lse, lse2), "fused and two-launch outputs differ"
+        assert torch.equal(kd, kd2) and torch.equal(vd, vd2), "fused and two-launch caches differ"
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_step_window_sinks_ring(fp8):
+    """Sliding window 128 over a 9-block ring, with sink logits: the step
+    writes into ring entry ((len - 1) / 16) mod 9."""
+    hq, hkv, d = (64, 8, 64) if fp8 else (32, 8, 128)
+    case, k_new, v_new, table = _setup(90 + fp8, [1, 16, 17, 128, 129, 145, 1000, 3001], hq, hkv, d,
+                                       fp8, True)
+    ring = 9
+    B = len(case.lens)
+    rk = np.zeros((B * ring,) + case.k_cache.shape[1:], case.k_cache.dtype)
+    rv = np.zeros_like(rk)
+    rtabs = (np.arange(ring)[None, :] + ring * np.arange(B)[:, None]).astype(np.int32)
+    for s in range(B):
+        for b in range((int(case.lens[s]) + BS - 1) // BS):
+            rk[rtabs[s, b % ring]] = case.k_cache[case.tables[s, b]]
+            rv[rtabs[s, b % ring]] = case.v_cache[case.tables[s, b]]
+    rng = np.random.default_rng(7)
+    sinks = rng.uniform(-1.0, 4.0, hq).astype(np.float32)
+    kc, vc, ref, ref_lse = _oracle_step(case, k_new, v_new, table, rtabs, rk, rv, 128, ring=ring,
+                                        sinks=sinks)
+    for chunk in (0, 2):
+        out, lse, kd, vd = _gpu(case, k_new, v_new, table, rtabs, rk, rv, 128, chunk, fused=True,
+                                ring=ring, sinks=sinks)
+        assert np.array_equal(pool_np(kd), kc) and np.array_equal(pool_np(vd), vc)
+        assert_close(out, ref, "ring step chunk %d" % chunk)
+        assert_lse_close(lse, ref_lse, "ring step lse")
+        out2, lse2, _, _ = _gpu(case, k_new, v_new, table, rtabs, rk, rv, 128, chunk, fused=False,
+                                ring=ring, sinks=sinks)
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_decode_step_in_a_graph_repeats():
+    """Replaying a captured step rewrites the same slots with the same bytes:
+    the cache and the output are those of one step, however many replays."""
+    case, k_new, v_new, table = _setup(95, [5, 300, 1024, 2500], 16, 2, 128, False, True)
+    kc, vc, ref, ref_lse = _oracle_step(case, k_new, v_new, table, case.tables, case.k_cache,
+                                        case.v_cache, -1)
+    B = len(case.lens)
+    desc = pkv.make_desc(num_q_heads=16, num_kv_heads=2, head_dim=128, num_blocks=case.k_cache.shape[0],
+                         max_blocks_per_seq=case.tables.shape[1])
+    max_ctx = int(case.lens.max())
+    kd, vd, q = _pool(case.k_cache), _pool(case.v_cache), _pool(case.q)
+    kn, vn, cs = _pool(k_new), _pool(v_new), _dev(table)
+    tabs, lens = _dev(case.tables), _dev(case.lens)
+    out = torch.empty((B, 16, 128), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, 16), device=DEV)
+    ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, 2), 256), dtype=torch.uint8,
+                     device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pkv.pkv_decode_step(desc, q, kn, vn, kd, vd, tabs, lens, max_ctx, 1 / math.sqrt(128), out, lse, ws,
+                            cos_sin=cs, chunk_blocks=2, stream=s)  # warm-up (attribute set)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.pkv_decode_step(desc, q, kn, vn, kd, vd, tabs, lens, max_ctx, 1 / math.sqrt(128), out, lse, ws,
+                            cos_sin=cs, chunk_blocks=2, stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(pool_np(kd), kc) and np.array_equal(pool_np(vd), vc)
+    assert_close(out, ref, "graph-replayed step")
+    assert_lse_close(lse, ref_lse, "graph-replayed step")
+    assert pkv.pkv_device_errors() == 0
