@@ -104,7 +104,8 @@ def _gpu(case, k_new, v_new, table, tables, k_cache, v_cache, window, chunk, fus
 
 
 @pytest.mark.parametrize("hq,hkv,d,fp8", [(16, 2, 128, False), (32, 8, 128, False), (8, 2, 64, False),
-                                          (64, 8, 64, True), (16, 2, 128, True)])
+                                          (64, 8, 64, True), (16, 2, 128, True), (16, 4, 64, False),
+                                          (32, 8, 128, True)])
 @pytest.mark.parametrize("rope", [True, False])
 def test_decode_step_matches_oracle_and_two_launch_path(hq, hkv, d, fp8, rope):
     case, k_new, v_new, table = _setup(80 + d + hq + fp8, LENS, hq, hkv, d, fp8, rope)

@@ -17,7 +17,11 @@ from tests._gpu import DEV, NTHREADS, assert_close, assert_lse_close
 pytestmark = pytest.mark.gpu
 
 # 64 blocks at most: chunk c gives ceil(64 / c) chunks for the longest sequence
-CHUNKS = {32: 2, 22: 3, 16: 4, 13: 5, 11: 6, 10: 7, 8: 8, 7: 10, 4: 16}
+CHUNKS = {64: 1, 32: 2, 22: 3, 16: 4, 13: 5, 11: 6, 10: 7, 8: 8, 7: 10, 4: 16}
+
+# (Hq, Hkv, D, e4m3): both head dims, both pool types, group sizes 4..8
+SHAPES = [(16, 2, 128, False), (64, 8, 64, True), (16, 4, 64, False), (32, 8, 128, True),
+          (16, 4, 64, True), (16, 2, 64, True)]
 
 
 def _pool(bits):
@@ -31,10 +35,9 @@ def _dev(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_cluster_and_ticket_merges_match_the_oracle(fp8):
-    rng = np.random.default_rng(120 + fp8)
-    hq, hkv, d = (64, 8, 64) if fp8 else (16, 2, 128)
+@pytest.mark.parametrize("hq,hkv,d,fp8", SHAPES)
+def test_cluster_and_ticket_merges_match_the_oracle(hq, hkv, d, fp8):
+    rng = np.random.default_rng(120 + hq + hkv + d + fp8)
     lens = [1, 16, 17, 100, 257, 511, 700, 1024]
     case = PagedCase(rng, lens, hq, hkv, d, fp8=fp8)
     desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=case.num_blocks,
