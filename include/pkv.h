@@ -159,8 +159,10 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc *desc, void *k_cache, void *v_ca
  * sum_t e^{l_t}), lse = ln(e^{sinks[h]} + sum_t e^{l_t}).
  * The KV range of each (sequence, KV head) is cut into chunks of whole
  * blocks (pkv_decode_plan); every chunk runs as one CTA whose warps share
- * the G query heads of the group; partial (o, lse) states go to the
- * workspace and the last chunk to finish merges them in the same launch.
+ * the G query heads of the group, and the chunks' partial (o, lse) states
+ * merge in the same launch: with 2-4 chunks inside a thread-block cluster
+ * (distributed shared memory), with more through the workspace, where the
+ * last chunk to finish merges them.
  *   q        : bf16 [num_seqs][Hq][D].      out: bf16 [num_seqs][Hq][D].
  *   lse_out  : fp32 [num_seqs][Hq], nullable.
  *   context_lens : int32 [num_seqs], each in [1, max_blocks_per_seq*bs]
