@@ -84,31 +84,51 @@ __device__ __forceinline__ uint32_t kv_off(int r, int chunk) {
     return static_cast<uint32_t>(u * 128 + (((chunk & 7) ^ (u & 7)) << 4));
 }
 
+// Four e4m3 codes (one 32-bit word, lowest byte first) -> two f16x2 words,
+// exactly (every e4m3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 // f16 staging of an fp8 tile: src [16][D] bytes (row-major) -> dst in the
-// kv_off layout, the one the bf16 path gets from TMA.
+// kv_off layout, the one the bf16 path gets from TMA.  Lane l converts the
+// 16-byte chunks l, l + 32, ...; their offsets depend on the lane only
+// (Fp8Lane, computed once per kernel).
 template <int D>
-__device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, int lane) {
-    constexpr int kChunksPerRow = D / 16;
-    constexpr int kChunks = kBlockSize * kChunksPerRow;
+struct Fp8Lane {
+    static constexpr int kChunksPerRow = D / 16;
+    static constexpr int kPerLane = kBlockSize * kChunksPerRow / 32;  // 2 (D=64) or 4 (D=128)
+    uint32_t src[kPerLane];
+    uint32_t dst0[kPerLane];
+    uint32_t dst1[kPerLane];
+    __device__ __forceinline__ explicit Fp8Lane(int lane) {
 #pragma unroll
-    for (int c = lane; c < kChunks; c += 32) {
-        const int r = c / kChunksPerRow;
-        const int cc = c % kChunksPerRow;
-        const uint4 v = *reinterpret_cast<const uint4*>(src + c * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-            h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-            h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+        for (int i = 0; i < kPerLane; ++i) {
+            const int c = lane + 32 * i;
+            const int r = c / kChunksPerRow;
+            const int d0 = (c % kChunksPerRow) * 2;  // destination 16-byte chunk (8 f16) in the row
+            src[i] = static_cast<uint32_t>(c * 16);
+            dst0[i] = kv_off<D>(r, d0);
+            dst1[i] = kv_off<D>(r, d0 + 1);
         }
-        const int d0 = cc * 2;  // destination 16-byte chunk (8 f16) index in the row
-        *reinterpret_cast<uint4*>(dst + kv_off<D>(r, d0)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(dst + kv_off<D>(r, d0 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+};
+
+template <int D>
+__device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, const Fp8Lane<D>& ln) {
+#pragma unroll
+    for (int i = 0; i < Fp8Lane<D>::kPerLane; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ln.src[i]);
+        uint32_t h[8];
+        e4m3x4_to_f16x4(v.x, h[0], h[1]);
+        e4m3x4_to_f16x4(v.y, h[2], h[3]);
+        e4m3x4_to_f16x4(v.z, h[4], h[5]);
+        e4m3x4_to_f16x4(v.w, h[6], h[7]);
+        *reinterpret_cast<uint4*>(dst + ln.dst0[i]) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + ln.dst1[i]) = make_uint4(h[4], h[5], h[6], h[7]);
     }
 }
 
@@ -362,6 +382,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
 #pragma unroll
     for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
+    const Fp8Lane<D> fp8_lane(lane);
     uint8_t* convK = wbase + C::kStages * C::kStageBytes;
     uint8_t* convV = convK + (kFp8 ? kBlockSize * D * 2 : 0);
     bool failed = false;
@@ -377,8 +398,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         const uint8_t* ktile = wbase + st * C::kStageBytes;
         const uint8_t* vtile = ktile + C::kTileBytes;
         if constexpr (kFp8) {
-            convert_fp8_tile<D>(ktile, convK, lane);
-            convert_fp8_tile<D>(vtile, convV, lane);
+            convert_fp8_tile<D>(ktile, convK, fp8_lane);
+            convert_fp8_tile<D>(vtile, convV, fp8_lane);
             __syncwarp();
             ktile = convK;
             vtile = convV;
