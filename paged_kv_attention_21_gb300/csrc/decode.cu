@@ -63,7 +63,7 @@ struct DecodeCfg {
     static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
     // bf16: one 5-D box per tile (16 rows x D/64 swizzled 128-byte slices);
     // fp8: one unswizzled 4-D box of 16 rows x D bytes
-    static constexpr int kConvBytes = kFp8 ? 2 * kBlockSize * D * 2 : 0;  // f16 K + V
+    static constexpr int kConvBytes = kFp8 ? kBlockSize * D * 2 : 0;  // f16 V (K is read raw)
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
     static constexpr int kCombBytes = kWarps * 16 * kCombStride * 4;
@@ -366,11 +366,32 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             }
         }
         if constexpr (kFp8) {
+            // e4m3 pools: K fragments come straight from the raw tile, lane
+            // (g, tig) reading its rows' bytes [tig D/4, (tig+1) D/4), so
+            // k-step kk of that lane holds dims tig D/4 + 4 kk + {0,1} (k =
+            // 2 tig, 2 tig + 1) and + {2,3} (k = 2 tig + 8, 2 tig + 9).  The
+            // dot product is a sum over dims, so q takes the same order:
+            // stage the rows in shared memory and read them back permuted.
+            uint8_t* qs = wbase + C::kStages * C::kStageBytes;  // the f16 V buffer, free until the loop
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk)
 #pragma unroll
-                for (int part = 0; part < 4; ++part)
-                    qa[kk][part] = pack2<true>(bf16_lo(qa[kk][part]), bf16_hi(qa[kk][part]));
+                for (int part = 0; part < 4; ++part) {
+                    const int row = g0 + ((part & 1) ? 8 : 0);
+                    const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
+                    *reinterpret_cast<uint32_t*>(qs + (row * D + col) * 2) = qa[kk][part];
+                }
+            __syncwarp();
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    const int row = g0 + ((part & 1) ? 8 : 0);
+                    const int dim = tig * (D / 4) + 4 * kk + ((part & 2) ? 2 : 0);
+                    const uint32_t v = *reinterpret_cast<const uint32_t*>(qs + (row * D + dim) * 2);
+                    qa[kk][part] = pack2<true>(bf16_lo(v), bf16_hi(v));
+                }
+            __syncwarp();
         }
     }
     float scale_log2 = a.sm_scale * 1.4426950408889634f;
@@ -383,8 +404,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
     const Fp8Lane<D> fp8_lane(lane);
-    uint8_t* convK = wbase + C::kStages * C::kStageBytes;
-    uint8_t* convV = convK + (kFp8 ? kBlockSize * D * 2 : 0);
+    uint8_t* convV = wbase + C::kStages * C::kStageBytes;
     bool failed = false;
     int k = 0;
     for (; k < my_n; ++k) {
@@ -398,10 +418,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         const uint8_t* ktile = wbase + st * C::kStageBytes;
         const uint8_t* vtile = ktile + C::kTileBytes;
         if constexpr (kFp8) {
-            convert_fp8_tile<D>(ktile, convK, fp8_lane);
             convert_fp8_tile<D>(vtile, convV, fp8_lane);
             __syncwarp();
-            ktile = convK;
             vtile = convV;
         }
         const uint32_t kaddr = smem_u32(ktile);
@@ -411,7 +429,29 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         float sacc[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-        {
+        if constexpr (kFp8) {
+            // rows g (tokens 0-7 tile) and g + 8 (tokens 8-15 tile), bytes
+            // [tig D/4, (tig+1) D/4): word kk -> k-step kk's two f16 pairs
+            uint32_t kw[2][D / 16];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int q4 = 0; q4 < D / 64; ++q4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(ktile + (g0 + 8 * n) * D + tig * (D / 4) + 16 * q4);
+                    kw[n][4 * q4] = v.x;
+                    kw[n][4 * q4 + 1] = v.y;
+                    kw[n][4 * q4 + 2] = v.z;
+                    kw[n][4 * q4 + 3] = v.w;
+                }
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                uint32_t b0, b1, b2, b3;
+                e4m3x4_to_f16x4(kw[0][kk], b0, b1);
+                e4m3x4_to_f16x4(kw[1][kk], b2, b3);
+                mma_16816<true>(sacc[0], qa[kk], b0, b1);
+                mma_16816<true>(sacc[1], qa[kk], b2, b3);
+            }
+        } else {
             const int tok = (lane & 7) + ((lane >> 4) << 3);
             const int csel = (lane >> 3) & 1;
 #pragma unroll
@@ -423,6 +463,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                 mma_16816<kFp8>(sacc[1], qa[kk], b10, b11);
             }
         }
+        (void)kaddr;
 
         // ---- mask + online softmax (exp2 domain)
         const int blk = b0 + warp + k * kWarps;
