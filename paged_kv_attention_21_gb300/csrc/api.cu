@@ -7,6 +7,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <utility>
+#include <vector>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -672,6 +674,19 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     a.total_q = total_q_tokens;
     a.num_blocks = staged.num_blocks;
     a.sm_scale = sm_scale;
+    if (qo_indptr_host && kv_lens_host && num_seqs <= pkv::kPrefillOrderMax) {
+        // dispatch the sequences with the most causal work first: key-query
+        // pairs q (kv - q) + q (q + 1) / 2 of each sequence
+        std::vector<std::pair<int64_t, int>> work(static_cast<size_t>(num_seqs));
+        for (int s = 0; s < num_seqs; ++s) {
+            const int64_t ql = qo_indptr_host[s + 1] - qo_indptr_host[s];
+            const int64_t kl = kv_lens_host[s];
+            work[static_cast<size_t>(s)] = {-(ql * (kl - ql) + ql * (ql + 1) / 2), s};
+        }
+        std::stable_sort(work.begin(), work.end());
+        for (int i = 0; i < num_seqs; ++i) a.seq_order[i] = static_cast<uint16_t>(work[static_cast<size_t>(i)].second);
+        a.ordered = 1;
+    }
     CUtensorMap qmap;
     st = q_map(q, total_q_tokens, desc, G, QT, &qmap);
     if (st != PKV_OK) return st;

@@ -110,6 +110,7 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 
+constexpr int kPrefillOrderMax = 256;  // sequences the prefill launch can reorder
 struct PrefillArgs {
     const void* q;
     const float* k_scale;  // nullable: per KV head, folded into the logit scale (staged FP8 pools)
@@ -125,6 +126,10 @@ struct PrefillArgs {
     int32_t total_q;  // rows of q / out
     int64_t num_blocks;
     float sm_scale;
+    // ordered != 0: grid z index i runs sequence seq_order[i], the host's
+    // order of decreasing work, so the heaviest CTAs are dispatched first
+    int32_t ordered;
+    uint16_t seq_order[kPrefillOrderMax];
 };
 // Query tokens per CTA tile for a group size (rows = tokens * group <= 128).
 int prefill_tc_q_tile(int group);

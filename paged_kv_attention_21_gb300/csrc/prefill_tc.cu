@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
     const int kvh = blockIdx.y;
-    const int seq = blockIdx.z;
+    const int seq = a.ordered ? static_cast<int>(a.seq_order[blockIdx.z]) : static_cast<int>(blockIdx.z);
     const int G = a.group;
     const int QT = a.q_tile;
     const int q0 = a.qo_indptr[seq];
