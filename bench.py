@@ -47,9 +47,12 @@ def parse_args():
     p.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
                    help="workload: 2 Qwen2.5-3B decode (default), 3 Qwen3-4B decode+append, "
                         "4 Llama-3-8B mixed step, 5 FP8 two-layer decode")
-    p.add_argument("--part", choices=["step", "prefill"], default="step",
+    p.add_argument("--part", choices=["step", "prefill", "cascade", "verify", "cow", "ring",
+                                      "fp8-prefill"], default="step",
                    help="step: the workload's whole step (default); prefill: the ragged causal "
-                        "prefill part of workload 4 alone, timed against the tensor-core peak")
+                        "prefill part of workload 4 alone, timed against the tensor-core peak; "
+                        "cascade / verify / cow / ring / fp8-prefill: the next-step rows, each "
+                        "on its own seeded workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--two-launch", action="store_true",
                    help="run append and decode as two launches per layer instead of the "
@@ -614,6 +617,261 @@ def main_prefill(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------ next-step parts --
+
+def _timed_launches(run, K, W, dev, flush):
+    """W untimed launches, then K launches each after an L2 flush (a 256 MiB
+    write outside the events), timed with CUDA events on the launching
+    stream.  Returns (per-launch ms list, clocks)."""
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(W):
+        run()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index)
+    times = []
+    for _ in range(K):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize(dev)
+    return times, sampler.stop()
+
+
+def _part_line(args, world, metric, value, unit, ms_list, dtype, config, roofline, launches,
+               clocks, extra=None):
+    ms = float(np.mean(ms_list))
+    roofline = dict(roofline, avg_launch_ms=round(ms, 5),
+                    p10_ms=round(float(np.percentile(ms_list, 10)), 5),
+                    p90_ms=round(float(np.percentile(ms_list, 90)), 5))
+    line = {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world,
+            "steps": len(ms_list), "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic: seeded N(0,1) values, seeded lengths and scattered block tables",
+            "config": dict(config, l2="256 MiB write before every timed launch"),
+            "roofline": roofline, "gpu_launches": launches * len(ms_list), "clocks": clocks}
+    if extra:
+        line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def main_next(args, rank, world, local):
+    """One next-step row on its own seeded workload (rank 0 reports):
+      cascade     shared-prefix decode (16 groups x 8 sequences, 32/8 heads, D128), KV GB/s
+                  with each prefix read once, beside plain decode over the same contexts;
+      verify      speculative-verify queries of 2-8 tokens per sequence through the ragged
+                  kernel on the Qwen2.5-3B-shaped cache, KV GB/s and query tokens/s;
+      cow         copy-on-write of 4096 whole blocks of that pool, GB/s moved;
+      ring        the FP8 workload's window-128 layer over a 9-block ring cache with sink
+                  logits, one decode step (append + decode), KV GB/s;
+      fp8-prefill the Llama-3-8B-shaped prefill part over e4m3 pools (staging + tcgen05
+                  prefill), TFLOP/s."""
+    import paged_kv_attention_21_gb300 as pkv
+    from paged_kv_attention_21_gb300 import workloads as wl
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K, W = max(1, args.steps), max(3, args.warmup)
+    hbm, hbm_kind = measured_peaks()
+    part = args.part
+
+    if part == "cascade":
+        spec = wl.CASCADE_DECODE
+        if rank:
+            spec = wl.dataclasses.replace(spec, seed=spec.seed + 7919 * rank)
+        cb = wl.make_cascade_batch(spec, dev)
+        B = spec.groups * spec.group_size
+        desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                             head_dim=spec.head_dim, num_blocks=cb.k_cache.shape[0],
+                             max_blocks_per_seq=cb.prefix_tables.shape[1])
+        max_suffix = int(cb.suffix_host.max())
+        ws = torch.zeros(max(pkv.pkv_cascade_workspace_size(desc, B, max_suffix), 256),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(cb.q)
+        run = lambda: pkv.pkv_cascade_decode(desc, cb.q, cb.k_cache, cb.v_cache, cb.group_indptr,
+                                             cb.group_indptr_host, cb.prefix_tables, cb.prefix_lens,
+                                             cb.prefix_host, cb.suffix_tables, cb.suffix_lens,
+                                             max_suffix, spec.sm_scale, out, None, ws)
+        times, clocks = _timed_launches(run, K, W, dev, flush)
+        max_ctx = int(cb.prefix_host.max() + cb.suffix_host.max())
+        wsd = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, 0), 256),
+                          dtype=torch.uint8, device=dev)
+        plain = lambda: pkv.pkv_decode_attention(desc, cb.q, cb.k_cache, cb.v_cache,
+                                                 cb.concat_tables, cb.concat_lens, max_ctx,
+                                                 spec.sm_scale, out, None, wsd)
+        ptimes, _ = _timed_launches(plain, K, W, dev, flush)
+        ms = reduce_max(float(np.mean(times)), world)
+        pms = reduce_max(float(np.mean(ptimes)), world)
+        if rank:
+            return
+        nbytes = cb.cascade_kv_bytes()
+        gbs = nbytes / (ms / 1e3) / 1e9
+        _part_line(args, world, "shared-prefix (cascade) decode KV GB/s, each prefix read once",
+                   gbs * world, "GB/s", times, "bf16",
+                   {"workload": spec.name, "sequences": B, "groups": spec.groups},
+                   {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4), "traffic": None,
+                    "kernel": "prefix pass (prefill_tc_kernel) + suffix decode + merge_kernel",
+                    "peak_source": "%s hbm_gbs" % hbm_kind, "algorithmic_bytes_per_launch": nbytes},
+                   3, clocks,
+                   {"plain_decode": {"ms": round(pms, 5), "kv_bytes": cb.uncached_kv_bytes(),
+                                     "speedup_of_cascade": round(pms / ms, 3),
+                                     "note": "pkv_decode_attention over each sequence's "
+                                             "concatenated prefix + suffix table"}})
+        return
+
+    if part in ("verify", "cow"):
+        spec = wl.QWEN25_3B
+        if rank:
+            spec = wl.dataclasses.replace(spec, seed=spec.seed + 7919 * rank)
+        b = wl.make_decode_batch(spec, dev)
+        desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                             head_dim=spec.head_dim, num_blocks=b.k_cache.shape[0],
+                             max_blocks_per_seq=b.tables_host.shape[1])
+        if part == "verify":
+            rng = np.random.default_rng(spec.seed + 3)
+            lo, hi = wl.VERIFY_Q_LENS
+            ql = rng.integers(lo, hi + 1, size=spec.batch).astype(np.int32)
+            qo = np.zeros(spec.batch + 1, np.int32)
+            qo[1:] = np.cumsum(ql)
+            g = torch.Generator(device=dev).manual_seed(spec.seed + 3)
+            q = wl.fill_bf16((int(qo[-1]), spec.num_q_heads, spec.head_dim), g, dev)
+            qo_d = torch.from_numpy(qo).to(dev)
+            out = torch.empty_like(q)
+            run = lambda: pkv.pkv_prefill_attention_ragged(
+                desc, q, qo_d, b.k_cache, b.v_cache, b.block_tables, b.context_lens,
+                spec.sm_scale, out, qo_indptr_host=qo, kv_lens_host=b.lens_host)
+            times, clocks = _timed_launches(run, K, W, dev, flush)
+            ms = reduce_max(float(np.mean(times)), world)
+            if rank:
+                return
+            nbytes = b.kv_bytes()
+            gbs = nbytes / (ms / 1e3) / 1e9
+            _part_line(args, world, "speculative-verify attention (2-8 query tokens per sequence) "
+                       "KV GB/s", gbs * world, "GB/s", times, "bf16",
+                       {"workload": spec.name + ", q_len U[2,8] per sequence", "query_tokens":
+                        int(qo[-1])},
+                       {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(gbs / hbm, 4), "traffic": None,
+                        "kernel": "prefill_tc_kernel (one query tile holds every verify token)",
+                        "peak_source": "%s hbm_gbs" % hbm_kind,
+                        "algorithmic_bytes_per_launch": nbytes},
+                       1, clocks, {"query_tokens_per_s": round(int(qo[-1]) / (ms / 1e3), 1)})
+            return
+        # cow: 4096 (src, dst) pairs, dst blocks outside every table
+        used = set(b.tables_host[b.tables_host >= 0].tolist())
+        free = np.array([i for i in range(b.k_cache.shape[0]) if i not in used], np.int32)
+        rng = np.random.default_rng(spec.seed + 5)
+        npairs = 4096
+        src = rng.choice(np.array(sorted(used), np.int32), npairs, replace=False)
+        dst = rng.choice(free, npairs, replace=False)
+        src_d = torch.from_numpy(src.astype(np.int32)).to(dev)
+        dst_d = torch.from_numpy(dst.astype(np.int32)).to(dev)
+        run = lambda: pkv.pkv_copy_blocks(desc, b.k_cache, b.v_cache, src_d, dst_d)
+        times, clocks = _timed_launches(run, K, W, dev, flush)
+        ms = reduce_max(float(np.mean(times)), world)
+        if rank:
+            return
+        block_bytes = spec.num_kv_heads * spec.block_size * spec.head_dim * 2
+        nbytes = npairs * 2 * 2 * block_bytes  # K and V, read and written
+        gbs = nbytes / (ms / 1e3) / 1e9
+        _part_line(args, world, "copy-on-write block copy GB/s (read + write)", gbs * world, "GB/s",
+                   times, "bytes", {"workload": "4096 whole-block copies in the Qwen2.5-3B-shaped "
+                                                "pool (16 x 2 x 128 bf16 per block and pool)"},
+                   {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4), "traffic": None, "kernel": "copy_blocks_kernel",
+                    "peak_source": "%s hbm_gbs" % hbm_kind, "algorithmic_bytes_per_launch": nbytes},
+                   1, clocks)
+        return
+
+    if part == "ring":
+        spec = wl.FP8_DECODE
+        if rank:
+            spec = wl.dataclasses.replace(spec, seed=spec.seed + 7919 * rank)
+        R, window = wl.FP8_RING, wl.FP8_WINDOW
+        rng = np.random.default_rng(spec.seed + 11)
+        lens = wl.draw_lengths(spec, rng)
+        B = spec.batch
+        g = torch.Generator(device=dev).manual_seed(spec.seed + 11)
+        shape = (B * R, spec.num_kv_heads, spec.block_size, spec.head_dim)
+        kc, ks = wl.fill_e4m3(shape, g, dev)
+        vc, vs = wl.fill_e4m3(shape, g, dev)
+        perm = rng.permutation(B * R).astype(np.int32).reshape(B, R)
+        tabs = torch.from_numpy(perm).to(dev)
+        lens_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        q = wl.fill_bf16((B, spec.num_q_heads, spec.head_dim), g, dev)
+        kn = wl.fill_bf16((B, spec.num_kv_heads, spec.head_dim), g, dev)
+        vn = wl.fill_bf16((B, spec.num_kv_heads, spec.head_dim), g, dev)
+        sinks = torch.from_numpy(rng.uniform(-1.0, 3.0, spec.num_q_heads).astype(np.float32)).to(dev)
+        table = torch.from_numpy(pkv.pkv_rope_cos_sin_table(spec.rope_theta, spec.head_dim,
+                                                            spec.ctx_hi)).to(dev)
+        desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                             head_dim=spec.head_dim, num_blocks=B * R, max_blocks_per_seq=R,
+                             kv_dtype=pkv.KV_FP8_E4M3, ring_blocks=R)
+        max_ctx = int(lens.max())
+        ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, window, 0), 256),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        run = lambda: pkv.pkv_decode_step(desc, q, kn, vn, kc, vc, tabs, lens_d, max_ctx,
+                                          spec.sm_scale, out, None, ws, cos_sin=table,
+                                          window=window, k_scale=ks, v_scale=vs, sinks=sinks)
+        times, clocks = _timed_launches(run, K, W, dev, flush)
+        ms = reduce_max(float(np.mean(times)), world)
+        if rank:
+            return
+        nbytes = int(np.minimum(lens, window).astype(np.int64).sum()) * spec.num_kv_heads * \
+            spec.head_dim * 1 * 2
+        gbs = nbytes / (ms / 1e3) / 1e9
+        _part_line(args, world, "sliding-window (128) decode step over a 9-block ring cache with "
+                   "sink logits, KV GB/s", gbs * world, "GB/s", times, "e4m3 KV, bf16 q/o, fp32 "
+                   "accumulate", {"workload": "FP8 workload's window layer: B128, 64/8 heads, D64, "
+                                              "ctx U[1024,16384], ring of 9 blocks per sequence"},
+                   {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4), "traffic": None,
+                    "kernel": "decode_kernel (fused append, ring tables, sinks)",
+                    "peak_source": "%s hbm_gbs" % hbm_kind, "algorithmic_bytes_per_launch": nbytes},
+                   1, clocks)
+        return
+
+    # fp8-prefill: workload 4's prefill part with its pools quantised to e4m3
+    P = PrefillPart(dev, rank)
+    pb = P.pb
+    amax_k = pb.k_cache.float().abs().amax(dim=(0, 2, 3))
+    amax_v = pb.v_cache.float().abs().amax(dim=(0, 2, 3))
+    ks = (amax_k / 448.0).contiguous()
+    vs = (amax_v / 448.0).contiguous()
+    k8 = (pb.k_cache.float() / ks.view(1, -1, 1, 1)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (pb.v_cache.float() / vs.view(1, -1, 1, 1)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    spec = P.spec
+    desc8 = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                          head_dim=spec.head_dim, num_blocks=k8.shape[0],
+                          max_blocks_per_seq=pb.tables_host.shape[1], kv_dtype=pkv.KV_FP8_E4M3)
+    ws = torch.zeros(max(pkv.pkv_prefill_workspace_size(desc8, spec.num_chunks, P.tokens), 256),
+                     dtype=torch.uint8, device=dev)
+    run = lambda: pkv.pkv_prefill_attention_ragged(
+        desc8, pb.q, pb.qo_indptr, k8, v8, pb.block_tables, pb.kv_lens, spec.sm_scale, P.out,
+        qo_indptr_host=pb.qo_indptr_host, kv_lens_host=pb.kv_lens_host, workspace=ws,
+        k_scale=ks, v_scale=vs)
+    times, clocks = _timed_launches(run, K, W, dev, flush)
+    ms = reduce_max(float(np.mean(times)), world)
+    if rank:
+        return
+    peak, kind = measured_tensor_peak()
+    tflops = P.flops / (ms / 1e3) / 1e12
+    _part_line(args, world, "ragged causal chunked-prefill attention over an e4m3 cache TFLOP/s",
+               tflops * world, "TFLOP/s", times, "e4m3 KV staged to bf16, bf16 MMA, fp32 accumulate",
+               {"workload": spec.name + ", e4m3 pools with per-head scales", "q_tokens": P.tokens},
+               {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(tflops / peak, 4), "traffic": None,
+                "kernel": "stage_fp8_kernel + prefill_tc_kernel", "peak_source":
+                "%s bf16_tflops (burst)" % kind, "algorithmic_flops_per_launch": int(P.flops)},
+               2, clocks)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args.gpus)
@@ -621,6 +879,8 @@ def main():
         return main_reference(args, rank, world, local)
     if args.part == "prefill":
         return main_prefill(args, rank, world, local)
+    if args.part != "step":
+        return main_next(args, rank, world, local)
     r = time_pkv(args, rank, world, local)
     if rank != 0:
         return

@@ -77,6 +77,29 @@ class PrefillSpec:
         return 1.0 / math.sqrt(self.head_dim)
 
 
+@dataclasses.dataclass(frozen=True)
+class CascadeSpec:
+    """Groups of decode sequences sharing a block-aligned cached prefix (a
+    radix-cache hit), each with its own suffix."""
+
+    name: str
+    groups: int
+    group_size: int
+    prefix_lo: int
+    prefix_hi: int
+    suffix_lo: int
+    suffix_hi: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    seed: int
+    block_size: int = BLOCK_SIZE
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
 # The five workloads.  Names say what they are shaped like.
 TINY = DecodeSpec("tiny decode, 4 seqs, 8/2 heads, D64", batch=4, num_q_heads=8, num_kv_heads=2,
                   head_dim=64, ctx_lo=17, ctx_hi=255, seed=20261, pool_blocks=64,
@@ -97,6 +120,14 @@ FP8_DECODE = DecodeSpec("FP8 e4m3 decode, B128, 64/8 heads, D64, ctx 1024-16384"
                         batch=128, num_q_heads=64, num_kv_heads=8, head_dim=64, ctx_lo=1024,
                         ctx_hi=16384, seed=20265, kv_dtype="fp8_e4m3")
 FP8_WINDOW = 128  # the sliding-window layer of the FP8 workload
+FP8_RING = 9      # ring blocks that hold any 128-key window: ceil((128 - 1) / 16) + 1
+
+# Supplementary workloads of the next-step rows (not the headline).
+CASCADE_DECODE = CascadeSpec("shared-prefix decode: 16 groups x 8 sequences, prefix U[1024,8192] "
+                             "(block-aligned), suffix U[16,512], 32/8 heads, D128",
+                             groups=16, group_size=8, prefix_lo=1024, prefix_hi=8192, suffix_lo=16,
+                             suffix_hi=512, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=20266)
+VERIFY_Q_LENS = (2, 8)  # speculative-verify query tokens per sequence, uniform
 
 CONFIGS = {1: TINY, 2: QWEN25_3B, 3: QWEN3_4B, 4: LLAMA3_8B_DECODE, 5: FP8_DECODE}
 
@@ -356,3 +387,77 @@ def make_prefill_batch(spec: PrefillSpec, device="cpu", pool=None, free_blocks=N
                         qo_indptr=torch.from_numpy(qo).to(device),
                         kv_lens=torch.from_numpy(kv_lens).to(device), qo_indptr_host=qo,
                         kv_lens_host=kv_lens, tables_host=tables, prefix_host=prefixes)
+
+
+@dataclasses.dataclass
+class CascadeBatch:
+    spec: CascadeSpec
+    q: torch.Tensor                # bf16 [B][Hq][D]
+    k_cache: torch.Tensor          # bf16 [NB][Hkv][bs][D]
+    v_cache: torch.Tensor
+    group_indptr: torch.Tensor     # int32 [groups + 1]
+    prefix_tables: torch.Tensor    # int32 [groups][mbps]
+    prefix_lens: torch.Tensor      # int32 [groups]
+    suffix_tables: torch.Tensor    # int32 [B][mbps]
+    suffix_lens: torch.Tensor      # int32 [B]
+    concat_tables: torch.Tensor    # int32 [B][mbps]: prefix blocks then suffix blocks
+    concat_lens: torch.Tensor      # int32 [B]
+    group_indptr_host: np.ndarray
+    prefix_host: np.ndarray
+    suffix_host: np.ndarray
+
+    def cascade_kv_bytes(self) -> int:
+        """K+V bytes with each group's prefix read once."""
+        s = self.spec
+        toks = int(self.prefix_host.astype(np.int64).sum() + self.suffix_host.astype(np.int64).sum())
+        return toks * s.num_kv_heads * s.head_dim * 2 * 2
+
+    def uncached_kv_bytes(self) -> int:
+        """K+V bytes of plain decode over each sequence's whole context."""
+        s = self.spec
+        per_seq = np.repeat(self.prefix_host, s.group_size).astype(np.int64) + self.suffix_host
+        return int(per_seq.sum()) * s.num_kv_heads * s.head_dim * 2 * 2
+
+
+def make_cascade_batch(spec: CascadeSpec, device="cpu") -> CascadeBatch:
+    """Seeded shared-prefix batch: group g's prefix blocks are shared by its
+    sequences (one table row per group); each sequence's suffix has its own
+    blocks.  Prefixes are whole blocks, so the concatenated table of a
+    sequence is its prefix blocks followed by its suffix blocks."""
+    rng = np.random.default_rng(spec.seed)
+    gen = torch.Generator(device=device).manual_seed(spec.seed)
+    bs = spec.block_size
+    B = spec.groups * spec.group_size
+    prefix = (bs * rng.integers(spec.prefix_lo // bs, spec.prefix_hi // bs + 1,
+                                size=spec.groups)).astype(np.int32)
+    suffix = rng.integers(spec.suffix_lo, spec.suffix_hi + 1, size=B).astype(np.int32)
+    pblk = prefix // bs
+    sblk = blocks_for(suffix, bs)
+    need = int(pblk.sum() + sblk.sum())
+    nb = int(need * 1.25) + 16
+    shape = (nb, spec.num_kv_heads, bs, spec.head_dim)
+    k_cache = fill_bf16(shape, gen, device)
+    v_cache = fill_bf16(shape, gen, device)
+    ids = rng.permutation(nb).astype(np.int32)
+    mbps = int(pblk.max() + sblk.max())
+    ptab = np.full((spec.groups, mbps), -1, np.int32)
+    stab = np.full((B, mbps), -1, np.int32)
+    ctab = np.full((B, mbps), -1, np.int32)
+    off = 0
+    for g in range(spec.groups):
+        ptab[g, :pblk[g]] = ids[off:off + pblk[g]]
+        off += pblk[g]
+    for i in range(B):
+        g = i // spec.group_size
+        stab[i, :sblk[i]] = ids[off:off + sblk[i]]
+        off += sblk[i]
+        ctab[i, :pblk[g]] = ptab[g, :pblk[g]]
+        ctab[i, pblk[g]:pblk[g] + sblk[i]] = stab[i, :sblk[i]]
+    gptr = (spec.group_size * np.arange(spec.groups + 1)).astype(np.int32)
+    q = fill_bf16((B, spec.num_q_heads, spec.head_dim), gen, device)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return CascadeBatch(spec=spec, q=q, k_cache=k_cache, v_cache=v_cache, group_indptr=t(gptr),
+                        prefix_tables=t(ptab), prefix_lens=t(prefix), suffix_tables=t(stab),
+                        suffix_lens=t(suffix), concat_tables=t(ctab),
+                        concat_lens=t(np.repeat(prefix, spec.group_size) + suffix),
+                        group_indptr_host=gptr, prefix_host=prefix, suffix_host=suffix)
