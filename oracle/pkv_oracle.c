@@ -400,7 +400,9 @@ static void *attn_worker(void *arg) {
     attn_job *J = (attn_job *)arg;
     int32_t max_len = 0;
     for (int32_t s = 0; s < J->num_seqs; ++s) if (J->kv_lens[s] > max_len) max_len = J->kv_lens[s];
-    if (J->window > 0 && J->window < max_len) max_len = J->window;
+    /* a causal window holds at most W keys; without causality a query's
+     * range [p - W + 1, kv_len) can be longer, so only causal windows cap it */
+    if (J->causal && J->window > 0 && J->window < max_len) max_len = J->window;
     size_t n = (size_t)(max_len > 0 ? max_len : 1);
     if (J->precision == 64) {
         double *logit = (double *)malloc(sizeof(double) * n);

@@ -399,12 +399,15 @@ def test_prefill_causal_matches_sdpa_is_causal():
     assert np.abs(out - ref.permute(1, 0, 2).numpy()).max() < 2e-6
 
 
-@pytest.mark.parametrize("window", [-1, 128, 7])
-def test_ragged_prefill_over_prefix_matches_dense(window):
+@pytest.mark.parametrize("causal,window", [(True, -1), (True, 128), (True, 7), (False, 7),
+                                           (False, 128)])
+def test_ragged_prefill_over_prefix_matches_dense(causal, window):
+    """Without causality a windowed query sees [p - W + 1, kv_len): more than
+    W keys, the case that sizes the oracle's per-worker logit buffer."""
     rng = np.random.default_rng(19)
     case = PagedCase(rng, [200, 37, 64, 300], 8, 2, 64, q_lens=[50, 37, 1, 16])
-    out, lse = _run(case, 0.125, window=window)
-    ref, ref_lse = dense_reference(case, 0.125, window=window)
+    out, lse = _run(case, 0.125, causal=causal, window=window)
+    ref, ref_lse = dense_reference(case, 0.125, causal=causal, window=window)
     assert np.abs(out - ref).max() < 2e-6
     assert np.abs(lse - ref_lse).max() < 2e-5
 
