@@ -296,6 +296,28 @@ pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, in
     return PKV_OK;
 }
 
+// The short-query kernel's plan: chunk length in blocks and chunks per
+// (sequence, KV head), at most kSqMaxSplits (one cluster).  Like the decode
+// planner it aims at one wave of resident CTAs.  False when the longest KV
+// range does not fit kSqMaxSplits chunks.
+bool plan_short_query(const pkv_cache_desc* desc, int num_seqs, int max_kv, int max_q, int window,
+                      int num_sms, int* chunk_out, int* splits_out) {
+    int mb = std::max(1, (max_kv + 15) / 16);
+    if (window > 0) mb = std::min(mb, (window + max_q + 14) / 16 + 1);
+    if (mb > pkv::kSqMaxSplits * pkv::kSqMaxChunk) return false;
+    const double pairs = double(num_seqs) * desc->num_kv_heads;
+    const int per_sm = std::max(1, std::min(3, (228 * 1024) / (pkv::short_query_smem_bytes(desc->head_dim) + 1024)));
+    const double slots = double(std::max(num_sms, 1)) * per_sm;
+    const double target = std::max(slots - 0.5 * pairs, 0.25 * slots);
+    int chunk = int(std::ceil(pairs * std::max(1.0, 0.55 * mb) / target));
+    chunk = std::max(16, std::min(pkv::kSqMaxChunk, chunk));
+    if (chunk > mb) chunk = mb;
+    if ((mb + chunk - 1) / chunk > pkv::kSqMaxSplits) chunk = (mb + pkv::kSqMaxSplits - 1) / pkv::kSqMaxSplits;
+    *chunk_out = chunk;
+    *splits_out = (mb + chunk - 1) / chunk;
+    return true;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct DecodeWs {
@@ -652,6 +674,18 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     st = pool_map(vpool, &staged, &vmap);
     if (st != PKV_OK) return st;
     pkv::PrefillArgs a{};
+    // at most 64 query rows (tokens x heads of a group) per sequence: the
+    // decode-shaped short-query kernel (needs the host query lengths)
+    int sq_chunk = 0, sq_splits = 0;
+    int kv_bound = desc->max_blocks_per_seq * desc->block_size;
+    if (kv_lens_host) {
+        kv_bound = 0;
+        for (int s2 = 0; s2 < num_seqs; ++s2) kv_bound = std::max(kv_bound, kv_lens_host[s2]);
+    }
+    int sms = 0;
+    const bool short_q = qo_indptr_host && max_q * G <= pkv::kSqMaxRowTiles * 16 &&
+                         device_state(nullptr, &sms) == PKV_OK &&
+                         plan_short_query(desc, num_seqs, kv_bound, max_q, window, sms, &sq_chunk, &sq_splits);
     a.k_scale = fp8 ? k_scale : nullptr;
     a.v_scale = fp8 ? v_scale : nullptr;
     a.q = q;
@@ -686,6 +720,19 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
         std::stable_sort(work.begin(), work.end());
         for (int i = 0; i < num_seqs; ++i) a.seq_order[i] = static_cast<uint16_t>(work[static_cast<size_t>(i)].second);
         a.ordered = 1;
+    }
+    if (short_q) {
+        CUtensorMap tkmap, tvmap;
+        st = pool_map(kpool, &staged, &tkmap, kMapTileRows);
+        if (st != PKV_OK) return st;
+        st = pool_map(vpool, &staged, &tvmap, kMapTileRows);
+        if (st != PKV_OK) return st;
+        a.sq_chunk = sq_chunk;
+        a.sq_splits = sq_splits;
+        a.sq_row_tiles = (max_q * G + 15) / 16;
+        cudaError_t e = pkv::launch_short_query(a, tkmap, tvmap, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "short-query launch");
+        return PKV_OK;
     }
     CUtensorMap qmap;
     st = q_map(q, total_q_tokens, desc, G, QT, &qmap);
@@ -939,7 +986,23 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.total_q = num_seqs;
         a.num_blocks = desc->num_blocks;
         a.sm_scale = sm_scale;
-        if (a.max_qtiles > 0) {
+        int max_prefix = 0;
+        for (int g = 0; g < num_groups; ++g) max_prefix = std::max(max_prefix, prefix_lens_host[g]);
+        int sq_chunk = 0, sq_splits = 0;
+        if (a.max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
+            plan_short_query(desc, num_groups, max_prefix, max_group, -1, sms, &sq_chunk, &sq_splits)) {
+            // a group's queries (at most 64 rows) over its prefix: short-query kernel
+            CUtensorMap tkmap, tvmap;
+            st = pool_map(k_cache, desc, &tkmap, kMapTileRows);
+            if (st != PKV_OK) return st;
+            st = pool_map(v_cache, desc, &tvmap, kMapTileRows);
+            if (st != PKV_OK) return st;
+            a.sq_chunk = sq_chunk;
+            a.sq_splits = sq_splits;
+            a.sq_row_tiles = (max_group * G + 15) / 16;
+            cudaError_t e = pkv::launch_short_query(a, tkmap, tvmap, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
+        } else if (a.max_qtiles > 0) {
             cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
         }

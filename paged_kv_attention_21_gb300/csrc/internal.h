@@ -130,7 +130,19 @@ struct PrefillArgs {
     // order of decreasing work, so the heaviest CTAs are dispatched first
     int32_t ordered;
     uint16_t seq_order[kPrefillOrderMax];
+    // short-query kernel (short_query.cu): blocks per chunk, chunks per
+    // (sequence, KV head) (<= kSqMaxSplits; > 1 launches clusters) and m16
+    // row tiles per CTA (rows = q_len * group <= 16 * this)
+    int32_t sq_chunk, sq_splits, sq_row_tiles;
 };
+constexpr int kSqMaxRowTiles = 4;   // 64 query rows (tokens x heads of a KV group)
+constexpr int kSqMaxSplits = 4;     // chunks per (sequence, KV head): one cluster
+constexpr int kSqMaxChunk = 512;    // blocks per chunk (their ids sit in shared memory)
+int short_query_smem_bytes(int d);
+// Ragged attention of at most 64 query rows per (sequence, KV head) over bf16
+// pools; tensor maps as for decode (one 5-D box per (block, head) tile).
+cudaError_t launch_short_query(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t stream);
 // Query tokens per CTA tile for a group size (rows = tokens * group <= 128).
 int prefill_tc_q_tile(int group);
 // qmap: 3-D tiled view of q [total_q][Hq][D], box {64, G, q_tile}, 128-byte swizzle.

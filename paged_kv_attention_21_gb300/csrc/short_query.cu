@@ -1,0 +1,468 @@
+// short_query.cu -- attention of a few query tokens per sequence over the
+// paged cache: speculative verify (q_len 2-8 tokens; infer-lab, "Technique"
+// table: speculative decoding) and the queries of a group over its shared
+// prefix (cascade decode; infer-lab, "Technique" table: prefix caching).
+//
+// What it computes is the ragged attention of prefill_tc.cu: query token i of
+// a sequence with q_len queries and kv_len keys sits at position
+// kv_len - q_len + i and sees keys t < kv_len, t <= that position when
+// causal, and t > position - window with a window; o = softmax(sm_scale q K^T) V.
+//
+// Why a second kernel: a 128-row tcgen05 tile holds at most 64 useful rows
+// here (q_len x G), so the tensor-core prefill spends its per-tile cost on
+// padding and runs near a third of HBM speed.  This kernel is decode-shaped:
+// rows = (query token, head of the KV group) pairs, at most 64, in m16 tiles;
+// warp w of a CTA owns row tile w for every block of the chunk, and the
+// CTA's warps share one ring of (K, V) block tiles loaded by TMA (the last
+// warp to be done with a stage refills it).  A sequence's KV range is cut
+// into at most 4 chunks; 2-4 chunks launch as a thread-block cluster and
+// merge through distributed shared memory, so no workspace is needed.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kSqStages = 8;  // shared ring of (K, V) block tiles
+
+template <int D>
+struct SqCfg {
+    static constexpr int kTileBytes = kBlockSize * D * 2;  // one bf16 (block, head) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRingBytes = kSqStages * kStageBytes;
+    static constexpr int kStateStride = D + 8;  // fp32 row stride of the merge state
+    static constexpr int kStateFloats = kSqMaxRowTiles * 16 * kStateStride;
+    static constexpr int kMergeFloats = kStateFloats + kSqMaxSplits * kSqMaxRowTiles * 16 + 2 * 64;
+    static constexpr int kBodyBytes =
+        kRingBytes > kMergeFloats * 4 ? kRingBytes : kMergeFloats * 4;
+    static constexpr int kSmemBytes = kBodyBytes + 1024;  // + alignment slack
+};
+
+// Byte offset of 16-byte chunk `chunk` of row r of a 16 x D bf16 tile as the
+// 128-byte-swizzled 5-D TMA box writes it (row r's D/64 slices side by side,
+// unit u = r D/64 + chunk / 8, chunks swizzled by u % 8).
+template <int D>
+__device__ __forceinline__ uint32_t sq_off(int r, int chunk) {
+    const int u = r * (D / 64) + (chunk >> 3);
+    return static_cast<uint32_t>(u * 128 + (((chunk & 7) ^ (u & 7)) << 4));
+}
+
+template <int D, int kMT, bool kCluster>
+__global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs a,
+                                                               const __grid_constant__ CUtensorMap kmap,
+                                                               const __grid_constant__ CUtensorMap vmap) {
+    using C = SqCfg<D>;
+    constexpr int KSTEPS = D / 16;
+    constexpr int NTILES = D / 8;
+    constexpr int kThreads = kMT * 32;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t full[kSqStages];
+    __shared__ uint32_t released[kSqStages];
+    __shared__ int32_t s_ids[kSqMaxChunk];
+    __shared__ float s_lse[kSqMaxRowTiles * 16];
+    __shared__ int s_flag;
+    __shared__ int s_issued;
+
+    pdl_wait();
+    pdl_launch_dependents();
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int seq = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+
+    const int q0 = a.qo_indptr[seq];
+    const int q_len = a.qo_indptr[seq + 1] - q0;
+    if (q_len <= 0) return;
+    int kv_len = a.kv_lens[seq];
+    const int rows = q_len * G;
+    const int cap = a.mbps * kBlockSize;
+    if (q0 < 0 || q0 + q_len > a.total_q || rows > kMT * 16 || (a.causal && kv_len < q_len)) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) flag_error(a.err, PKV_DEVERR_POSITION);
+        return;
+    }
+    if (kv_len > cap) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+        kv_len = cap;
+    }
+    // query i sits at position off + i; the keys any row may see: [klo, kv_len)
+    const int off = kv_len - q_len;
+    const int klo = (a.window > 0) ? max(0, off - a.window + 1) : 0;
+    if (kv_len <= 0 || klo >= kv_len) {  // no visible key: o = 0, lse = -inf
+        if (split == 0) {
+            for (int i = threadIdx.x; i < rows * D; i += kThreads) {
+                const int r = i / D;
+                const size_t orow = static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G;
+                if (a.out_f32)
+                    a.out_f32[orow * D + i % D] = 0.f;
+                else
+                    static_cast<__nv_bfloat16*>(a.out)[orow * D + i % D] = __float2bfloat16_rn(0.f);
+                if (a.lse_out && i % D == 0) a.lse_out[orow] = -INFINITY;
+            }
+        }
+        return;
+    }
+    const int first_blk = klo / kBlockSize;
+    const int last_blk = (kv_len - 1) / kBlockSize;
+    int nsplit = (last_blk - first_blk + a.sq_chunk) / a.sq_chunk;
+    if (nsplit > a.sq_splits) {  // lengths beyond the host's plan: flagged, never a rank past the cluster
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+        nsplit = a.sq_splits;
+    }
+    if (split >= nsplit) return;
+    const int b0 = first_blk + split * a.sq_chunk;
+    const int nb = min(last_blk + 1, b0 + a.sq_chunk) - b0;
+
+    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
+        int id = bt[b0 + i];
+        if (id < 0 || id >= a.num_blocks) {
+            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+            id = 0;  // read a valid block; the output is flagged invalid
+        }
+        s_ids[i] = id;
+    }
+    if (threadIdx.x < kSqStages) {
+        mbar_init(&full[threadIdx.x], 1);
+        released[threadIdx.x] = 0u;
+    }
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        s_flag = 0;
+        s_issued = 0;
+    }
+    fence_barrier_init();
+    __syncthreads();
+
+    auto issue = [&](int k) {  // block k of the chunk into its stage (one thread)
+        const int st = k % kSqStages;
+        uint8_t* dst = smem + st * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+        tma_load_5d(dst, &kmap, &full[st], 0, 0, 0, kvh, s_ids[k]);
+        tma_load_5d(dst + C::kTileBytes, &vmap, &full[st], 0, 0, 0, kvh, s_ids[k]);
+        s_issued = k + 1;
+    };
+    if (threadIdx.x == 0)
+        for (int k = 0; k < min(kSqStages, nb); ++k) issue(k);
+
+    // this warp's rows: r = 16 warp + g0 (+ 8); row r is query r / G, head r % G
+    const int g0 = lane >> 2;
+    const int tig = lane & 3;
+    int hi_r[2], lo_r[2];
+    uint32_t qa[KSTEPS][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int r = warp * 16 + g0 + 8 * h;
+        const int pos = off + r / G;  // the window is relative to the query's position
+        hi_r[h] = r < rows ? (a.causal ? pos : kv_len - 1) : -1;  // padding rows see no key
+        lo_r[h] = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+    }
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            const int r = warp * 16 + g0 + ((part & 1) ? 8 : 0);
+            const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
+            uint32_t v = 0;
+            if (r < rows) {
+                const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
+                                            (static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G) * D;
+                v = *reinterpret_cast<const uint32_t*>(qrow + col);
+            }
+            qa[kk][part] = v;
+        }
+    }
+    const float scale_log2 = a.sm_scale * 1.4426950408889634f * (a.k_scale ? a.k_scale[kvh] : 1.f);
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float o[NTILES][4];
+#pragma unroll
+    for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    // the last of the kMT warps to be done with stage st refills it
+    auto release = [&](int st, int k) {
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const uint32_t before = atomicAdd(&released[st], 1u);
+            if (before == kMT - 1) {
+                released[st] = 0u;
+                __threadfence_block();
+                const int kn = k + kSqStages;
+                if (kn < nb) {
+                    fence_proxy_async_smem();
+                    issue(kn);
+                }
+            }
+        }
+    };
+
+    // A warp whose 16 rows are all padding only keeps the ring moving.
+    const bool active = warp * 16 < rows;
+    bool failed = false;
+    int k = 0;
+    for (; k < nb; ++k) {
+        const int st = k % kSqStages;
+        const uint32_t ph = (k / kSqStages) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], ph))) {
+            failed = true;
+            break;
+        }
+        if (!active) {
+            release(st, k);
+            continue;
+        }
+        const uint32_t kaddr = smem_u32(smem + st * C::kStageBytes);
+        const uint32_t vaddr = kaddr + C::kTileBytes;
+        const int tok_base = (b0 + k) * kBlockSize;
+
+        // ---- S = Q . K^T  (16 rows x 16 tokens)
+        float sacc[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+        {
+            const int tok = (lane & 7) + ((lane >> 4) << 3);
+            const int csel = (lane >> 3) & 1;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                uint32_t b00, b01, b10, b11;
+                ldmatrix_x4(b00, b01, b10, b11, kaddr + sq_off<D>(tok, 2 * kk + csel));
+                mma_16816<false>(sacc[0], qa[kk], b00, b01);
+                mma_16816<false>(sacc[1], qa[kk], b10, b11);
+            }
+        }
+        // ---- per-row mask + online softmax (exp2 domain)
+        float x[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = e >> 1;
+                const int t = tok_base + n * 8 + 2 * tig + (e & 1);
+                x[n][e] = (t < lo_r[h] || t > hi_r[h]) ? -INFINITY : sacc[n][e] * scale_log2;
+            }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+        const float mn0 = fmaxf(m_run[0], mx0);
+        const float mn1 = fmaxf(m_run[1], mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m_run[0] - mu0);
+        const float al1 = fast_exp2(m_run[1] - mu1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            p[n][0] = fast_exp2(x[n][0] - mu0);
+            p[n][1] = fast_exp2(x[n][1] - mu0);
+            p[n][2] = fast_exp2(x[n][2] - mu1);
+            p[n][3] = fast_exp2(x[n][3] - mu1);
+        }
+        l_run[0] = l_run[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        l_run[1] = l_run[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int nt = 0; nt < NTILES; ++nt) {
+                o[nt][0] *= al0;
+                o[nt][1] *= al0;
+                o[nt][2] *= al1;
+                o[nt][3] *= al1;
+            }
+        }
+        uint32_t pa[4];
+        pa[0] = pack2<false>(p[0][0], p[0][1]);
+        pa[1] = pack2<false>(p[0][2], p[0][3]);
+        pa[2] = pack2<false>(p[1][0], p[1][1]);
+        pa[3] = pack2<false>(p[1][2], p[1][3]);
+        // ---- O += P . V, V rows outside [klo, kv_len) zeroed (0 * NaN never
+        // reaches the MMA)
+        uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
+        if (tok_base < klo || tok_base + kBlockSize > kv_len) {
+            const int t0 = tok_base + 2 * tig;
+            const bool v0 = t0 >= klo && t0 < kv_len, v1 = t0 + 1 >= klo && t0 + 1 < kv_len;
+            const bool v8 = t0 + 8 >= klo && t0 + 8 < kv_len, v9 = t0 + 9 >= klo && t0 + 9 < kv_len;
+            keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
+            keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
+        }
+        {
+            const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int csel = lane >> 4;
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(v0, v1, v2, v3, vaddr + sq_off<D>(tok, 2 * j + csel));
+                v0 &= keep_lo;
+                v2 &= keep_lo;
+                v1 &= keep_hi;
+                v3 &= keep_hi;
+                mma_16816<false>(o[2 * j], pa, v0, v1);
+                mma_16816<false>(o[2 * j + 1], pa, v2, v3);
+            }
+        }
+        release(st, k);
+    }
+    if (failed) {
+        // wait (bounded) for the loads still in flight, then report
+        const int issued = *reinterpret_cast<volatile int*>(&s_issued);
+        for (int kk = k; kk < issued; ++kk) (void)mbar_wait(&full[kk % kSqStages], (kk / kSqStages) & 1);
+        if (lane == 0) {
+            flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            atomicOr(&s_flag, 1);
+        }
+    }
+    __syncthreads();  // the ring is drained: its bytes take the merge state
+    const bool cta_failed = s_flag != 0;
+    float* state = reinterpret_cast<float*>(smem);  // [row][kStateStride]
+
+    // ---- this chunk's state per row: o / l and lse
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float L = l_run[h];
+        L += __shfl_xor_sync(0xFFFFFFFFu, L, 1);
+        L += __shfl_xor_sync(0xFFFFFFFFu, L, 2);
+        const int r = warp * 16 + g0 + 8 * h;
+        const float inv = L > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / L : 0.f;
+        const float lse = L > 0.f && !cta_failed ? (m_run[h] + __log2f(L)) * 0.6931471805599453f : -INFINITY;
+        if (nsplit == 1) {
+            if (r >= rows || cta_failed) continue;
+            const size_t orow = static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G;
+#pragma unroll
+            for (int nt = 0; nt < NTILES; ++nt) {
+                const int col = nt * 8 + 2 * tig;
+                const float v0 = o[nt][2 * h] * inv, v1 = o[nt][2 * h + 1] * inv;
+                if (a.out_f32)
+                    *reinterpret_cast<float2*>(a.out_f32 + orow * D + col) = make_float2(v0, v1);
+                else
+                    *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + col) =
+                        pack2<false>(v0, v1);
+            }
+            if (a.lse_out && tig == 0) a.lse_out[orow] = lse;
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NTILES; ++nt) {
+                const int col = nt * 8 + 2 * tig;
+                *reinterpret_cast<float2*>(state + r * C::kStateStride + col) =
+                    make_float2(o[nt][2 * h] * inv, o[nt][2 * h + 1] * inv);
+            }
+            if (tig == 0) s_lse[r] = lse;
+        }
+    }
+    if constexpr (kCluster) {
+        if (nsplit == 1) return;
+        // ---- cluster merge: chunk c holds rows' o_c (state) and lse_c (s_lse)
+        cluster_sync();
+        float* wts = state + C::kStateFloats;            // [chunk][row]
+        float* rowM = wts + kSqMaxSplits * kSqMaxRowTiles * 16;
+        float* rowW = rowM + 64;
+        for (int r = threadIdx.x; r < kMT * 16; r += kThreads) {
+            float l[kSqMaxSplits];
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kSqMaxSplits; ++c) {
+                l[c] = c < nsplit ? ld_cluster_f32(cluster_map(smem_u32(&s_lse[r]), c)) : -INFINITY;
+                M = fmaxf(M, l[c]);
+            }
+            float W = 0.f;
+#pragma unroll
+            for (int c = 0; c < kSqMaxSplits; ++c) {
+                const float wv = l[c] == -INFINITY ? 0.f : __expf(l[c] - M);
+                wts[c * 64 + r] = wv;
+                W += wv;
+            }
+            rowM[r] = M;
+            rowW[r] = W;
+        }
+        __syncthreads();
+        constexpr int kSlotsPerRow = D / 4;
+        const int total = rows * kSlotsPerRow;
+        const int s_lo = split * total / nsplit;
+        const int s_hi = (split + 1) * total / nsplit;
+        for (int slot = s_lo + threadIdx.x; slot < s_hi; slot += kThreads) {
+            const int r = slot / kSlotsPerRow;
+            const int c4 = slot % kSlotsPerRow;
+            const uint32_t local = smem_u32(state + r * C::kStateStride + c4 * 4);
+            float4 v[kSqMaxSplits];
+#pragma unroll
+            for (int c = 0; c < kSqMaxSplits; ++c)
+                if (c < nsplit) v[c] = ld_cluster_f32x4(cluster_map(local, c));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < kSqMaxSplits; ++c) {
+                const float w = wts[c * 64 + r];
+                if (c < nsplit && w != 0.f) {
+                    acc.x += w * v[c].x;
+                    acc.y += w * v[c].y;
+                    acc.z += w * v[c].z;
+                    acc.w += w * v[c].w;
+                }
+            }
+            const float W = rowW[r];
+            const float inv = W > 0.f ? 1.f / W : 0.f;
+            const size_t orow = static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G;
+            if (a.out_f32) {
+                *reinterpret_cast<float4*>(a.out_f32 + orow * D + c4 * 4) =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            } else {
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + c4 * 4) =
+                    make_uint2(pack2<false>(acc.x * inv, acc.y * inv), pack2<false>(acc.z * inv, acc.w * inv));
+            }
+            if (a.lse_out && c4 == 0) a.lse_out[orow] = W > 0.f ? rowM[r] + __logf(W) : -INFINITY;
+        }
+        cluster_sync();  // no chunk exits while a peer may still read its shared memory
+    }
+}
+
+template <int D, int kMT>
+cudaError_t launch_sq_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        cudaStream_t stream) {
+    using C = SqCfg<D>;
+    static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+    const bool cluster = a.sq_splits > 1;
+    auto kern = cluster ? short_query_kernel<D, kMT, true> : short_query_kernel<D, kMT, false>;
+    static bool attr_set[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[cluster][dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[cluster][dev] = true;
+    }
+    dim3 grid(a.sq_splits, a.hkv, a.num_seqs);
+    return launch_pdl_cluster(kern, grid, dim3(kMT * 32), C::kSmemBytes, stream,
+                              cluster ? static_cast<unsigned>(a.sq_splits) : 1u, a, kmap, vmap);
+}
+
+template <int D>
+cudaError_t launch_sq_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        cudaStream_t stream) {
+    switch (a.sq_row_tiles) {
+        case 1: return launch_sq_t<D, 1>(a, kmap, vmap, stream);
+        case 2: return launch_sq_t<D, 2>(a, kmap, vmap, stream);
+        case 3: return launch_sq_t<D, 3>(a, kmap, vmap, stream);
+        default: return launch_sq_t<D, 4>(a, kmap, vmap, stream);
+    }
+}
+
+}  // namespace
+
+int short_query_smem_bytes(int d) { return d == 64 ? SqCfg<64>::kSmemBytes : SqCfg<128>::kSmemBytes; }
+
+cudaError_t launch_short_query(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t stream) {
+    return a.d == 64 ? launch_sq_d<64>(a, kmap, vmap, stream) : launch_sq_d<128>(a, kmap, vmap, stream);
+}
+
+}  // namespace pkv
