@@ -237,7 +237,14 @@ pkv_status pkv_decode_plan(const pkv_cache_desc *desc, int32_t num_seqs,
  *   q, out   : bf16 [total_q_tokens][Hq][D].  lse_out: fp32, nullable.
  *   qo_indptr: int32 [num_seqs + 1] (device).  kv_lens: int32 [num_seqs].
  *   qo_indptr_host, kv_lens_host: host copies (nullable, used for planning
- *              and validation only; they must match the device arrays).
+ *              and validation only; they must match the device arrays).  With
+ *              qo_indptr_host, a batch whose every sequence has at most 64
+ *              query rows (q_len * Hq / Hkv: speculative verify, infer-lab
+ *              "Technique" table) runs a decode-shaped kernel (mma.sync rows,
+ *              KV cut into <= 4 chunks merged in a thread-block cluster);
+ *              larger ones run the tcgen05 prefill.  kv_lens_host, when given,
+ *              sizes that plan and orders the tcgen05 launch by work; without
+ *              it the plan assumes full tables.
  *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL): k = code * k_scale[h],
  *              v = code * v_scale[h] (InferX, "The kernels underneath": FP8 KV cache).
  *   workspace: >= pkv_prefill_workspace_size(...) bytes, 256-byte aligned; 0
