@@ -137,8 +137,7 @@ struct PrefillArgs {
 };
 constexpr int kSqMaxRowTiles = 4;   // 64 query rows (tokens x heads of a KV group)
 constexpr int kSqMaxSplits = 4;     // chunks per (sequence, KV head): one cluster
-constexpr int kSqMaxChunk = 512;    // blocks per chunk (their ids sit in shared memory)
-int short_query_smem_bytes(int d);
+constexpr int kSqMaxChunk = 512;    // blocks per chunk (a warp's ids: 4 per lane)
 // Ragged attention of at most 64 query rows per (sequence, KV head) over bf16
 // pools; tensor maps as for decode (one 5-D box per (block, head) tile).
 cudaError_t launch_short_query(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

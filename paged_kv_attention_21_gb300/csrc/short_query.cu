@@ -11,12 +11,13 @@
 // Why a second kernel: a 128-row tcgen05 tile holds at most 64 useful rows
 // here (q_len x G), so the tensor-core prefill spends its per-tile cost on
 // padding and runs near a third of HBM speed.  This kernel is decode-shaped:
-// rows = (query token, head of the KV group) pairs, at most 64, in m16 tiles;
-// warp w of a CTA owns row tile w for every block of the chunk, and the
-// CTA's warps share one ring of (K, V) block tiles loaded by TMA (the last
-// warp to be done with a stage refills it).  A sequence's KV range is cut
-// into at most 4 chunks; 2-4 chunks launch as a thread-block cluster and
-// merge through distributed shared memory, so no workspace is needed.
+// the rows (query token, head of the KV group), at most 64, are cut into
+// m16 tiles and a CTA owns one tile of one chunk of the KV range; its 4 warps
+// take the chunk's blocks round-robin, each with its own 2-stage TMA ring,
+// and combine in shared memory.  The row tiles of a sequence run side by
+// side and read the same blocks, mostly from L2.  A KV range is cut into at
+// most 4 chunks; 2-4 chunks launch as a thread-block cluster and merge
+// through distributed shared memory, so no workspace is needed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,18 +25,18 @@ namespace pkv {
 
 namespace {
 
-constexpr int kSqStages = 8;  // shared ring of (K, V) block tiles
+constexpr int kSqWarps = 4;
+constexpr int kSqThreads = kSqWarps * 32;
+constexpr int kSqStages = 2;  // per-warp ring of (K, V) block tiles
 
 template <int D>
 struct SqCfg {
     static constexpr int kTileBytes = kBlockSize * D * 2;  // one bf16 (block, head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRingBytes = kSqStages * kStageBytes;
-    static constexpr int kStateStride = D + 8;  // fp32 row stride of the merge state
-    static constexpr int kStateFloats = kSqMaxRowTiles * 16 * kStateStride;
-    static constexpr int kMergeFloats = kStateFloats + kSqMaxSplits * kSqMaxRowTiles * 16 + 2 * 64;
-    static constexpr int kBodyBytes =
-        kRingBytes > kMergeFloats * 4 ? kRingBytes : kMergeFloats * 4;
+    static constexpr int kWarpBytes = kSqStages * kStageBytes;
+    static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
+    static constexpr int kCombBytes = kSqWarps * 16 * kCombStride * 4;
+    static constexpr int kBodyBytes = kSqWarps * kWarpBytes > kCombBytes ? kSqWarps * kWarpBytes : kCombBytes;
     static constexpr int kSmemBytes = kBodyBytes + 1024;  // + alignment slack
 };
 
@@ -48,28 +49,28 @@ __device__ __forceinline__ uint32_t sq_off(int r, int chunk) {
     return static_cast<uint32_t>(u * 128 + (((chunk & 7) ^ (u & 7)) << 4));
 }
 
-template <int D, int kMT, bool kCluster>
-__global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs a,
-                                                               const __grid_constant__ CUtensorMap kmap,
-                                                               const __grid_constant__ CUtensorMap vmap) {
+// One CTA = (chunk, KV head and 16-row tile, sequence).  Rows of tile t are
+// R = 16 t + r -> query token R / G, head R % G of the KV group.
+template <int D, bool kCluster>
+__global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillArgs a,
+                                                                 const __grid_constant__ CUtensorMap kmap,
+                                                                 const __grid_constant__ CUtensorMap vmap) {
     using C = SqCfg<D>;
     constexpr int KSTEPS = D / 16;
     constexpr int NTILES = D / 8;
-    constexpr int kThreads = kMT * 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t full[kSqStages];
-    __shared__ uint32_t released[kSqStages];
-    __shared__ int32_t s_ids[kSqMaxChunk];
-    __shared__ float s_lse[kSqMaxRowTiles * 16];
+    __shared__ __align__(8) uint64_t bars[kSqWarps][kSqStages];
+    __shared__ float s_m[kSqWarps][16];
+    __shared__ float s_l[kSqWarps][16];
     __shared__ int s_flag;
-    __shared__ int s_issued;
 
     pdl_wait();
     pdl_launch_dependents();
     const int split = blockIdx.x;
-    const int kvh = blockIdx.y;
+    const int kvh = blockIdx.y / a.sq_row_tiles;
+    const int tile = blockIdx.y % a.sq_row_tiles;
     const int seq = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -77,26 +78,27 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
 
     const int q0 = a.qo_indptr[seq];
     const int q_len = a.qo_indptr[seq + 1] - q0;
-    if (q_len <= 0) return;
-    int kv_len = a.kv_lens[seq];
     const int rows = q_len * G;
+    if (q_len <= 0 || 16 * tile >= rows) return;  // no rows in this tile
+    int kv_len = a.kv_lens[seq];
     const int cap = a.mbps * kBlockSize;
-    if (q0 < 0 || q0 + q_len > a.total_q || rows > kMT * 16 || (a.causal && kv_len < q_len)) {
-        if (threadIdx.x == 0 && split == 0 && kvh == 0) flag_error(a.err, PKV_DEVERR_POSITION);
+    if (q0 < 0 || q0 + q_len > a.total_q || rows > 16 * a.sq_row_tiles || (a.causal && kv_len < q_len)) {
+        if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag_error(a.err, PKV_DEVERR_POSITION);
         return;
     }
     if (kv_len > cap) {
-        if (threadIdx.x == 0 && split == 0 && kvh == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+        if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
         kv_len = cap;
     }
+    const int trows = min(16, rows - 16 * tile);  // valid rows of this tile
     // query i sits at position off + i; the keys any row may see: [klo, kv_len)
     const int off = kv_len - q_len;
     const int klo = (a.window > 0) ? max(0, off - a.window + 1) : 0;
     if (kv_len <= 0 || klo >= kv_len) {  // no visible key: o = 0, lse = -inf
         if (split == 0) {
-            for (int i = threadIdx.x; i < rows * D; i += kThreads) {
-                const int r = i / D;
-                const size_t orow = static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G;
+            for (int i = threadIdx.x; i < trows * D; i += kSqThreads) {
+                const int R = 16 * tile + i / D;
+                const size_t orow = static_cast<size_t>(q0 + R / G) * a.hq + kvh * G + R % G;
                 if (a.out_f32)
                     a.out_f32[orow * D + i % D] = 0.f;
                 else
@@ -110,68 +112,79 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
     const int last_blk = (kv_len - 1) / kBlockSize;
     int nsplit = (last_blk - first_blk + a.sq_chunk) / a.sq_chunk;
     if (nsplit > a.sq_splits) {  // lengths beyond the host's plan: flagged, never a rank past the cluster
-        if (threadIdx.x == 0 && split == 0 && kvh == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+        if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
         nsplit = a.sq_splits;
     }
     if (split >= nsplit) return;
     const int b0 = first_blk + split * a.sq_chunk;
-    const int nb = min(last_blk + 1, b0 + a.sq_chunk) - b0;
+    const int b1 = min(last_blk + 1, b0 + a.sq_chunk);
+    const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kSqWarps - 1) / kSqWarps : 0;  // <= 128
 
-    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
-        int id = bt[b0 + i];
-        if (id < 0 || id >= a.num_blocks) {
-            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;  // read a valid block; the output is flagged invalid
-        }
-        s_ids[i] = id;
-    }
-    if (threadIdx.x < kSqStages) {
-        mbar_init(&full[threadIdx.x], 1);
-        released[threadIdx.x] = 0u;
-    }
+    if (threadIdx.x < kSqWarps * kSqStages) mbar_init(&bars[threadIdx.x / kSqStages][threadIdx.x % kSqStages], 1);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
         s_flag = 0;
-        s_issued = 0;
     }
     fence_barrier_init();
     __syncthreads();
 
-    auto issue = [&](int k) {  // block k of the chunk into its stage (one thread)
-        const int st = k % kSqStages;
-        uint8_t* dst = smem + st * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-        tma_load_5d(dst, &kmap, &full[st], 0, 0, 0, kvh, s_ids[k]);
-        tma_load_5d(dst + C::kTileBytes, &vmap, &full[st], 0, 0, 0, kvh, s_ids[k]);
-        s_issued = k + 1;
+    // this warp's blocks b0 + warp + 4 k; lane l holds the ids of k = l, l + 32, l + 64, l + 96
+    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
+    int ids[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int kk = lane + 32 * j;
+        int id = 0;
+        if (kk < my_n) {
+            id = bt[b0 + warp + kSqWarps * kk];
+            if (id < 0 || id >= a.num_blocks) {
+                flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                id = 0;  // read a valid block; the output is flagged invalid
+            }
+        }
+        ids[j] = id;
+    }
+    auto block_id = [&](int kk) {  // warp-uniform kk < 128
+        const int j = kk >> 5;
+        const int v = j == 0 ? ids[0] : j == 1 ? ids[1] : j == 2 ? ids[2] : ids[3];
+        return __shfl_sync(0xFFFFFFFFu, v, kk & 31);
     };
-    if (threadIdx.x == 0)
-        for (int k = 0; k < min(kSqStages, nb); ++k) issue(k);
+    uint8_t* wbase = smem + warp * C::kWarpBytes;
+#pragma unroll
+    for (int kk = 0; kk < kSqStages; ++kk) {
+        const int pb = block_id(kk);
+        if (lane == 0 && kk < my_n) {
+            uint8_t* dst = wbase + kk * C::kStageBytes;
+            mbar_arrive_expect_tx(&bars[warp][kk], C::kStageBytes);
+            tma_load_5d(dst, &kmap, &bars[warp][kk], 0, 0, 0, kvh, pb);
+            tma_load_5d(dst + C::kTileBytes, &vmap, &bars[warp][kk], 0, 0, 0, kvh, pb);
+        }
+    }
 
-    // this warp's rows: r = 16 warp + g0 (+ 8); row r is query r / G, head r % G
+    // rows of the tile: lane rows g0 and g0 + 8
     const int g0 = lane >> 2;
     const int tig = lane & 3;
     int hi_r[2], lo_r[2];
-    uint32_t qa[KSTEPS][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int r = warp * 16 + g0 + 8 * h;
-        const int pos = off + r / G;  // the window is relative to the query's position
-        hi_r[h] = r < rows ? (a.causal ? pos : kv_len - 1) : -1;  // padding rows see no key
+        const int r = g0 + 8 * h;
+        const int pos = off + (16 * tile + r) / G;  // the window is relative to the query's position
+        hi_r[h] = r < trows ? (a.causal ? pos : kv_len - 1) : -1;  // padding rows see no key
         lo_r[h] = a.window > 0 ? max(0, pos - a.window + 1) : 0;
     }
+    uint32_t qa[KSTEPS][4];
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
 #pragma unroll
         for (int part = 0; part < 4; ++part) {
-            const int r = warp * 16 + g0 + ((part & 1) ? 8 : 0);
+            const int r = g0 + ((part & 1) ? 8 : 0);
             const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
             uint32_t v = 0;
-            if (r < rows) {
+            if (r < trows) {
+                const int R = 16 * tile + r;
                 const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
-                                            (static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G) * D;
+                                            (static_cast<size_t>(q0 + R / G) * a.hq + kvh * G + R % G) * D;
                 v = *reinterpret_cast<const uint32_t*>(qrow + col);
             }
             qa[kk][part] = v;
@@ -185,42 +198,18 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
 #pragma unroll
     for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-    // the last of the kMT warps to be done with stage st refills it
-    auto release = [&](int st, int k) {
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            const uint32_t before = atomicAdd(&released[st], 1u);
-            if (before == kMT - 1) {
-                released[st] = 0u;
-                __threadfence_block();
-                const int kn = k + kSqStages;
-                if (kn < nb) {
-                    fence_proxy_async_smem();
-                    issue(kn);
-                }
-            }
-        }
-    };
-
-    // A warp whose 16 rows are all padding only keeps the ring moving.
-    const bool active = warp * 16 < rows;
     bool failed = false;
     int k = 0;
-    for (; k < nb; ++k) {
+    for (; k < my_n; ++k) {
         const int st = k % kSqStages;
         const uint32_t ph = (k / kSqStages) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], ph))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[warp][st], ph))) {
             failed = true;
             break;
         }
-        if (!active) {
-            release(st, k);
-            continue;
-        }
-        const uint32_t kaddr = smem_u32(smem + st * C::kStageBytes);
+        const uint32_t kaddr = smem_u32(wbase + st * C::kStageBytes);
         const uint32_t vaddr = kaddr + C::kTileBytes;
-        const int tok_base = (b0 + k) * kBlockSize;
+        const int tok_base = (b0 + warp + k * kSqWarps) * kBlockSize;
 
         // ---- S = Q . K^T  (16 rows x 16 tokens)
         float sacc[2][4];
@@ -310,74 +299,114 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
                 mma_16816<false>(o[2 * j + 1], pa, v2, v3);
             }
         }
-        release(st, k);
+        __syncwarp();
+        // refill this stage with the block NSTAGE ahead
+        const int kn = k + kSqStages;
+        const int pb = block_id(kn & 127);
+        if (lane == 0 && kn < my_n) {
+            fence_proxy_async_smem();
+            uint8_t* dst = wbase + st * C::kStageBytes;
+            mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
+            tma_load_5d(dst, &kmap, &bars[warp][st], 0, 0, 0, kvh, pb);
+            tma_load_5d(dst + C::kTileBytes, &vmap, &bars[warp][st], 0, 0, 0, kvh, pb);
+        }
     }
     if (failed) {
-        // wait (bounded) for the loads still in flight, then report
-        const int issued = *reinterpret_cast<volatile int*>(&s_issued);
-        for (int kk = k; kk < issued; ++kk) (void)mbar_wait(&full[kk % kSqStages], (kk / kSqStages) & 1);
+        // drain the loads still in flight (bounded), then report
+        for (int kk = k + 1; kk < min(my_n, k + kSqStages); ++kk)
+            (void)mbar_wait(&bars[warp][kk % kSqStages], (kk / kSqStages) & 1);
         if (lane == 0) {
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
             atomicOr(&s_flag, 1);
         }
     }
-    __syncthreads();  // the ring is drained: its bytes take the merge state
-    const bool cta_failed = s_flag != 0;
-    float* state = reinterpret_cast<float*>(smem);  // [row][kStateStride]
 
-    // ---- this chunk's state per row: o / l and lse
+    // ---- combine the 4 warps of the CTA
+    l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], 1);
+    l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], 2);
+    l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], 1);
+    l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], 2);
+    __syncthreads();  // every warp is done with its stage buffers
+    float* comb = reinterpret_cast<float*>(smem);
+    {
+        float* cw = comb + warp * 16 * C::kCombStride;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float L = l_run[h];
-        L += __shfl_xor_sync(0xFFFFFFFFu, L, 1);
-        L += __shfl_xor_sync(0xFFFFFFFFu, L, 2);
-        const int r = warp * 16 + g0 + 8 * h;
+        for (int nt = 0; nt < NTILES; ++nt) {
+            const int col = nt * 8 + 2 * tig;
+            *reinterpret_cast<float2*>(cw + g0 * C::kCombStride + col) = make_float2(o[nt][0], o[nt][1]);
+            *reinterpret_cast<float2*>(cw + (g0 + 8) * C::kCombStride + col) = make_float2(o[nt][2], o[nt][3]);
+        }
+        if (tig == 0) {
+            s_m[warp][g0] = m_run[0];
+            s_m[warp][g0 + 8] = m_run[1];
+            s_l[warp][g0] = l_run[0];
+            s_l[warp][g0 + 8] = l_run[1];
+        }
+    }
+    __syncthreads();
+    const bool cta_failed = s_flag != 0;
+    // per row, once: the warps' weights 2^(m_w - M) / L (v_scale folded in)
+    // replace s_m, and the row's lse goes to s_l[0]
+    if (threadIdx.x < 16) {
+        const int r = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kSqWarps; ++w) M = fmaxf(M, s_m[w][r]);
+        float f[kSqWarps];
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSqWarps; ++w) {
+            f[w] = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
+            L += f[w] * s_l[w][r];
+        }
         const float inv = L > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / L : 0.f;
-        const float lse = L > 0.f && !cta_failed ? (m_run[h] + __log2f(L)) * 0.6931471805599453f : -INFINITY;
-        if (nsplit == 1) {
-            if (r >= rows || cta_failed) continue;
-            const size_t orow = static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G;
+        const float lse = L > 0.f && !cta_failed ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < NTILES; ++nt) {
-                const int col = nt * 8 + 2 * tig;
-                const float v0 = o[nt][2 * h] * inv, v1 = o[nt][2 * h + 1] * inv;
+        for (int w = 0; w < kSqWarps; ++w) s_m[w][r] = f[w] * inv;
+        s_l[0][r] = lse;
+    }
+    __syncthreads();
+    if (!cta_failed) {
+        for (int idx = threadIdx.x; idx < trows * D; idx += kSqThreads) {
+            const int r = idx / D;
+            const int d = idx % D;
+            float ov = 0.f;
+#pragma unroll
+            for (int w = 0; w < kSqWarps; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
+            if (nsplit == 1) {
+                const int R = 16 * tile + r;
+                const size_t orow = static_cast<size_t>(q0 + R / G) * a.hq + kvh * G + R % G;
                 if (a.out_f32)
-                    *reinterpret_cast<float2*>(a.out_f32 + orow * D + col) = make_float2(v0, v1);
+                    a.out_f32[orow * D + d] = ov;
                 else
-                    *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + col) =
-                        pack2<false>(v0, v1);
+                    static_cast<__nv_bfloat16*>(a.out)[orow * D + d] = __float2bfloat16_rn(ov);
+                if (a.lse_out && d == 0) a.lse_out[orow] = s_l[0][r];
+            } else {
+                comb[r * C::kCombStride + d] = ov;  // this chunk's state, in place of warp 0's rows
             }
-            if (a.lse_out && tig == 0) a.lse_out[orow] = lse;
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < NTILES; ++nt) {
-                const int col = nt * 8 + 2 * tig;
-                *reinterpret_cast<float2*>(state + r * C::kStateStride + col) =
-                    make_float2(o[nt][2 * h] * inv, o[nt][2 * h + 1] * inv);
-            }
-            if (tig == 0) s_lse[r] = lse;
         }
     }
     if constexpr (kCluster) {
         if (nsplit == 1) return;
-        // ---- cluster merge: chunk c holds rows' o_c (state) and lse_c (s_lse)
+        // ---- cluster merge: chunk c holds o_c (warp 0's rows of comb) and lse_c (s_l[0])
         cluster_sync();
-        float* wts = state + C::kStateFloats;            // [chunk][row]
-        float* rowM = wts + kSqMaxSplits * kSqMaxRowTiles * 16;
-        float* rowW = rowM + 64;
-        for (int r = threadIdx.x; r < kMT * 16; r += kThreads) {
+        float* wts = comb + 16 * C::kCombStride;  // warp 1's slice, free now: [chunk][16]
+        float* rowM = wts + kSqMaxSplits * 16;
+        float* rowW = rowM + 16;
+        if (threadIdx.x < 16) {
+            const int r = threadIdx.x;
             float l[kSqMaxSplits];
             float M = -INFINITY;
 #pragma unroll
             for (int c = 0; c < kSqMaxSplits; ++c) {
-                l[c] = c < nsplit ? ld_cluster_f32(cluster_map(smem_u32(&s_lse[r]), c)) : -INFINITY;
+                l[c] = c < nsplit ? ld_cluster_f32(cluster_map(smem_u32(&s_l[0][r]), c)) : -INFINITY;
                 M = fmaxf(M, l[c]);
             }
             float W = 0.f;
 #pragma unroll
             for (int c = 0; c < kSqMaxSplits; ++c) {
                 const float wv = l[c] == -INFINITY ? 0.f : __expf(l[c] - M);
-                wts[c * 64 + r] = wv;
+                wts[c * 16 + r] = wv;
                 W += wv;
             }
             rowM[r] = M;
@@ -385,13 +414,13 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
         }
         __syncthreads();
         constexpr int kSlotsPerRow = D / 4;
-        const int total = rows * kSlotsPerRow;
+        const int total = trows * kSlotsPerRow;
         const int s_lo = split * total / nsplit;
         const int s_hi = (split + 1) * total / nsplit;
-        for (int slot = s_lo + threadIdx.x; slot < s_hi; slot += kThreads) {
+        for (int slot = s_lo + threadIdx.x; slot < s_hi; slot += kSqThreads) {
             const int r = slot / kSlotsPerRow;
             const int c4 = slot % kSlotsPerRow;
-            const uint32_t local = smem_u32(state + r * C::kStateStride + c4 * 4);
+            const uint32_t local = smem_u32(comb + r * C::kCombStride + c4 * 4);
             float4 v[kSqMaxSplits];
 #pragma unroll
             for (int c = 0; c < kSqMaxSplits; ++c)
@@ -399,7 +428,7 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kSqMaxSplits; ++c) {
-                const float w = wts[c * 64 + r];
+                const float w = wts[c * 16 + r];
                 if (c < nsplit && w != 0.f) {
                     acc.x += w * v[c].x;
                     acc.y += w * v[c].y;
@@ -409,7 +438,8 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
             }
             const float W = rowW[r];
             const float inv = W > 0.f ? 1.f / W : 0.f;
-            const size_t orow = static_cast<size_t>(q0 + r / G) * a.hq + kvh * G + r % G;
+            const int R = 16 * tile + r;
+            const size_t orow = static_cast<size_t>(q0 + R / G) * a.hq + kvh * G + R % G;
             if (a.out_f32) {
                 *reinterpret_cast<float4*>(a.out_f32 + orow * D + c4 * 4) =
                     make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -423,13 +453,14 @@ __global__ void __launch_bounds__(kMT * 32) short_query_kernel(const PrefillArgs
     }
 }
 
-template <int D, int kMT>
-cudaError_t launch_sq_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+template <int D>
+cudaError_t launch_sq_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         cudaStream_t stream) {
     using C = SqCfg<D>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert((kSqMaxSplits + 2) * 16 <= 16 * C::kCombStride, "cluster merge scratch");
     const bool cluster = a.sq_splits > 1;
-    auto kern = cluster ? short_query_kernel<D, kMT, true> : short_query_kernel<D, kMT, false>;
+    auto kern = cluster ? short_query_kernel<D, true> : short_query_kernel<D, false>;
     static bool attr_set[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -440,25 +471,12 @@ cudaError_t launch_sq_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUt
         if (e != cudaSuccess) return e;
         attr_set[cluster][dev] = true;
     }
-    dim3 grid(a.sq_splits, a.hkv, a.num_seqs);
-    return launch_pdl_cluster(kern, grid, dim3(kMT * 32), C::kSmemBytes, stream,
+    dim3 grid(a.sq_splits, a.hkv * a.sq_row_tiles, a.num_seqs);
+    return launch_pdl_cluster(kern, grid, dim3(kSqThreads), C::kSmemBytes, stream,
                               cluster ? static_cast<unsigned>(a.sq_splits) : 1u, a, kmap, vmap);
 }
 
-template <int D>
-cudaError_t launch_sq_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        cudaStream_t stream) {
-    switch (a.sq_row_tiles) {
-        case 1: return launch_sq_t<D, 1>(a, kmap, vmap, stream);
-        case 2: return launch_sq_t<D, 2>(a, kmap, vmap, stream);
-        case 3: return launch_sq_t<D, 3>(a, kmap, vmap, stream);
-        default: return launch_sq_t<D, 4>(a, kmap, vmap, stream);
-    }
-}
-
 }  // namespace
-
-int short_query_smem_bytes(int d) { return d == 64 ? SqCfg<64>::kSmemBytes : SqCfg<128>::kSmemBytes; }
 
 cudaError_t launch_short_query(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream) {
