@@ -63,7 +63,7 @@ struct DecodeCfg {
     static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
     // bf16: one 5-D box per tile (16 rows x D/64 swizzled 128-byte slices);
     // fp8: one unswizzled 4-D box of 16 rows x D bytes
-    static constexpr int kConvBytes = kFp8 ? kBlockSize * D * 2 : 0;  // f16 V (K is read raw)
+    static constexpr int kConvBytes = kFp8 ? kBlockSize * D * 2 : 0;  // q rows staged once (e4m3)
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
     static constexpr int kCombBytes = kWarps * 16 * kCombStride * 4;
@@ -91,45 +91,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
         "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
-}
-
-// f16 staging of an fp8 tile: src [16][D] bytes (row-major) -> dst in the
-// kv_off layout, the one the bf16 path gets from TMA.  Lane l converts the
-// 16-byte chunks l, l + 32, ...; their offsets depend on the lane only
-// (Fp8Lane, computed once per kernel).
-template <int D>
-struct Fp8Lane {
-    static constexpr int kChunksPerRow = D / 16;
-    static constexpr int kPerLane = kBlockSize * kChunksPerRow / 32;  // 2 (D=64) or 4 (D=128)
-    uint32_t src[kPerLane];
-    uint32_t dst0[kPerLane];
-    uint32_t dst1[kPerLane];
-    __device__ __forceinline__ explicit Fp8Lane(int lane) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int c = lane + 32 * i;
-            const int r = c / kChunksPerRow;
-            const int d0 = (c % kChunksPerRow) * 2;  // destination 16-byte chunk (8 f16) in the row
-            src[i] = static_cast<uint32_t>(c * 16);
-            dst0[i] = kv_off<D>(r, d0);
-            dst1[i] = kv_off<D>(r, d0 + 1);
-        }
-    }
-};
-
-template <int D>
-__device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, const Fp8Lane<D>& ln) {
-#pragma unroll
-    for (int i = 0; i < Fp8Lane<D>::kPerLane; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + ln.src[i]);
-        uint32_t h[8];
-        e4m3x4_to_f16x4(v.x, h[0], h[1]);
-        e4m3x4_to_f16x4(v.y, h[2], h[3]);
-        e4m3x4_to_f16x4(v.z, h[4], h[5]);
-        e4m3x4_to_f16x4(v.w, h[6], h[7]);
-        *reinterpret_cast<uint4*>(dst + ln.dst0[i]) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(dst + ln.dst1[i]) = make_uint4(h[4], h[5], h[6], h[7]);
-    }
 }
 
 // One (block, head) tile of K or V into shared memory.
@@ -403,8 +364,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
 #pragma unroll
     for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-    const Fp8Lane<D> fp8_lane(lane);
-    uint8_t* convV = wbase + C::kStages * C::kStageBytes;
+
     bool failed = false;
     int k = 0;
     for (; k < my_n; ++k) {
@@ -417,11 +377,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         }
         const uint8_t* ktile = wbase + st * C::kStageBytes;
         const uint8_t* vtile = ktile + C::kTileBytes;
-        if constexpr (kFp8) {
-            convert_fp8_tile<D>(vtile, convV, fp8_lane);
-            __syncwarp();
-            vtile = convV;
-        }
         const uint32_t kaddr = smem_u32(ktile);
         const uint32_t vaddr = smem_u32(vtile);
 
@@ -529,7 +484,47 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
             keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
         }
-        {
+        if constexpr (kFp8) {
+            // e4m3 V straight from the raw tile.  The B operand pairs two
+            // tokens of one dim; lane (g, tig) takes dims [g D/8, (g+1) D/8)
+            // of V rows 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9 (b1), so
+            // n-tile nt's column of this lane is dim g D/8 + nt.  O's n-tile nt
+            // then holds dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt, which the
+            // combine below puts back in order.
+            constexpr int W = D / 32;  // 32-bit words of a lane's slice of one row
+            uint32_t r0[W], r1[W], r8[W], r9[W];
+            const uint8_t* vb = vtile + g0 * (D / 8);
+            auto row_words = [&](int row, uint32_t (&w)[W]) {
+                if constexpr (W == 2) {
+                    const uint2 t = *reinterpret_cast<const uint2*>(vb + row * D);
+                    w[0] = t.x;
+                    w[1] = t.y;
+                } else {
+                    const uint4 t = *reinterpret_cast<const uint4*>(vb + row * D);
+                    w[0] = t.x;
+                    w[1] = t.y;
+                    w[2] = t.z;
+                    w[3] = t.w;
+                }
+            };
+            row_words(2 * tig, r0);
+            row_words(2 * tig + 1, r1);
+            row_words(2 * tig + 8, r8);
+            row_words(2 * tig + 9, r9);
+#pragma unroll
+            for (int nt = 0; nt < NTILES; nt += 2) {
+                // bytes s, s+1 of word nt/4 from both rows of a pair: (a_s, b_s, a_s+1, b_s+1)
+                const uint32_t sel = (nt % 4 == 0) ? 0x5140u : 0x7362u;
+                uint32_t plo, phi;
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(plo) : "r"(r0[nt / 4]), "r"(r1[nt / 4]), "r"(sel));
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(phi) : "r"(r8[nt / 4]), "r"(r9[nt / 4]), "r"(sel));
+                uint32_t b0a, b0b, b1a, b1b;
+                e4m3x4_to_f16x4(plo, b0a, b0b);
+                e4m3x4_to_f16x4(phi, b1a, b1b);
+                mma_16816<true>(o[nt], pa, b0a & keep_lo, b1a & keep_hi);
+                mma_16816<true>(o[nt + 1], pa, b0b & keep_lo, b1b & keep_hi);
+            }
+        } else {
             const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
             const int csel = lane >> 4;
 #pragma unroll
@@ -545,6 +540,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                 mma_16816<kFp8>(o[2 * j + 1], pa, v2, v3);
             }
         }
+        (void)vaddr;
         __syncwarp();
         // refill this stage with the block NSTAGE ahead
         const int kn = k + C::kStages;
@@ -579,10 +575,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         float* cw = comb + warp * 16 * C::kCombStride;
 #pragma unroll
         for (int nt = 0; nt < NTILES; ++nt) {
-            const int col = nt * 8 + 2 * tig;
-            *reinterpret_cast<float2*>(cw + g0 * C::kCombStride + col) = make_float2(o[nt][0], o[nt][1]);
-            *reinterpret_cast<float2*>(cw + (g0 + 8) * C::kCombStride + col) =
-                make_float2(o[nt][2], o[nt][3]);
+            if constexpr (kFp8) {  // dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt
+                const int c0 = 2 * tig * (D / 8) + nt;
+                const int c1 = c0 + D / 8;
+                cw[g0 * C::kCombStride + c0] = o[nt][0];
+                cw[g0 * C::kCombStride + c1] = o[nt][1];
+                cw[(g0 + 8) * C::kCombStride + c0] = o[nt][2];
+                cw[(g0 + 8) * C::kCombStride + c1] = o[nt][3];
+            } else {
+                const int col = nt * 8 + 2 * tig;
+                *reinterpret_cast<float2*>(cw + g0 * C::kCombStride + col) = make_float2(o[nt][0], o[nt][1]);
+                *reinterpret_cast<float2*>(cw + (g0 + 8) * C::kCombStride + col) =
+                    make_float2(o[nt][2], o[nt][3]);
+            }
         }
         if (tig == 0) {
             s_m[warp][g0] = m_run[0];
