@@ -67,6 +67,8 @@ def library_path() -> str:
 def load_library():
     """Load libpkv.so (built in-tree by ``__graft_entry__.build()``)."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
