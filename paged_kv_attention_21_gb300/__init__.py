@@ -219,6 +219,42 @@ def pkv_decode_step(desc, q, k_new, v_new, k_cache, v_cache, block_tables, conte
         ws_bytes, _stream(stream)))
 
 
+class BoundCall:
+    """A C-ABI call with its arguments marshalled once.  The tensors are bound
+    by address and kept alive here: write new contents into the same tensors
+    and call again (the persistent-buffer pattern of a serving loop).  Each
+    call returns after the launch, like the unbound function."""
+
+    __slots__ = ("_fn", "_args", "_keep")
+
+    def __init__(self, fn, args, keep):
+        self._fn = fn
+        self._args = args
+        self._keep = keep
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            _check(st)
+
+
+def bind_decode_step(desc, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                     max_context_len, sm_scale, out, lse=None, workspace=None, cos_sin=None,
+                     window=-1, chunk_blocks=0, k_scale=None, v_scale=None, sinks=None, stream=None):
+    """pkv_decode_step with every argument marshalled once (see BoundCall)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    max_pos = 0 if cos_sin is None else int(cos_sin.shape[0])
+    desc_copy = CacheDesc.from_buffer_copy(desc)
+    args = (ctypes.byref(desc_copy), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cos_sin), max_pos,
+            _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+            _ptr(context_lens), int(context_lens.shape[0]), int(max_context_len), float(sm_scale),
+            int(window), _ptr(sinks), int(chunk_blocks), _ptr(out), _ptr(lse), _ptr(workspace),
+            ws_bytes, _stream(stream))
+    keep = (desc_copy, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, lse,
+            workspace, cos_sin, k_scale, v_scale, sinks)
+    return BoundCall(load_library().pkv_decode_step, args, keep)
+
+
 def pkv_decode_attention_static(desc, q, k_cache, v_cache, block_tables, context_lens,
                                 max_context_len, sm_scale, out, lse=None, window=-1,
                                 chunk_blocks=0, k_scale=None, v_scale=None, sinks=None,
@@ -290,4 +326,4 @@ def pkv_last_error() -> str:
 
 __all__ = [n for n in dir() if n.startswith("pkv_")] + [
     "CacheDesc", "make_desc", "PkvError", "load_library", "library_path", "KV_BF16",
-    "KV_FP8_E4M3"]
+    "KV_FP8_E4M3", "BoundCall", "bind_decode_step"]

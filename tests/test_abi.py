@@ -177,6 +177,17 @@ def test_decode_step_validates_its_new_token_arguments(lib):
     assert "max_context_len" in pkv.pkv_last_error()
 
 
+def test_bound_decode_step_reports_argument_errors_when_called(lib):
+    import torch
+    d = _desc()
+    q = torch.zeros((2, 16, 128), dtype=torch.bfloat16)
+    t = torch.zeros((2, 256), dtype=torch.int32)
+    l = torch.zeros(2, dtype=torch.int32)
+    call = pkv.bind_decode_step(d, q, None, q, q, q, t, l, 100, 0.1, q, stream=0)
+    with pytest.raises(pkv.PkvError, match="k_new"):
+        call()
+
+
 def test_planner_fills_the_gpu_and_respects_limits(lib):
     sms = 152
     # (Hq, Hkv, D, dtype, B, max_ctx, window)

@@ -188,3 +188,41 @@ def test_decode_step_in_a_graph_repeats():
     assert_close(out, ref, "graph-replayed step")
     assert_lse_close(lse, ref_lse, "graph-replayed step")
     assert pkv.pkv_device_errors() == 0
+
+
+def test_bound_decode_step_equals_the_unbound_call():
+    """bind_decode_step marshals the arguments once; refilling the bound q
+    and calling again gives the bits of a fresh unbound call."""
+    case, k_new, v_new, table = _setup(97, [40, 300, 1024, 2500], 16, 2, 128, False, True)
+    B = len(case.lens)
+    desc = pkv.make_desc(num_q_heads=16, num_kv_heads=2, head_dim=128, num_blocks=case.k_cache.shape[0],
+                         max_blocks_per_seq=case.tables.shape[1])
+    max_ctx = int(case.lens.max())
+    kn, vn, cs = _pool(k_new), _pool(v_new), _dev(table)
+    tabs, lens = _dev(case.tables), _dev(case.lens)
+    ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, 0), 256), dtype=torch.uint8,
+                     device=DEV)
+    rng = np.random.default_rng(98)
+    for trial in range(2):
+        q_new = _pool(bf16_bits(rng.standard_normal((B, 16, 128)).astype(np.float32)))
+        # unbound on fresh caches
+        kd, vd = _pool(case.k_cache), _pool(case.v_cache)
+        out_u = torch.empty((B, 16, 128), dtype=torch.bfloat16, device=DEV)
+        pkv.pkv_decode_step(desc, q_new, kn, vn, kd, vd, tabs, lens, max_ctx, 1 / math.sqrt(128), out_u,
+                            None, ws, cos_sin=cs)
+        # bound on fresh caches: q written into the bound buffer first
+        kd2, vd2 = _pool(case.k_cache), _pool(case.v_cache)
+        if trial == 0:
+            q_buf = torch.empty_like(q_new)
+            out_b = torch.empty_like(out_u)
+            call = pkv.bind_decode_step(desc, q_buf, kn, vn, kd2, vd2, tabs, lens, max_ctx,
+                                        1 / math.sqrt(128), out_b, None, ws, cos_sin=cs)
+        else:
+            # the bound caches are the first trial's: refill them in place
+            call._keep[4].copy_(kd2)
+            call._keep[5].copy_(vd2)
+        q_buf.copy_(q_new)
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(out_b, out_u)
+    assert pkv.pkv_device_errors() == 0
