@@ -34,7 +34,7 @@
  * rounding error.  Every sum runs in ascending index order; every product and
  * sum is a separately rounded operation (build with -ffp-contract=off).
  *
- * Readings of points the pages leave open (each is also listed in the design doc):
+ * Readings of points the pages leave open:
  *   cache layout [num_blocks][Hkv][block_size][D], K and V in separate pools;
  *   query head h reads KV head h / (Hq / Hkv);
  *   RoPE is the half-split (NeoX) form over the whole head_dim, fp32, with a

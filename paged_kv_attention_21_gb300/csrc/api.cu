@@ -301,9 +301,7 @@ pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, in
 // KV range takes the most chunks one cluster merges (kSqMaxSplits): on the
 // verify and cascade workloads that measured 1.2-1.3x faster than a one-wave
 // plan.  False when the longest KV range does not fit kSqMaxSplits chunks.
-bool plan_short_query(const pkv_cache_desc* desc, int max_kv, int max_q, int window, int* chunk_out,
-                      int* splits_out) {
-    (void)desc;
+bool plan_short_query(int max_kv, int max_q, int window, int* chunk_out, int* splits_out) {
     int mb = std::max(1, (max_kv + 15) / 16);
     if (window > 0) mb = std::min(mb, (window + max_q + 14) / 16 + 1);
     if (mb > pkv::kSqMaxSplits * pkv::kSqMaxChunk) return false;
@@ -678,7 +676,7 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
         for (int s2 = 0; s2 < num_seqs; ++s2) kv_bound = std::max(kv_bound, kv_lens_host[s2]);
     }
     const bool short_q = qo_indptr_host && max_q * G <= pkv::kSqMaxRowTiles * 16 &&
-                         plan_short_query(desc, kv_bound, max_q, window, &sq_chunk, &sq_splits);
+                         plan_short_query(kv_bound, max_q, window, &sq_chunk, &sq_splits);
     a.k_scale = fp8 ? k_scale : nullptr;
     a.v_scale = fp8 ? v_scale : nullptr;
     a.q = q;
@@ -983,7 +981,7 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         for (int g = 0; g < num_groups; ++g) max_prefix = std::max(max_prefix, prefix_lens_host[g]);
         int sq_chunk = 0, sq_splits = 0;
         if (a.max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
-            plan_short_query(desc, max_prefix, max_group, -1, &sq_chunk, &sq_splits)) {
+            plan_short_query(max_prefix, max_group, -1, &sq_chunk, &sq_splits)) {
             // a group's queries (at most 64 rows) over its prefix: short-query kernel
             CUtensorMap tkmap, tvmap;
             st = pool_map(k_cache, desc, &tkmap, kMapTileRows);
