@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
 
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
+    const bool hi_rows = G > 8;  // else each lane's second row (g0 + 8) is padding: its P stays 0
     float o[NTILES][4];
 #pragma unroll
     for (int nt = 0; nt < NTILES; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
@@ -436,29 +437,36 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
                 }
             }
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
         const float mn0 = fmaxf(m_run[0], mx0);
-        const float mn1 = fmaxf(m_run[1], mx1);
         const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
         const float al0 = fast_exp2(m_run[0] - mu0);
-        const float al1 = fast_exp2(m_run[1] - mu1);
         m_run[0] = mn0;
-        m_run[1] = mn1;
         float p[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
             p[n][0] = fast_exp2(x[n][0] - mu0);
             p[n][1] = fast_exp2(x[n][1] - mu0);
-            p[n][2] = fast_exp2(x[n][2] - mu1);
-            p[n][3] = fast_exp2(x[n][3] - mu1);
+            p[n][2] = p[n][3] = 0.f;
         }
         l_run[0] = l_run[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        l_run[1] = l_run[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        float al1 = 1.f;
+        if (hi_rows) {  // rows 8-15 are query heads only when the group has more than 8
+            float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+            const float mn1 = fmaxf(m_run[1], mx1);
+            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+            al1 = fast_exp2(m_run[1] - mu1);
+            m_run[1] = mn1;
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                p[n][2] = fast_exp2(x[n][2] - mu1);
+                p[n][3] = fast_exp2(x[n][3] - mu1);
+            }
+            l_run[1] = l_run[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        }
         if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
             for (int nt = 0; nt < NTILES; ++nt) {
