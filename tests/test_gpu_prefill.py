@@ -188,14 +188,18 @@ def test_mixed_step_workload_full_size():
     assert pkv.pkv_device_errors() == 0
 
 
-@pytest.mark.parametrize("hq,hkv,d,window", [(32, 8, 128, -1), (64, 8, 64, -1), (16, 2, 128, 128),
-                                             (64, 8, 64, 128)])
-def test_fp8_prefill_matches_oracle(hq, hkv, d, window):
+@pytest.mark.parametrize("hq,hkv,d,window,short", [(32, 8, 128, -1, False), (64, 8, 64, -1, False),
+                                                   (16, 2, 128, 128, False), (64, 8, 64, 128, False),
+                                                   (32, 8, 128, -1, True), (64, 8, 64, 128, True)])
+def test_fp8_prefill_matches_oracle(hq, hkv, d, window, short):
     """Ragged causal prefill over e4m3 pools with per-head scales (InferX, "The
-    kernels underneath": FP8 KV cache): against the oracle on the same codes."""
+    kernels underneath": FP8 KV cache): against the oracle on the same codes.
+    short: at most 64 query rows per sequence, so the staged pool is read by
+    the short-query kernel with the scales folded in."""
     from tests._cases import PagedCase
-    rng = np.random.default_rng(80 + d + hq + (window > 0))
-    case = PagedCase(rng, [300, 1000, 77, 520, 1], hq, hkv, d, q_lens=[64, 200, 77, 1, 1], fp8=True)
+    rng = np.random.default_rng(80 + d + hq + (window > 0) + 7 * short)
+    q_lens = [min(8, 64 // (hq // hkv)), 1, 3, 1, 1] if short else [64, 200, 77, 1, 1]
+    case = PagedCase(rng, [300, 1000, 77, 520, 1], hq, hkv, d, q_lens=q_lens, fp8=True)
     sm = 1.0 / np.sqrt(d)
     desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=case.num_blocks,
                          max_blocks_per_seq=case.mbps, kv_dtype=pkv.KV_FP8_E4M3)
