@@ -47,13 +47,12 @@ namespace pkv {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 4;  // warps of a CTA (a 2-warp variant serves one-chunk window plans)
 // Plans of 2..4 chunks per sequence merge inside a cluster (larger clusters
 // measured slower than the ticket merge: co-scheduling them leaves slots idle).
 constexpr int kMaxClusterSplits = 4;
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, int kW = kWarps>
 struct DecodeCfg {
     // bf16 tiles: 2 stages per warp keep ~3 CTAs (12 warps) resident per SM,
     // which measured faster than 3 stages at 2 CTAs; e4m3 tiles are small.
@@ -66,8 +65,8 @@ struct DecodeCfg {
     static constexpr int kConvBytes = kFp8 ? kBlockSize * D * 2 : 0;  // q rows staged once (e4m3)
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
-    static constexpr int kCombBytes = kWarps * 16 * kCombStride * 4;
-    static constexpr int kBodyBytes = kWarps * kWarpBytes > kCombBytes ? kWarps * kWarpBytes
+    static constexpr int kCombBytes = kW * 16 * kCombStride * 4;
+    static constexpr int kBodyBytes = kW * kWarpBytes > kCombBytes ? kW * kWarpBytes
                                                                        : kCombBytes;
     static constexpr int kSmemBytes = kBodyBytes + 1024;  // + alignment slack
 };
@@ -167,19 +166,20 @@ __device__ __forceinline__ void append_new_token(const DecodeArgs& a, int seq, i
 // (grid x = cluster x = max_splits, so a chunk's cluster rank is blockIdx.x)
 // and merge through distributed shared memory; otherwise through the
 // workspace and a ticket.
-template <int D, bool kFp8, bool kCluster>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
+template <int D, bool kFp8, bool kCluster, int kW>
+__global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
                                                           const __grid_constant__ CUtensorMap kmap,
                                                           const __grid_constant__ CUtensorMap vmap) {
-    using C = DecodeCfg<D, kFp8>;
+    using C = DecodeCfg<D, kFp8, kW>;
+    constexpr int kThreads = kW * 32;
     constexpr int KSTEPS = D / 16;   // k-steps of Q.K^T
     constexpr int NTILES = D / 8;    // n-tiles of O
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
-    __shared__ float s_m[kWarps][16];
-    __shared__ float s_l[kWarps][16];
+    __shared__ __align__(8) uint64_t bars[kW][C::kStages];
+    __shared__ float s_m[kW][16];
+    __shared__ float s_l[kW][16];
     __shared__ int s_flag;
 
     pdl_wait();
@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
     int phys = 0;
     if (a.window <= 0) {
-        const int lb = split * a.chunk_blocks + warp + lane * kWarps;
-        if (lane * kWarps < a.chunk_blocks && lb < a.mbps) phys = bt[lb];
+        const int lb = split * a.chunk_blocks + warp + lane * kW;
+        if (lane * kW < a.chunk_blocks && lb < a.mbps) phys = bt[lb];
     }
     int ctx = a.context_lens[seq];
     // the split plan (and the workspace) covers contexts up to max_ctx, which
@@ -231,9 +231,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     if (split >= nsplit) return;
     const int b0 = first_blk + split * a.chunk_blocks;
     const int b1 = min(last_blk + 1, b0 + a.chunk_blocks);
-    const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kWarps - 1) / kWarps : 0;
+    const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kW - 1) / kW : 0;
 
-    if (threadIdx.x < kWarps * C::kStages) mbar_init(&bars[threadIdx.x / C::kStages][threadIdx.x % C::kStages], 1);
+    if (threadIdx.x < kW * C::kStages) mbar_init(&bars[threadIdx.x / C::kStages][threadIdx.x % C::kStages], 1);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     // Physical block ids of this warp's blocks: lane k holds the k-th one.
     bool bad_id = false;
     if (lane < my_n) {
-        const int lb = b0 + warp + lane * kWarps;  // logical block
+        const int lb = b0 + warp + lane * kW;  // logical block
         if (a.window > 0) phys = bt[a.ring > 0 ? lb % a.ring : lb];
         if (phys < 0 || phys >= a.num_blocks) {
             flag_error(a.err, PKV_DEVERR_BLOCK_ID);
@@ -258,9 +258,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     // Fused append: the warp that loads the sequence's last block writes the
     // new token into it first -- before its prologue when that block is one
     // of the first NSTAGE, else right after (the refill that loads it comes later).
-    const int k_last = (last_blk - b0) / kWarps;
+    const int k_last = (last_blk - b0) / kW;
     const bool appender = a.k_new != nullptr && !clamped && split == nsplit - 1 &&
-                          warp == (last_blk - b0) % kWarps;
+                          warp == (last_blk - b0) % kW;
     auto append = [&]() {
         const int pb = __shfl_sync(0xFFFFFFFFu, phys, k_last & 31);
         const bool bad = __shfl_sync(0xFFFFFFFFu, bad_id, k_last & 31);
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         (void)kaddr;
 
         // ---- mask + online softmax (exp2 domain)
-        const int blk = b0 + warp + k * kWarps;
+        const int blk = b0 + warp + k * kW;
         const int tok_base = blk * kBlockSize;
         const bool edge = tok_base < lo || tok_base + kBlockSize > ctx;
         float x[2][4];
@@ -613,11 +613,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         const int r = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][r]);
-        float f[kWarps];
+        for (int w = 0; w < kW; ++w) M = fmaxf(M, s_m[w][r]);
+        float f[kW];
         float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < kW; ++w) {
             f[w] = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
             L += f[w] * s_l[w][r];
         }
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             lse = lse2;
         }
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s_m[w][r] = f[w] * inv;
+        for (int w = 0; w < kW; ++w) s_m[w][r] = f[w] * inv;
         s_l[0][r] = lse;
     }
     __syncthreads();
@@ -643,7 +643,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             const int d = idx % D;
             float ov = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
+            for (int w = 0; w < kW; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
             if (nsplit == 1) {
                 const size_t oi = (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d;
                 if (a.out_f32)
@@ -662,6 +662,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
         }
     }
     if (nsplit == 1) return;
+    // the 2-warp variant runs one-chunk plans only; the merges below assume 4 warps
+    if constexpr (kW < kWarps) return;
 
     if constexpr (kCluster) {
         // ---- cluster merge: chunk c of the pair holds o_c (rows of warp 0's
@@ -825,29 +827,41 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
     if (threadIdx.x == 0) a.counters[pair] = 0u;
 }
 
-template <int D, bool kFp8>
-cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+template <int D, bool kFp8, bool kCluster, int kW>
+cudaError_t launch_decode_v(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
-    using C = DecodeCfg<D, kFp8>;
+    using C = DecodeCfg<D, kFp8, kW>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert((kMaxClusterSplits + 2) * 16 <= 16 * C::kCombStride, "cluster merge scratch");
-    const bool cluster = a.max_splits >= 2 && a.max_splits <= kMaxClusterSplits;
-    auto kern = cluster ? decode_kernel<D, kFp8, true> : decode_kernel<D, kFp8, false>;
+    auto kern = decode_kernel<D, kFp8, kCluster, kW>;
     // The shared-memory opt-in is a per-device function attribute: set it on
     // the first launch on each device (never inside a stream capture).
-    static bool attr_set[2][64] = {};
+    static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[cluster][dev]) {
+    if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[cluster][dev] = true;
+        attr_set[dev] = true;
     }
     dim3 grid(a.max_splits, a.hkv, a.num_seqs);
-    return launch_pdl_cluster(kern, grid, dim3(kThreads), C::kSmemBytes, stream,
-                              cluster ? static_cast<unsigned>(a.max_splits) : 1u, a, kmap, vmap);
+    return launch_pdl_cluster(kern, grid, dim3(kW * 32), C::kSmemBytes, stream,
+                              kCluster ? static_cast<unsigned>(a.max_splits) : 1u, a, kmap, vmap);
+}
+
+template <int D, bool kFp8>
+cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+    // A windowed plan of one chunk per sequence has a few blocks per CTA:
+    // 2-warp CTAs, more of them resident, keep such a layer to one wave.
+    // (Each lane holds one block id of its warp: at most 32 blocks per warp.)
+    if (a.window > 0 && a.max_splits == 1 && a.chunk_blocks <= 2 * 32)
+        return launch_decode_v<D, kFp8, false, 2>(a, kmap, vmap, stream);
+    if (a.max_splits >= 2 && a.max_splits <= kMaxClusterSplits)
+        return launch_decode_v<D, kFp8, true, kWarps>(a, kmap, vmap, stream);
+    return launch_decode_v<D, kFp8, false, kWarps>(a, kmap, vmap, stream);
 }
 
 }  // namespace
