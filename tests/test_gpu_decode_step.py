@@ -17,8 +17,10 @@ import torch
 
 import oracle
 import paged_kv_attention_21_gb300 as pkv
+from paged_kv_attention_21_gb300 import workloads as wl
 from tests._cases import BS, PagedCase, bf16_bits
-from tests._gpu import DEV, NTHREADS, assert_close, assert_lse_close, pool_np
+from tests._gpu import (DEV, NTHREADS, assert_close, assert_lse_close, compact_pool, desc_for, on_device,
+                        pool_np, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -226,3 +228,53 @@ def test_bound_decode_step_equals_the_unbound_call():
         torch.cuda.synchronize()
         assert torch.equal(out_b, out_u)
     assert pkv.pkv_device_errors() == 0
+
+
+@pytest.mark.parametrize("cfg,window", [(2, -1), (3, -1), (5, -1), (5, wl.FP8_WINDOW)])
+def test_full_size_decode_step_on_sampled_sequences(cfg, window):
+    """The full-size batches in the benchmark's launch configuration (one
+    planned decode-step launch, inputs generated on the GPU).  A sample of
+    sequences -- shortest, longest and random ones -- is checked against the
+    oracle's own append and attention on a host copy of just their blocks,
+    and their appended cache rows byte for byte."""
+    spec = wl.CONFIGS[cfg]
+    b = wl.make_decode_batch(spec, DEV)
+    d = on_device(b)
+    desc = desc_for(spec, b.k_cache, b.tables_host)
+    max_ctx = b.max_context_len
+    rng = np.random.default_rng(100 + cfg)
+    seqs = sorted(set([int(np.argmin(b.lens_host)), int(np.argmax(b.lens_host))] +
+                      rng.choice(spec.batch, size=4, replace=False).tolist()))
+    k0, v0, tabs = compact_pool(d["k_cache"], d["v_cache"], b.tables_host, seqs)  # before the step
+    table = pkv.pkv_rope_cos_sin_table(spec.rope_theta, spec.head_dim, max_ctx)
+    ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, spec.batch, max_ctx, window, 0), 256),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=DEV)
+    pkv.pkv_decode_step(desc, d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["block_tables"],
+                        d["context_lens"], max_ctx, spec.sm_scale, out, lse, ws,
+                        cos_sin=torch.from_numpy(table).to(DEV), window=window, k_scale=d["k_scale"],
+                        v_scale=d["v_scale"])
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_errors() == 0
+    fp8 = spec.kv_dtype == "fp8_e4m3"
+    ks = None if d["k_scale"] is None else d["k_scale"].cpu().numpy()
+    vs = None if d["v_scale"] is None else d["v_scale"].cpu().numpy()
+    lens = b.lens_host[seqs]
+    q_rot = oracle.append_rope(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                               head_dim=spec.head_dim, block_size=BS, kv_dtype=1 if fp8 else 0,
+                               k_cache=k0, v_cache=v0, block_tables=tabs,
+                               token_to_seq=np.arange(len(seqs), dtype=np.int32),
+                               positions=(lens - 1).astype(np.int32), k_new=u16(d["k_new"])[seqs],
+                               v_new=u16(d["v_new"])[seqs], q=u16(d["q"])[seqs],
+                               cos_sin=oracle.rope_table(spec.rope_theta, spec.head_dim, max_ctx),
+                               k_scale=ks, v_scale=vs)
+    k1, v1, _ = compact_pool(d["k_cache"], d["v_cache"], b.tables_host, seqs)  # after the step
+    assert np.array_equal(k1, k0) and np.array_equal(v1, v0), "appended rows differ from the oracle's"
+    ref, ref_lse = oracle.paged_attention(q=q_rot, k_cache=k0, v_cache=v0, block_tables=tabs,
+                                          qo_indptr=np.arange(len(seqs) + 1), kv_lens=lens,
+                                          num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                                          sm_scale=spec.sm_scale, window=window, kv_dtype=1 if fp8 else 0,
+                                          k_scale=ks, v_scale=vs, nthreads=NTHREADS)
+    assert_close(out[seqs], ref, "%s decode step, sampled" % spec.name)
+    assert_lse_close(lse[seqs], ref_lse, "%s decode step" % spec.name)
