@@ -54,6 +54,9 @@ def parse_args():
                         "cascade / verify / cow / ring / fp8-prefill: the next-step rows, each "
                         "on its own seeded workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--chunk-blocks", type=int, default=0,
+                   help="decode chunk length in blocks passed to the library (0: the planner's "
+                        "choice)")
     p.add_argument("--two-launch", action="store_true",
                    help="run append and decode as two launches per layer instead of the "
                         "fused decode step")
@@ -199,9 +202,10 @@ class DecodeWorkload:
     """A decode workload: instances over disjoint regions of one pool (per
     layer), each with its own device workspace-free inputs."""
 
-    def __init__(self, config, dev, rank, fused=True):
+    def __init__(self, config, dev, rank, fused=True, chunk=0):
         import paged_kv_attention_21_gb300 as pkv
         self.fused = fused
+        self.chunk = chunk
         from paged_kv_attention_21_gb300 import workloads as wl
         self.pkv = pkv
         spec = wl.CONFIGS[config]
@@ -236,7 +240,7 @@ class DecodeWorkload:
                                   max_blocks_per_seq=b0.tables_host.shape[1],
                                   kv_dtype=spec.kv_dtype)
         self.max_ctx = spec.ctx_hi
-        ws = max(pkv.pkv_decode_workspace_size(self.desc, spec.batch, self.max_ctx, w, 0)
+        ws = max(pkv.pkv_decode_workspace_size(self.desc, spec.batch, self.max_ctx, w, chunk)
                  for w in self.windows)
         self.ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
         self.table = torch.from_numpy(pkv.pkv_rope_cos_sin_table(spec.rope_theta, spec.head_dim,
@@ -279,8 +283,8 @@ class DecodeWorkload:
                 pkv.pkv_decode_step(self.desc, b.q, b.k_new, b.v_new, b.k_cache, b.v_cache,
                                     b.block_tables, b.context_lens, self.max_ctx,
                                     self.spec.sm_scale, self.out, self.lse, self.ws,
-                                    cos_sin=self.table, window=w, k_scale=b.k_scale,
-                                    v_scale=b.v_scale)
+                                    cos_sin=self.table, window=w, chunk_blocks=self.chunk,
+                                    k_scale=b.k_scale, v_scale=b.v_scale)
                 if ev_pairs is not None:
                     ev_pairs[li][1].record()
                 n += 1
@@ -292,8 +296,8 @@ class DecodeWorkload:
                 ev_pairs[li][0].record()
             pkv.pkv_decode_attention(self.desc, b.q, b.k_cache, b.v_cache, b.block_tables,
                                      b.context_lens, self.max_ctx, self.spec.sm_scale, self.out,
-                                     self.lse, self.ws, window=w, k_scale=b.k_scale,
-                                     v_scale=b.v_scale)
+                                     self.lse, self.ws, window=w, chunk_blocks=self.chunk,
+                                     k_scale=b.k_scale, v_scale=b.v_scale)
             if ev_pairs is not None:
                 ev_pairs[li][1].record()
             n += 2
@@ -338,7 +342,7 @@ def time_pkv(args, rank, world, local):
     import paged_kv_attention_21_gb300 as pkv
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    W = DecodeWorkload(args.config, dev, rank, fused=not args.two_launch)
+    W = DecodeWorkload(args.config, dev, rank, fused=not args.two_launch, chunk=args.chunk_blocks)
     K, Wm = args.steps, max(3, args.warmup)
     R = 64 if W.n_inst > 1 else 8          # steps per captured graph
     R = max(W.n_inst, min(R, K))
@@ -461,8 +465,8 @@ def time_e2e(W, dev, steps):
                 bound[(j, li)] = pkv.bind_decode_step(
                     W.desc, devbuf["q"], devbuf["k_new"], devbuf["v_new"], b.k_cache, b.v_cache,
                     devbuf["block_tables"], devbuf["context_lens"], W.max_ctx, W.spec.sm_scale,
-                    W.out, None, W.ws, cos_sin=W.table, window=w, k_scale=b.k_scale,
-                    v_scale=b.v_scale, stream=sh)
+                    W.out, None, W.ws, cos_sin=W.table, window=w, chunk_blocks=W.chunk,
+                    k_scale=b.k_scale, v_scale=b.v_scale, stream=sh)
 
     def one(i):
         dev_all.copy_(host[i % W.n_inst], non_blocking=True)
@@ -477,7 +481,7 @@ def time_e2e(W, dev, steps):
             pkv.pkv_decode_attention(W.desc, devbuf["q"], b.k_cache, b.v_cache,
                                      devbuf["block_tables"], devbuf["context_lens"], W.max_ctx,
                                      W.spec.sm_scale, W.out, None, W.ws, window=w,
-                                     k_scale=b.k_scale, v_scale=b.v_scale)
+                                     chunk_blocks=W.chunk, k_scale=b.k_scale, v_scale=b.v_scale)
         if W.prefill is not None:
             W.prefill.run()
         out_h.copy_(W.out, non_blocking=True)

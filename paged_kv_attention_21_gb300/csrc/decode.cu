@@ -162,6 +162,262 @@ __device__ __forceinline__ void append_new_token(const DecodeArgs& a, int seq, i
     __syncwarp();
 }
 
+// Q fragments (A operand) of sequence seq's group kvh: rows = the G query
+// heads, zero-padded to 16.  rot_pos >= 0 also loads the (cos, sin) pairs
+// of that position that rotate_q applies; the loads are only issued here, so
+// a caller can overlap them with other work before rotating.
+template <int D>
+__device__ __forceinline__ void load_q_raw(const DecodeArgs& a, int seq, int kvh, int rot_pos, int lane,
+                                           uint32_t (&qa)[D / 16][4], float4 (&cs)[D / 32][2]) {
+    constexpr int KSTEPS = D / 16;
+    const int G = a.group;
+    const int g0 = lane >> 2;
+    const int tig = lane & 3;
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) +
+                              (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            const int row = g0 + ((part & 1) ? 8 : 0);
+            const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
+            uint32_t v = 0;
+            if (row < G) v = *reinterpret_cast<const uint32_t*>(qb + row * D + col);
+            qa[kk][part] = v;
+        }
+    }
+    if (rot_pos >= 0) {
+        // column c of k-step kk pairs with column c + D/2 (k-step kk + KSTEPS/2);
+        // a lane's columns are kk 16 + 2 tig (+ 8), each with its neighbour c + 1
+        const float* t = a.cos_sin + static_cast<size_t>(rot_pos) * (D / 2) * 2;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS / 2; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                cs[kk][h] = *reinterpret_cast<const float4*>(t + (kk * 16 + 2 * tig + 8 * h) * 2);
+    }
+}
+
+// RoPE on the Q fragments with the (cos, sin) pairs load_q_raw fetched,
+// rounded to bf16 as the standalone append rounds q: columns c, c + 1 sit in
+// one register, and their partners c + D/2, c + D/2 + 1 in k-step kk + D/32.
+template <int D>
+__device__ __forceinline__ void rotate_q(uint32_t (&qa)[D / 16][4], const float4 (&cs)[D / 32][2]) {
+    constexpr int KSTEPS = D / 16;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS / 2; ++kk) {
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            const float4 t = cs[kk][(part & 2) ? 1 : 0];  // c, s of col, col + 1
+            const uint32_t va = qa[kk][part];
+            const uint32_t vb = qa[kk + KSTEPS / 2][part];
+            const float a0 = bf16_lo(va), a1 = bf16_hi(va);
+            const float b0v = bf16_lo(vb), b1v = bf16_hi(vb);
+            const float lo0 = __fsub_rn(__fmul_rn(a0, t.x), __fmul_rn(b0v, t.y));
+            const float hi0 = __fadd_rn(__fmul_rn(b0v, t.x), __fmul_rn(a0, t.y));
+            const float lo1 = __fsub_rn(__fmul_rn(a1, t.z), __fmul_rn(b1v, t.w));
+            const float hi1 = __fadd_rn(__fmul_rn(b1v, t.z), __fmul_rn(a1, t.w));
+            qa[kk][part] = pack2<false>(lo0, lo1);
+            qa[kk + KSTEPS / 2][part] = pack2<false>(hi0, hi1);
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int seq, int kvh, int rot_pos, int lane,
+                                       uint32_t (&qa)[D / 16][4]) {
+    float4 cs[D / 32][2];
+    load_q_raw<D>(a, seq, kvh, rot_pos, lane, qa, cs);
+    if (rot_pos >= 0) rotate_q<D>(qa, cs);
+}
+
+// One block of K and V (16 tokens of one KV head, in shared memory) into a
+// warp's running state:
+//     S[16 x 16] = Q . K^T              (rows: the group's query heads, padded)
+//     online softmax of S over the keys in [lo, ctx), exp2 domain
+//     O[16 x D] += P . V
+// tok_base is the block's first token position.  Rows g0 + 8 take part only
+// when hi_rows (a group of more than 8 heads).
+template <int D, bool kFp8>
+__device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
+                                             float (&m_run)[2], float (&l_run)[2], const uint8_t* ktile,
+                                             const uint8_t* vtile, int lane, int tok_base, int lo, int ctx,
+                                             float scale_log2, bool hi_rows) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int NTILES = D / 8;
+    const int g0 = lane >> 2;
+    const int tig = lane & 3;
+    const uint32_t kaddr = smem_u32(ktile);
+    const uint32_t vaddr = smem_u32(vtile);
+
+    // ---- S = Q . K^T  (16 heads x 16 tokens)
+    float sacc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+    if constexpr (kFp8) {
+        // rows g (tokens 0-7 tile) and g + 8 (tokens 8-15 tile), bytes
+        // [tig D/4, (tig+1) D/4): word kk -> k-step kk's two f16 pairs
+        uint32_t kw[2][D / 16];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int q4 = 0; q4 < D / 64; ++q4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(ktile + (g0 + 8 * n) * D + tig * (D / 4) + 16 * q4);
+                kw[n][4 * q4] = v.x;
+                kw[n][4 * q4 + 1] = v.y;
+                kw[n][4 * q4 + 2] = v.z;
+                kw[n][4 * q4 + 3] = v.w;
+            }
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            e4m3x4_to_f16x4(kw[0][kk], b0, b1);
+            e4m3x4_to_f16x4(kw[1][kk], b2, b3);
+            mma_16816<true>(sacc[0], qa[kk], b0, b1);
+            mma_16816<true>(sacc[1], qa[kk], b2, b3);
+        }
+    } else {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            const int chunk = 2 * kk + csel;
+            uint32_t b00, b01, b10, b11;
+            ldmatrix_x4(b00, b01, b10, b11, kaddr + kv_off<D>(tok, chunk));
+            mma_16816<kFp8>(sacc[0], qa[kk], b00, b01);
+            mma_16816<kFp8>(sacc[1], qa[kk], b10, b11);
+        }
+    }
+    (void)kaddr;
+
+    // ---- mask + online softmax (exp2 domain)
+    const bool edge = tok_base < lo || tok_base + kBlockSize > ctx;
+    float x[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[n][e] = sacc[n][e] * scale_log2;
+            if (edge) {
+                const int t = tok_base + n * 8 + 2 * tig + (e & 1);
+                if (t < lo || t >= ctx) x[n][e] = -INFINITY;
+            }
+        }
+    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+    const float mn0 = fmaxf(m_run[0], mx0);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float al0 = fast_exp2(m_run[0] - mu0);
+    m_run[0] = mn0;
+    float p[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        p[n][0] = fast_exp2(x[n][0] - mu0);
+        p[n][1] = fast_exp2(x[n][1] - mu0);
+        p[n][2] = p[n][3] = 0.f;
+    }
+    l_run[0] = l_run[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+    float al1 = 1.f;
+    if (hi_rows) {  // rows 8-15 are query heads only when the group has more than 8
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+        const float mn1 = fmaxf(m_run[1], mx1);
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        al1 = fast_exp2(m_run[1] - mu1);
+        m_run[1] = mn1;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            p[n][2] = fast_exp2(x[n][2] - mu1);
+            p[n][3] = fast_exp2(x[n][3] - mu1);
+        }
+        l_run[1] = l_run[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+    }
+    if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < NTILES; ++nt) {
+            o[nt][0] *= al0;
+            o[nt][1] *= al0;
+            o[nt][2] *= al1;
+            o[nt][3] *= al1;
+        }
+    }
+    uint32_t pa[4];
+    pa[0] = pack2<kFp8>(p[0][0], p[0][1]);
+    pa[1] = pack2<kFp8>(p[0][2], p[0][3]);
+    pa[2] = pack2<kFp8>(p[1][0], p[1][1]);
+    pa[3] = pack2<kFp8>(p[1][2], p[1][3]);
+
+    // ---- O += P . V   (V rows masked to zero past the visible range so a
+    // NaN in an unused slot never meets a zero weight inside the MMA)
+    uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
+    if (edge) {
+        const int t0 = tok_base + 2 * tig;
+        const bool v0 = t0 >= lo && t0 < ctx, v1 = t0 + 1 >= lo && t0 + 1 < ctx;
+        const bool v8 = t0 + 8 >= lo && t0 + 8 < ctx, v9 = t0 + 9 >= lo && t0 + 9 < ctx;
+        keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
+        keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
+    }
+    if constexpr (kFp8) {
+        // e4m3 V straight from the raw tile.  The B operand pairs two
+        // tokens of one dim; lane (g, tig) takes dims [g D/8, (g+1) D/8)
+        // of V rows 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9 (b1), so
+        // n-tile nt's column of this lane is dim g D/8 + nt.  O's n-tile nt
+        // then holds dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt, which the
+        // combine below puts back in order.
+        constexpr int W = D / 32;  // 32-bit words of a lane's slice of one row
+        uint32_t r0[W], r1[W], r8[W], r9[W];
+        const uint8_t* vb = vtile + g0 * (D / 8);
+        auto row_words = [&](int row, uint32_t (&w)[W]) {
+            if constexpr (W == 2) {
+                const uint2 t = *reinterpret_cast<const uint2*>(vb + row * D);
+                w[0] = t.x;
+                w[1] = t.y;
+            } else {
+                const uint4 t = *reinterpret_cast<const uint4*>(vb + row * D);
+                w[0] = t.x;
+                w[1] = t.y;
+                w[2] = t.z;
+                w[3] = t.w;
+            }
+        };
+        row_words(2 * tig, r0);
+        row_words(2 * tig + 1, r1);
+        row_words(2 * tig + 8, r8);
+        row_words(2 * tig + 9, r9);
+#pragma unroll
+        for (int nt = 0; nt < NTILES; nt += 2) {
+            // bytes s, s+1 of word nt/4 from both rows of a pair: (a_s, b_s, a_s+1, b_s+1)
+            const uint32_t sel = (nt % 4 == 0) ? 0x5140u : 0x7362u;
+            uint32_t plo, phi;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(plo) : "r"(r0[nt / 4]), "r"(r1[nt / 4]), "r"(sel));
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(phi) : "r"(r8[nt / 4]), "r"(r9[nt / 4]), "r"(sel));
+            uint32_t b0a, b0b, b1a, b1b;
+            e4m3x4_to_f16x4(plo, b0a, b0b);
+            e4m3x4_to_f16x4(phi, b1a, b1b);
+            mma_16816<true>(o[nt], pa, b0a & keep_lo, b1a & keep_hi);
+            mma_16816<true>(o[nt + 1], pa, b0b & keep_lo, b1b & keep_hi);
+        }
+    } else {
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+            const int chunk = 2 * j + csel;
+            uint32_t v0, v1, v2, v3;
+            ldmatrix_x4_trans(v0, v1, v2, v3, vaddr + kv_off<D>(tok, chunk));
+            v0 &= keep_lo;
+            v2 &= keep_lo;
+            v1 &= keep_hi;
+            v3 &= keep_hi;
+            mma_16816<kFp8>(o[2 * j], pa, v0, v1);
+            mma_16816<kFp8>(o[2 * j + 1], pa, v2, v3);
+        }
+    }
+    (void)vaddr;
+}
+
 // kCluster: the chunks of one (sequence, KV head) form a thread-block cluster
 // (grid x = cluster x = max_splits, so a chunk's cluster rank is blockIdx.x)
 // and merge through distributed shared memory; otherwise through the
@@ -287,45 +543,8 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const int g0 = lane >> 2;
     const int tig = lane & 3;
     uint32_t qa[KSTEPS][4];
+    load_q<D>(a, seq, kvh, (a.k_new != nullptr && a.cos_sin != nullptr && !clamped) ? ctx - 1 : -1, lane, qa);
     {
-        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) +
-                                  (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                const int row = g0 + ((part & 1) ? 8 : 0);
-                const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
-                uint32_t v = 0;
-                if (row < G) v = *reinterpret_cast<const uint32_t*>(qb + row * D + col);
-                qa[kk][part] = v;
-            }
-        }
-        if (a.k_new != nullptr && a.cos_sin != nullptr && !clamped) {
-            // decode step: rotate q at the new token's position, rounded to
-            // bf16 as the standalone append rounds it.  Column c of k-step kk
-            // pairs with column c + D/2, held by the same lane in k-step
-            // kk + KSTEPS/2; columns c, c+1 sit in one register.
-            const float* cs = a.cos_sin + static_cast<size_t>(ctx - 1) * (D / 2) * 2;
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS / 2; ++kk) {
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {
-                    const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
-                    const float4 t = *reinterpret_cast<const float4*>(cs + col * 2);  // c, s of col, col+1
-                    const uint32_t va = qa[kk][part];
-                    const uint32_t vb = qa[kk + KSTEPS / 2][part];
-                    const float a0 = bf16_lo(va), a1 = bf16_hi(va);
-                    const float b0v = bf16_lo(vb), b1v = bf16_hi(vb);
-                    const float lo0 = __fsub_rn(__fmul_rn(a0, t.x), __fmul_rn(b0v, t.y));
-                    const float hi0 = __fadd_rn(__fmul_rn(b0v, t.x), __fmul_rn(a0, t.y));
-                    const float lo1 = __fsub_rn(__fmul_rn(a1, t.z), __fmul_rn(b1v, t.w));
-                    const float hi1 = __fadd_rn(__fmul_rn(b1v, t.z), __fmul_rn(a1, t.w));
-                    qa[kk][part] = pack2<false>(lo0, lo1);
-                    qa[kk + KSTEPS / 2][part] = pack2<false>(hi0, hi1);
-                }
-            }
-        }
         if constexpr (kFp8) {
             // e4m3 pools: K fragments come straight from the raw tile, lane
             // (g, tig) reading its rows' bytes [tig D/4, (tig+1) D/4), so
@@ -377,178 +596,8 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
             break;
         }
         const uint8_t* ktile = wbase + st * C::kStageBytes;
-        const uint8_t* vtile = ktile + C::kTileBytes;
-        const uint32_t kaddr = smem_u32(ktile);
-        const uint32_t vaddr = smem_u32(vtile);
-
-        // ---- S = Q . K^T  (16 heads x 16 tokens)
-        float sacc[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-        if constexpr (kFp8) {
-            // rows g (tokens 0-7 tile) and g + 8 (tokens 8-15 tile), bytes
-            // [tig D/4, (tig+1) D/4): word kk -> k-step kk's two f16 pairs
-            uint32_t kw[2][D / 16];
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int q4 = 0; q4 < D / 64; ++q4) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(ktile + (g0 + 8 * n) * D + tig * (D / 4) + 16 * q4);
-                    kw[n][4 * q4] = v.x;
-                    kw[n][4 * q4 + 1] = v.y;
-                    kw[n][4 * q4 + 2] = v.z;
-                    kw[n][4 * q4 + 3] = v.w;
-                }
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                uint32_t b0, b1, b2, b3;
-                e4m3x4_to_f16x4(kw[0][kk], b0, b1);
-                e4m3x4_to_f16x4(kw[1][kk], b2, b3);
-                mma_16816<true>(sacc[0], qa[kk], b0, b1);
-                mma_16816<true>(sacc[1], qa[kk], b2, b3);
-            }
-        } else {
-            const int tok = (lane & 7) + ((lane >> 4) << 3);
-            const int csel = (lane >> 3) & 1;
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int chunk = 2 * kk + csel;
-                uint32_t b00, b01, b10, b11;
-                ldmatrix_x4(b00, b01, b10, b11, kaddr + kv_off<D>(tok, chunk));
-                mma_16816<kFp8>(sacc[0], qa[kk], b00, b01);
-                mma_16816<kFp8>(sacc[1], qa[kk], b10, b11);
-            }
-        }
-        (void)kaddr;
-
-        // ---- mask + online softmax (exp2 domain)
-        const int blk = b0 + warp + k * kW;
-        const int tok_base = blk * kBlockSize;
-        const bool edge = tok_base < lo || tok_base + kBlockSize > ctx;
-        float x[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[n][e] = sacc[n][e] * scale_log2;
-                if (edge) {
-                    const int t = tok_base + n * 8 + 2 * tig + (e & 1);
-                    if (t < lo || t >= ctx) x[n][e] = -INFINITY;
-                }
-            }
-        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-        const float mn0 = fmaxf(m_run[0], mx0);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float al0 = fast_exp2(m_run[0] - mu0);
-        m_run[0] = mn0;
-        float p[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            p[n][0] = fast_exp2(x[n][0] - mu0);
-            p[n][1] = fast_exp2(x[n][1] - mu0);
-            p[n][2] = p[n][3] = 0.f;
-        }
-        l_run[0] = l_run[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        float al1 = 1.f;
-        if (hi_rows) {  // rows 8-15 are query heads only when the group has more than 8
-            float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-            const float mn1 = fmaxf(m_run[1], mx1);
-            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            al1 = fast_exp2(m_run[1] - mu1);
-            m_run[1] = mn1;
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                p[n][2] = fast_exp2(x[n][2] - mu1);
-                p[n][3] = fast_exp2(x[n][3] - mu1);
-            }
-            l_run[1] = l_run[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-        }
-        if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int nt = 0; nt < NTILES; ++nt) {
-                o[nt][0] *= al0;
-                o[nt][1] *= al0;
-                o[nt][2] *= al1;
-                o[nt][3] *= al1;
-            }
-        }
-        uint32_t pa[4];
-        pa[0] = pack2<kFp8>(p[0][0], p[0][1]);
-        pa[1] = pack2<kFp8>(p[0][2], p[0][3]);
-        pa[2] = pack2<kFp8>(p[1][0], p[1][1]);
-        pa[3] = pack2<kFp8>(p[1][2], p[1][3]);
-
-        // ---- O += P . V   (V rows masked to zero past the visible range so a
-        // NaN in an unused slot never meets a zero weight inside the MMA)
-        uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
-        if (edge) {
-            const int t0 = tok_base + 2 * tig;
-            const bool v0 = t0 >= lo && t0 < ctx, v1 = t0 + 1 >= lo && t0 + 1 < ctx;
-            const bool v8 = t0 + 8 >= lo && t0 + 8 < ctx, v9 = t0 + 9 >= lo && t0 + 9 < ctx;
-            keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
-            keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
-        }
-        if constexpr (kFp8) {
-            // e4m3 V straight from the raw tile.  The B operand pairs two
-            // tokens of one dim; lane (g, tig) takes dims [g D/8, (g+1) D/8)
-            // of V rows 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9 (b1), so
-            // n-tile nt's column of this lane is dim g D/8 + nt.  O's n-tile nt
-            // then holds dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt, which the
-            // combine below puts back in order.
-            constexpr int W = D / 32;  // 32-bit words of a lane's slice of one row
-            uint32_t r0[W], r1[W], r8[W], r9[W];
-            const uint8_t* vb = vtile + g0 * (D / 8);
-            auto row_words = [&](int row, uint32_t (&w)[W]) {
-                if constexpr (W == 2) {
-                    const uint2 t = *reinterpret_cast<const uint2*>(vb + row * D);
-                    w[0] = t.x;
-                    w[1] = t.y;
-                } else {
-                    const uint4 t = *reinterpret_cast<const uint4*>(vb + row * D);
-                    w[0] = t.x;
-                    w[1] = t.y;
-                    w[2] = t.z;
-                    w[3] = t.w;
-                }
-            };
-            row_words(2 * tig, r0);
-            row_words(2 * tig + 1, r1);
-            row_words(2 * tig + 8, r8);
-            row_words(2 * tig + 9, r9);
-#pragma unroll
-            for (int nt = 0; nt < NTILES; nt += 2) {
-                // bytes s, s+1 of word nt/4 from both rows of a pair: (a_s, b_s, a_s+1, b_s+1)
-                const uint32_t sel = (nt % 4 == 0) ? 0x5140u : 0x7362u;
-                uint32_t plo, phi;
-                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(plo) : "r"(r0[nt / 4]), "r"(r1[nt / 4]), "r"(sel));
-                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(phi) : "r"(r8[nt / 4]), "r"(r9[nt / 4]), "r"(sel));
-                uint32_t b0a, b0b, b1a, b1b;
-                e4m3x4_to_f16x4(plo, b0a, b0b);
-                e4m3x4_to_f16x4(phi, b1a, b1b);
-                mma_16816<true>(o[nt], pa, b0a & keep_lo, b1a & keep_hi);
-                mma_16816<true>(o[nt + 1], pa, b0b & keep_lo, b1b & keep_hi);
-            }
-        } else {
-            const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int csel = lane >> 4;
-#pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                const int chunk = 2 * j + csel;
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(v0, v1, v2, v3, vaddr + kv_off<D>(tok, chunk));
-                v0 &= keep_lo;
-                v2 &= keep_lo;
-                v1 &= keep_hi;
-                v3 &= keep_hi;
-                mma_16816<kFp8>(o[2 * j], pa, v0, v1);
-                mma_16816<kFp8>(o[2 * j + 1], pa, v2, v3);
-            }
-        }
-        (void)vaddr;
+        attend_block<D, kFp8>(qa, o, m_run, l_run, ktile, ktile + C::kTileBytes, lane,
+                              (b0 + warp + k * kW) * kBlockSize, lo, ctx, scale_log2, hi_rows);
         __syncwarp();
         // refill this stage with the block NSTAGE ahead
         const int kn = k + C::kStages;
