@@ -576,11 +576,11 @@ def workload_config(W, extra=None):
 def main_prefill(args, rank, world, local):
     """The prefill part of the Llama-3-8B-shaped mixed step on its own: 8 chunks
     of 512 query tokens over cached prefixes U[0, 8192], 32/8 heads, D 128,
-    causal.  Each timed launch follows an L2 flush (a 256 MiB write)."""
+    causal.  Each timed launch follows an L2 flush (L2Flush)."""
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     P = PrefillPart(dev, rank)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
         P.run()
@@ -625,7 +625,7 @@ def main_prefill(args, rank, world, local):
         "config": {"workload": P.spec.name, "num_q_heads": P.spec.num_q_heads,
                    "num_kv_heads": P.spec.num_kv_heads, "head_dim": P.spec.head_dim,
                    "q_tokens": P.tokens, "causal": True,
-                   "l2": "256 MiB write before every timed launch"},
+                   "l2": L2_NOTE},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                      "kernel": "prefill_tc_kernel (tcgen05, two query tiles per CTA)",
@@ -642,10 +642,29 @@ def main_prefill(args, rank, world, local):
 
 # ------------------------------------------------------ next-step parts --
 
+class L2Flush:
+    """Between timed launches: write a 256 MiB buffer (twice L2), then read
+    another 256 MiB buffer.  The read evicts the written lines, so their
+    write-back to DRAM happens here and not inside the next timed launch,
+    which then starts against an L2 of clean lines that hold none of its
+    inputs."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+L2_NOTE = "before every timed launch a 256 MiB write, then a 256 MiB read (L2 left clean)"
+
+
 def _timed_launches(run, K, W, dev, flush):
-    """W untimed launches, then K launches each after an L2 flush (a 256 MiB
-    write outside the events), timed with CUDA events on the launching
-    stream.  Returns (per-launch ms list, clocks)."""
+    """W untimed launches, then K launches each after an L2 flush (L2Flush,
+    outside the events), timed with CUDA events on the launching stream.
+    Returns (per-launch ms list, clocks)."""
     stream = torch.cuda.current_stream(dev)
     for _ in range(W):
         run()
@@ -675,7 +694,7 @@ def _part_line(args, world, metric, value, unit, ms_list, dtype, config, rooflin
             "steps": len(ms_list), "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
             "data": "synthetic: seeded N(0,1) values, seeded lengths and scattered block tables",
-            "config": dict(config, l2="256 MiB write before every timed launch"),
+            "config": dict(config, l2=L2_NOTE),
             "roofline": roofline, "gpu_launches": launches * len(ms_list), "clocks": clocks}
     if extra:
         line.update(extra)
@@ -697,7 +716,7 @@ def main_next(args, rank, world, local):
     from paged_kv_attention_21_gb300 import workloads as wl
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     K, W = max(1, args.steps), max(3, args.warmup)
     hbm, hbm_kind = measured_peaks()
     part = args.part

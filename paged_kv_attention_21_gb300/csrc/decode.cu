@@ -56,7 +56,9 @@ template <int D, bool kFp8, int kW = kWarps>
 struct DecodeCfg {
     // bf16 tiles: 2 stages per warp keep ~3 CTAs (12 warps) resident per SM,
     // which measured faster than 3 stages at 2 CTAs; e4m3 tiles are small.
-    static constexpr int kStages = kFp8 ? 3 : 2;
+    // The 2-warp variant runs windows of at most 9 blocks: with e4m3 tiles a
+    // warp's whole share (5 blocks) is in flight after one round of loads.
+    static constexpr int kStages = kFp8 ? (kW < kWarps ? 5 : 3) : 2;
     static constexpr int kElem = kFp8 ? 1 : 2;
     static constexpr int kTileBytes = kBlockSize * D * kElem;  // one block of one head
     static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
