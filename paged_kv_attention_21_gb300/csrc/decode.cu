@@ -40,6 +40,8 @@
 // Roofline: HBM.  Per (block, KV head) the kernel reads 2*16*D*elem bytes
 // and does 4*16*D*G flops, G flop/byte for bf16 -- far below the tensor
 // pipe's ridge, so the design goal is bytes in flight, not MMA rate.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -351,8 +353,9 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
     pa[2] = pack2<kFp8>(p[1][0], p[1][1]);
     pa[3] = pack2<kFp8>(p[1][2], p[1][3]);
 
-    // ---- O += P . V   (V rows masked to zero past the visible range so a
-    // NaN in an unused slot never meets a zero weight inside the MMA)
+    // ---- O += P . V   (V rows outside the visible range are zeroed so that
+    // a NaN in an unused slot never meets a zero weight inside the MMA; with
+    // e4m3 tiles a block whose rows are all visible skips the masking)
     uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
     if (edge) {
         const int t0 = tok_base + 2 * tig;
@@ -361,61 +364,83 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
         keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
         keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
     }
-    if constexpr (kFp8) {
-        // e4m3 V straight from the raw tile.  The B operand pairs two
-        // tokens of one dim; lane (g, tig) takes dims [g D/8, (g+1) D/8)
-        // of V rows 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9 (b1), so
-        // n-tile nt's column of this lane is dim g D/8 + nt.  O's n-tile nt
-        // then holds dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt, which the
-        // combine below puts back in order.
-        constexpr int W = D / 32;  // 32-bit words of a lane's slice of one row
-        uint32_t r0[W], r1[W], r8[W], r9[W];
-        const uint8_t* vb = vtile + g0 * (D / 8);
-        auto row_words = [&](int row, uint32_t (&w)[W]) {
-            if constexpr (W == 2) {
-                const uint2 t = *reinterpret_cast<const uint2*>(vb + row * D);
-                w[0] = t.x;
-                w[1] = t.y;
-            } else {
-                const uint4 t = *reinterpret_cast<const uint4*>(vb + row * D);
-                w[0] = t.x;
-                w[1] = t.y;
-                w[2] = t.z;
-                w[3] = t.w;
+    auto pv = [&](auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
+        if constexpr (kFp8) {
+            // e4m3 V straight from the raw tile.  The B operand pairs two
+            // tokens of one dim; lane (g, tig) takes dims [g D/8, (g+1) D/8)
+            // of V rows 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9 (b1), so
+            // n-tile nt's column of this lane is dim g D/8 + nt.  O's n-tile nt
+            // then holds dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt, which the
+            // combine puts back in order.
+            constexpr int W = D / 32;  // 32-bit words of a lane's slice of one row
+            uint32_t r0[W], r1[W], r8[W], r9[W];
+            const uint8_t* vb = vtile + g0 * (D / 8);
+            auto row_words = [&](int row, uint32_t (&w)[W]) {
+                if constexpr (W == 2) {
+                    const uint2 t = *reinterpret_cast<const uint2*>(vb + row * D);
+                    w[0] = t.x;
+                    w[1] = t.y;
+                } else {
+                    const uint4 t = *reinterpret_cast<const uint4*>(vb + row * D);
+                    w[0] = t.x;
+                    w[1] = t.y;
+                    w[2] = t.z;
+                    w[3] = t.w;
+                }
+            };
+            row_words(2 * tig, r0);
+            row_words(2 * tig + 1, r1);
+            row_words(2 * tig + 8, r8);
+            row_words(2 * tig + 9, r9);
+#pragma unroll
+            for (int nt = 0; nt < NTILES; nt += 2) {
+                // bytes s, s+1 of word nt/4 from both rows of a pair: (a_s, b_s, a_s+1, b_s+1)
+                const uint32_t sel = (nt % 4 == 0) ? 0x5140u : 0x7362u;
+                uint32_t plo, phi;
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(plo) : "r"(r0[nt / 4]), "r"(r1[nt / 4]), "r"(sel));
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(phi) : "r"(r8[nt / 4]), "r"(r9[nt / 4]), "r"(sel));
+                uint32_t b0a, b0b, b1a, b1b;
+                e4m3x4_to_f16x4(plo, b0a, b0b);
+                e4m3x4_to_f16x4(phi, b1a, b1b);
+                if constexpr (kMask) {
+                    b0a &= keep_lo;
+                    b0b &= keep_lo;
+                    b1a &= keep_hi;
+                    b1b &= keep_hi;
+                }
+                mma_16816<true>(o[nt], pa, b0a, b1a);
+                mma_16816<true>(o[nt + 1], pa, b0b, b1b);
             }
-        };
-        row_words(2 * tig, r0);
-        row_words(2 * tig + 1, r1);
-        row_words(2 * tig + 8, r8);
-        row_words(2 * tig + 9, r9);
+        } else {
+            const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int csel = lane >> 4;
 #pragma unroll
-        for (int nt = 0; nt < NTILES; nt += 2) {
-            // bytes s, s+1 of word nt/4 from both rows of a pair: (a_s, b_s, a_s+1, b_s+1)
-            const uint32_t sel = (nt % 4 == 0) ? 0x5140u : 0x7362u;
-            uint32_t plo, phi;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(plo) : "r"(r0[nt / 4]), "r"(r1[nt / 4]), "r"(sel));
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(phi) : "r"(r8[nt / 4]), "r"(r9[nt / 4]), "r"(sel));
-            uint32_t b0a, b0b, b1a, b1b;
-            e4m3x4_to_f16x4(plo, b0a, b0b);
-            e4m3x4_to_f16x4(phi, b1a, b1b);
-            mma_16816<true>(o[nt], pa, b0a & keep_lo, b1a & keep_hi);
-            mma_16816<true>(o[nt + 1], pa, b0b & keep_lo, b1b & keep_hi);
+            for (int j = 0; j < D / 16; ++j) {
+                const int chunk = 2 * j + csel;
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(v0, v1, v2, v3, vaddr + kv_off<D>(tok, chunk));
+                if constexpr (kMask) {
+                    v0 &= keep_lo;
+                    v2 &= keep_lo;
+                    v1 &= keep_hi;
+                    v3 &= keep_hi;
+                }
+                mma_16816<kFp8>(o[2 * j], pa, v0, v1);
+                mma_16816<kFp8>(o[2 * j + 1], pa, v2, v3);
+            }
         }
+    };
+    // The skip pays on e4m3 tiles, where the ALU pipe sets the pace (the
+    // conversions); bf16 tiles keep one masked loop (the second copy cost
+    // the memory-bound bf16 kernel registers and time).
+    if constexpr (kFp8) {
+        if (edge)
+            pv(std::true_type{});
+        else
+            pv(std::false_type{});
     } else {
-        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int csel = lane >> 4;
-#pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-            const int chunk = 2 * j + csel;
-            uint32_t v0, v1, v2, v3;
-            ldmatrix_x4_trans(v0, v1, v2, v3, vaddr + kv_off<D>(tok, chunk));
-            v0 &= keep_lo;
-            v2 &= keep_lo;
-            v1 &= keep_hi;
-            v3 &= keep_hi;
-            mma_16816<kFp8>(o[2 * j], pa, v0, v1);
-            mma_16816<kFp8>(o[2 * j + 1], pa, v2, v3);
-        }
+        pv(std::true_type{});
     }
     (void)vaddr;
 }
