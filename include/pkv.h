@@ -176,7 +176,14 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc *desc, void *k_cache, void *v_ca
  *   workspace: >= pkv_decode_workspace_size(...) bytes, 256-byte aligned,
  *              zero-filled before its first use; every call leaves it
  *              zeroed again.  Calls that share a workspace must not overlap
- *              on the GPU. */
+ *              on the GPU.
+ * Host-resident per-step arrays: with unified addressing (a GB300 and its
+ * Grace host), q, block_tables, context_lens, k_scale, v_scale, sinks, out
+ * and lse_out -- and k_new, v_new of pkv_decode_step -- may be pinned
+ * (page-locked) host memory.  The kernel then reads and writes them over the
+ * host link itself, so a step needs no separate copies; the results are the
+ * same bytes.  The pools, the workspace and rope_cos_sin stay in device
+ * memory. */
 pkv_status pkv_decode_attention(const pkv_cache_desc *desc, const void *q,
                                 const void *k_cache, const void *v_cache,
                                 const float *k_scale, const float *v_scale,

@@ -278,3 +278,36 @@ def test_full_size_decode_step_on_sampled_sequences(cfg, window):
                                           k_scale=ks, v_scale=vs, nthreads=NTHREADS)
     assert_close(out[seqs], ref, "%s decode step, sampled" % spec.name)
     assert_lse_close(lse[seqs], ref_lse, "%s decode step" % spec.name)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_pinned_host_inputs_and_outputs_give_the_same_bytes(fp8):
+    """The per-step arrays (q, k_new, v_new, tables, lengths, out, lse) in
+    pinned host memory, read and written by the kernel over the host link:
+    the cache, out and lse equal the all-device call bit for bit."""
+    hq, hkv, d = (16, 2, 128) if not fp8 else (64, 8, 64)
+    case, k_new, v_new, table = _setup(321 + fp8, LENS, hq, hkv, d, fp8, True)
+    B = len(case.lens)
+    max_ctx = int(case.lens.max())
+    desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=case.k_cache.shape[0],
+                         max_blocks_per_seq=case.tables.shape[1], kv_dtype=1 if fp8 else 0)
+    ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, 0), 256), dtype=torch.uint8,
+                     device=DEV)
+    cs = _dev(table)
+    ks, vs = _dev(case.k_scale), _dev(case.v_scale)
+    results = []
+    for host in (False, True):
+        put = (lambda t: t.cpu().contiguous().pin_memory()) if host else (lambda t: t)
+        q = put(_pool(case.q))
+        kn, vn = put(_pool(k_new)), put(_pool(v_new))
+        tabs, lens = put(_dev(case.tables)), put(_dev(case.lens))
+        kd, vd = _pool(case.k_cache), _pool(case.v_cache)
+        out = put(torch.full((B, hq, d), float("nan"), dtype=torch.bfloat16, device=DEV))
+        lse = put(torch.full((B, hq), float("nan"), device=DEV))
+        pkv.pkv_decode_step(desc, q, kn, vn, kd, vd, tabs, lens, max_ctx, 1 / math.sqrt(d), out, lse, ws,
+                            cos_sin=cs, k_scale=ks, v_scale=vs)
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_errors() == 0
+        results.append((out.cpu(), lse.cpu(), kd.cpu(), vd.cpu()))
+    for a, b in zip(*results):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
