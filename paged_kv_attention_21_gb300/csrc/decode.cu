@@ -465,6 +465,14 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     __shared__ float s_l[kW][16];
     __shared__ int s_flag;
 
+    // Shared-memory set-up touches nothing the previous kernel writes: it
+    // runs before the wait, while that kernel drains.
+    if (threadIdx.x < kW * C::kStages) mbar_init(&bars[threadIdx.x / C::kStages][threadIdx.x % C::kStages], 1);
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        s_flag = 0;
+    }
     pdl_wait();
     pdl_launch_dependents();
     const int split = blockIdx.x;
@@ -483,6 +491,11 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         const int lb = split * a.chunk_blocks + warp + lane * kW;
         if (lane * kW < a.chunk_blocks && lb < a.mbps) phys = bt[lb];
     }
+    // A ring table of at most 32 entries holds every block a window can
+    // touch: read all of it (lane k: entry k) while the length is in flight.
+    const bool ring_lanes = a.ring > 0 && a.ring <= 32;
+    int ring_id = 0;
+    if (ring_lanes && lane < a.ring) ring_id = bt[lane];
     int ctx = a.context_lens[seq];
     // the split plan (and the workspace) covers contexts up to max_ctx, which
     // the host checked against the table capacity
@@ -516,20 +529,19 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const int b1 = min(last_blk + 1, b0 + a.chunk_blocks);
     const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kW - 1) / kW : 0;
 
-    if (threadIdx.x < kW * C::kStages) mbar_init(&bars[threadIdx.x / C::kStages][threadIdx.x % C::kStages], 1);
-    if (threadIdx.x == 0) {
-        tma_prefetch_desc(&kmap);
-        tma_prefetch_desc(&vmap);
-        s_flag = 0;
-    }
     fence_barrier_init();
     __syncthreads();
 
     // Physical block ids of this warp's blocks: lane k holds the k-th one.
     bool bad_id = false;
+    if (ring_lanes) {
+        const int lb = b0 + warp + lane * kW;
+        const int v = __shfl_sync(0xFFFFFFFFu, ring_id, lane < my_n ? lb % a.ring : 0);
+        if (lane < my_n) phys = v;
+    }
     if (lane < my_n) {
         const int lb = b0 + warp + lane * kW;  // logical block
-        if (a.window > 0) phys = bt[a.ring > 0 ? lb % a.ring : lb];
+        if (a.window > 0 && !ring_lanes) phys = bt[a.ring > 0 ? lb % a.ring : lb];
         if (phys < 0 || phys >= a.num_blocks) {
             flag_error(a.err, PKV_DEVERR_BLOCK_ID);
             phys = 0;  // read a valid block; the output is flagged invalid
