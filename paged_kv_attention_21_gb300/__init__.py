@@ -2,9 +2,9 @@
 
 A thin ctypes binding over ``libpkv.so`` (C ABI in ``include/pkv.h``).  Each
 function carries the C entry point's name and only marshals arguments: torch
-tensors become device pointers, the current torch stream becomes the launch
-stream, and a non-OK status raises :class:`PkvError` with the library's
-message.  Every step of the computation runs in the library's kernels; if the
+tensors become pointers (device memory, or pinned host memory where the C
+declaration allows it), the current torch stream becomes the launch stream,
+and a non-OK status raises :class:`PkvError` with the library's message.  Every step of the computation runs in the library's kernels; if the
 library is missing the call fails loudly -- there is no fallback.
 
 PyTorch is used here for device memory and streams only.
@@ -208,7 +208,12 @@ def pkv_decode_step(desc, q, k_new, v_new, k_cache, v_cache, block_tables, conte
                     window=-1, chunk_blocks=0, k_scale=None, v_scale=None, sinks=None, stream=None):
     """One decode step of one layer in one launch: append each sequence's new
     token (k_new, v_new; RoPE'd with cos_sin) at context_lens - 1, rotate q
-    (read only), and attend -- as pkv_append_rope then pkv_decode_attention."""
+    (read only), and attend -- as pkv_append_rope then pkv_decode_attention.
+
+    q, k_new, v_new, block_tables, context_lens, the scales, sinks, out and
+    lse may also be pinned CPU tensors (``tensor.pin_memory()``): the kernel
+    reads and writes them over the host link itself.  The caches, workspace
+    and cos_sin stay on the GPU."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     max_pos = 0 if cos_sin is None else int(cos_sin.shape[0])
     _check(load_library().pkv_decode_step(
