@@ -1034,6 +1034,9 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.fp8 = 0;
         a.num_blocks = desc->num_blocks;
         a.sm_scale = sm_scale;
+        // the suffix pass reads nothing the prefix pass writes: it runs under
+        // the prefix pass's tail and waits for it only before exiting
+        a.defer_wait = 1;
         cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
         if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
     }

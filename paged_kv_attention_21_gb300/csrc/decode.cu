@@ -473,7 +473,17 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         tma_prefetch_desc(&vmap);
         s_flag = 0;
     }
-    pdl_wait();
+    // With defer_wait the grid-dependency wait moves to every exit: the work
+    // overlaps the previous kernel, and this grid still completes only after
+    // it, so kernels after this one see both.
+    struct WaitAtExit {
+        bool on;
+        __device__ ~WaitAtExit() {
+            if (on) pdl_wait();
+        }
+    };
+    const WaitAtExit wait_at_exit{a.defer_wait != 0};
+    if (!a.defer_wait) pdl_wait();
     pdl_launch_dependents();
     const int split = blockIdx.x;
     const int kvh = blockIdx.y;

@@ -106,6 +106,10 @@ struct DecodeArgs {
     const float* cos_sin;   // fp32 [max_pos][d/2][2]
     void* k_pool;           // the pools the tensor maps view, written
     void* v_pool;
+    // defer_wait != 0: the launch reads nothing the previous kernel in the
+    // stream writes (that kernel only waited for its own predecessors), so
+    // it starts without the grid-dependency wait and takes it before exiting
+    int32_t defer_wait;
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
