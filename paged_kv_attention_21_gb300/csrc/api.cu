@@ -946,6 +946,7 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
     const int G = desc->num_q_heads / desc->num_kv_heads;
 
     // part 0: every group's queries over its shared prefix
+    bool prefix_launched = false;
     {
         const int QT = pkv::prefill_tc_q_tile(G);
         CUtensorMap kmap, vmap, qmap;
@@ -993,9 +994,11 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
             a.sq_row_tiles = (max_group * G + 15) / 16;
             cudaError_t e = pkv::launch_short_query(a, tkmap, tvmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
+            prefix_launched = true;
         } else if (a.max_qtiles > 0) {
             cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
+            prefix_launched = true;
         }
     }
     // part 1: each sequence over its own suffix
@@ -1035,8 +1038,9 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.num_blocks = desc->num_blocks;
         a.sm_scale = sm_scale;
         // the suffix pass reads nothing the prefix pass writes: it runs under
-        // the prefix pass's tail and waits for it only before exiting
-        a.defer_wait = 1;
+        // the prefix pass's tail and waits for it only before exiting (the
+        // prefix kernel itself waited for everything before it in the stream)
+        a.defer_wait = prefix_launched ? 1 : 0;
         cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
         if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
     }
