@@ -1,19 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the paged-KV attention hot path on GB300.
 
-Default workload: the Qwen2.5-3B-shaped decode layer -- 64 sequences, 16
-query / 2 KV heads, head_dim 128, block_size 16, bf16 KV ~ N(0,1), context
-lengths uniform in [256, 4096], blocks scattered over a 40,000-block pool.
-One step is one pass of the whole hot path over one batch, in one launch
-per layer (pkv_decode_step): the append of each sequence's new token with
-RoPE (theta 1e6) at position ctx-1 and the rotation of q, fused into
-split-KV GQA decode attention with its planner, block-table gather and
-in-launch merge (``--two-launch`` runs append and decode as two launches).  Four batches over disjoint regions of the pool (572 MB of
-K/V, more than the 129 MB L2) rotate step by step, so no step finds its K/V
-in L2.  The timed steps replay a CUDA graph of the step sequence.
+Default workload: the Llama-3-8B-shaped mixed step -- 32 query / 8 KV heads,
+head_dim 128, block_size 16, bf16 -- the largest workload that fits one GPU.
+One step is one pass of the whole hot path: 120 decode sequences with
+context lengths uniform in [1024, 32768] (append of each sequence's new token
+with RoPE at position ctx-1, the rotation of q, and split-KV GQA decode with
+its planner, block-table gather and in-launch merge: one launch,
+pkv_decode_step), then 8 ragged causal prefill chunks of 512 tokens over
+cached prefixes uniform in [0, 8192] whose pairs share prefix blocks (one
+launch).  The step's 8.3 GB of K/V far exceed the 129 MB L2.  The timed
+steps replay a CUDA graph; K steps form one timed window, and windows repeat
+for at least a second (median, p10, p90).  The Qwen2.5-3B-shaped decode
+step is timed after it and carried in the same line.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-on a bounded sample of the same workload instead.
+``--config 2|3|5`` times another workload's step instead; ``--part`` times
+one part or next-step row on its own.  Prints one JSON line (rank 0).
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload instead.
 """
 from __future__ import annotations
 
@@ -21,7 +25,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import time
@@ -41,12 +44,15 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=40000)
-    p.add_argument("--warmup", type=int, default=256)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
-    p.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
-                   help="workload: 2 Qwen2.5-3B decode (default), 3 Qwen3-4B decode+append, "
-                        "4 Llama-3-8B mixed step, 5 FP8 two-layer decode")
+    p.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5],
+                   help="workload: 4 Llama-3-8B mixed step (default: the largest single-GPU "
+                        "workload), 2 Qwen2.5-3B decode, 3 Qwen3-4B decode+append, 5 FP8 "
+                        "two-layer decode")
+    p.add_argument("--no-carry", action="store_true",
+                   help="skip the Qwen2.5-3B decode figures carried beside the mixed step")
     p.add_argument("--part", choices=["step", "prefill", "cascade", "verify", "cow", "ring",
                                       "fp8-prefill"], default="step",
                    help="step: the workload's whole step (default); prefill: the ragged causal "
@@ -118,14 +124,20 @@ def measured_peaks():
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
-def measured_tensor_peak():
-    """Dense bf16 TFLOP/s for a kernel timed alone (the burst figure)."""
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def measured_tensor_peak(sustained=False):
+    """Dense bf16 TFLOP/s: the burst figure (a kernel timed alone), or the
+    sustained one (a kernel timed inside a long step)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["bf16_tflops"]), "measured"
-    return FALLBACK_BF16_TFLOPS, "fallback"
+        if key in d:
+            return float(d[key]), "measured"
+    return (FALLBACK_BF16_TFLOPS_SUSTAINED if sustained else FALLBACK_BF16_TFLOPS), "fallback"
 
 
 class ClockSampler:
@@ -180,20 +192,28 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def decode_traffic_per_launch(config):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.md")
-    src = os.path.join(ROOT, "paged_kv_attention_21_gb300", "csrc", "decode.cu")
-    if not os.path.exists(path):
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {"decode_kernel": "decode.cu", "prefill_tc_kernel": "prefill_tc.cu"}
+
+
+def kernel_traffic_per_launch(kernel, config):
+    """DRAM bytes (read + write) per launch of `kernel` on workload `config`
+    from profiles/traffic.json (machine-readable; the ncu summaries beside it
+    explain the figures), if they were taken on the current kernel source
+    (else None)."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
+    with open(TRAFFIC_JSON) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "paged_kv_attention_21_gb300", "csrc", KERNEL_SOURCES[kernel])
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    text = open(path).read()
-    m = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
-    t = re.search(r"config%d_dram_bytes_per_launch:\s*([0-9.eE+]+)" % config, text)
-    if not m or not t or m.group(1) != sha:
+    if ent.get("source_sha256_16") != sha:
         return None
-    return float(t.group(1))
+    v = ent.get("dram_bytes_per_launch", {}).get(str(config))
+    return None if v is None else float(v)
 
 
 # ------------------------------------------------------------- workloads --
@@ -269,9 +289,10 @@ class DecodeWorkload:
     def tokens(self, i):
         return self.spec.batch + (self.prefill.tokens if self.prefill is not None else 0)
 
-    def step(self, i, ev_pairs=None):
+    def step(self, i, ev_pairs=None, pev=None):
         """Launch one step for instance i; ev_pairs (list of (start, end)) are
-        recorded around each decode launch.  Returns the launch count."""
+        recorded around each decode launch, pev around the prefill launch.
+        Returns the launch count."""
         pkv = self.pkv
         n = 0
         for li, (layer, w) in enumerate(zip(self.layers, self.windows)):
@@ -302,7 +323,11 @@ class DecodeWorkload:
                 ev_pairs[li][1].record()
             n += 2
         if self.prefill is not None:
+            if pev is not None:
+                pev[0].record()
             self.prefill.run()
+            if pev is not None:
+                pev[1].record()
             n += 1
         return n
 
@@ -338,14 +363,35 @@ class PrefillPart:
 
 # ---------------------------------------------------------------- timing --
 
-def time_pkv(args, rank, world, local):
+def graph_len(K, n_inst):
+    """Steps per captured graph: a divisor of K (so the timed steps are
+    exactly K), at most 64, and at least the instance count when K allows."""
+    best = 1
+    for r in range(1, min(K, 64) + 1):
+        if K % r == 0:
+            best = r
+    return best
+
+
+def time_pkv(args, rank, world, local, config=None, steps=None, min_seconds=2.0,
+             with_e2e=True):
+    """Time one workload's step as replays of a captured CUDA graph.
+
+    A window is exactly K steps, bracketed by CUDA events on the launching
+    stream (after a barrier and a synchronize); windows repeat back to back
+    until at least `min_seconds` have passed (and at least 3 windows).  The
+    step time is the median window (max over ranks), with p10 / p90 beside it.
+    CUDA events inside the graph bracket the decode launch (and the prefill
+    launch of the mixed step) of every `stride`-th step; they give the
+    per-kernel launch times the rooflines use."""
     import paged_kv_attention_21_gb300 as pkv
+    config = args.config if config is None else config
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    W = DecodeWorkload(args.config, dev, rank, fused=not args.two_launch, chunk=args.chunk_blocks)
-    K, Wm = args.steps, max(3, args.warmup)
-    R = 64 if W.n_inst > 1 else 8          # steps per captured graph
-    R = max(W.n_inst, min(R, K))
+    W = DecodeWorkload(config, dev, rank, fused=not args.two_launch, chunk=args.chunk_blocks)
+    K = max(1, args.steps if steps is None else steps)
+    Wm = max(3, args.warmup)
+    R = graph_len(K, W.n_inst)
     nlayers = len(W.layers)
 
     # eager warm-up of every instance (first calls set up device state)
@@ -354,82 +400,141 @@ def time_pkv(args, rank, world, local):
     torch.cuda.synchronize()
     pkv.pkv_device_errors(reset=True)
 
-    # capture R steps with external timing events around each decode launch
-    # Timing events sit around the decode launches of every `stride`-th step
-    # only (a stride coprime with the instance count, so every instance is
-    # sampled): an event between two launches breaks their programmatic
-    # dependent launch, so the other steps keep back-to-back launches.
+    # Timing events sit around the decode launches (and the prefill launch) of
+    # every `stride`-th step only (a stride coprime with the instance count,
+    # so every instance is sampled): an event between two launches breaks
+    # their programmatic dependent launch, so the other steps keep
+    # back-to-back launches.
     stride = 2 * W.n_inst + 1
     sampled = list(range(0, R, stride))
-    evs = {j: [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nlayers)]
-           for j in sampled}
+    mk = lambda: (torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True))
+    evs = {j: [mk() for _ in range(nlayers)] for j in sampled}
+    pevs = {j: mk() for j in sampled} if W.prefill is not None else {}
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     launches_per_replay = 0
     with torch.cuda.graph(graph, stream=cap):
         for j in range(R):
-            launches_per_replay += W.step(j % W.n_inst, evs.get(j))
+            launches_per_replay += W.step(j % W.n_inst, evs.get(j), pevs.get(j))
     torch.cuda.synchronize()
-    replays = max(1, K // R)
-    K_eff = replays * R
-    # warm-up replays, then the eager remainder so warmup >= W steps
-    sampler = ClockSampler(local)
-    for _ in range(max(1, Wm // R)):
+    replays = K // R
+    for _ in range(max(1, -(-Wm // R))):   # warm-up replays: >= W steps
         graph.replay()
     torch.cuda.synchronize()
 
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    win_ms, dec_ms, pre_ms = [], [[] for _ in range(nlayers)], []
+    sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    start.record()
-    for _ in range(replays):
-        graph.replay()
-    end.record()
+    while True:
+        start.record()
+        for _ in range(replays):
+            graph.replay()
+        end.record()
+        end.synchronize()
+        win_ms.append(start.elapsed_time(end))
+        # the events of the window's last replay
+        for j in sampled:
+            for li in range(nlayers):
+                dec_ms[li].append(evs[j][li][0].elapsed_time(evs[j][li][1]))
+            if pevs:
+                pre_ms.append(pevs[j][0].elapsed_time(pevs[j][1]))
+        wall = time.perf_counter() - t0
+        if len(win_ms) >= 3 and (wall >= min_seconds or len(win_ms) >= 2000):
+            break
     torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
     barrier(world)
     clocks = sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
     err = pkv.pkv_device_errors(reset=True)
     if err:
         raise RuntimeError("device error word 0x%x after the timed region" % err)
 
-    # the dominant kernel: decode, timed by the events of the last replay
-    dec_ms = [[evs[j][li][0].elapsed_time(evs[j][li][1]) for j in sampled]
-              for li in range(nlayers)]
+    n_samp = len(sampled)
     dec_bytes = [[W.layers[li][j % W.n_inst].kv_bytes(W.windows[li]) for j in sampled]
                  for li in range(nlayers)]
-    # the layer with the most bytes is the dominant launch
-    li_dom = int(np.argmax([sum(x) for x in dec_bytes]))
+    li_dom = int(np.argmax([sum(x) for x in dec_bytes]))   # the layer with the most bytes
     dom_ms = float(np.mean(dec_ms[li_dom]))
     dom_bytes = float(np.mean(dec_bytes[li_dom]))
+    # per-launch byte-weighted rate over every sampled launch of every window
+    reps = len(win_ms)
+    samp_bytes = np.tile(np.array(dec_bytes[li_dom], dtype=np.float64), reps)
+    per_launch_gbs = samp_bytes / (np.array(dec_ms[li_dom]) / 1e3) / 1e9
 
-    bytes_per_rank = sum(W.kv_bytes(j % W.n_inst) for j in range(K_eff))
-    tokens_per_rank = sum(W.tokens(j % W.n_inst) for j in range(K_eff))
-    t_max = reduce_max(elapsed_ms / 1e3, world)
-    total_bytes = reduce_sum(bytes_per_rank, world)
-    total_tokens = reduce_sum(tokens_per_rank, world)
-    e2e = time_e2e(W, dev, min(K_eff, 512))
-    e2e_val = reduce_sum(e2e["bytes"], world) / reduce_max(e2e["seconds"], world) / 1e9
-    if e2e["direct"] is not None:
-        e2e["direct_val"] = (reduce_sum(e2e["direct"]["bytes"], world) /
-                             reduce_max(e2e["direct"]["seconds"], world) / 1e9)
-    return dict(W=W, K=K_eff, R=R, elapsed_s=t_max, wall_s=wall, total_bytes=total_bytes,
-                ev_stride=stride, ev_launches=len(sampled) * replays,
-                total_tokens=total_tokens, dom_ms=dom_ms, dom_bytes=dom_bytes,
-                dom_layer=li_dom, dec_ms=dec_ms, clocks=clocks,
-                launches=launches_per_replay * replays, e2e=e2e, e2e_val=e2e_val)
+    med_ms = float(np.median(win_ms))
+    bytes_per_window = sum(W.kv_bytes(j % W.n_inst) for j in range(K))
+    tokens_per_window = sum(W.tokens(j % W.n_inst) for j in range(K))
+    t_max = reduce_max(med_ms / 1e3, world)
+    total_bytes = reduce_sum(bytes_per_window, world)
+    total_tokens = reduce_sum(tokens_per_window, world)
+    res = dict(W=W, K=K, R=R, elapsed_s=t_max, wall_s=wall, total_bytes=total_bytes,
+               ev_stride=stride, total_tokens=total_tokens, dom_ms=dom_ms, dom_bytes=dom_bytes,
+               dom_layer=li_dom, dec_ms=dec_ms, clocks=clocks, windows=len(win_ms),
+               win_p10=float(np.percentile(win_ms, 10)), win_p90=float(np.percentile(win_ms, 90)),
+               dec_p10=float(np.percentile(dec_ms[li_dom], 10)),
+               dec_p90=float(np.percentile(dec_ms[li_dom], 90)),
+               per_launch_gbs=float(np.median(per_launch_gbs)),
+               launches=launches_per_replay * replays * len(win_ms),
+               launches_per_step=launches_per_replay / R)
+    if pre_ms:
+        res.update(pre_ms=float(np.mean(pre_ms)), pre_p10=float(np.percentile(pre_ms, 10)),
+                   pre_p90=float(np.percentile(pre_ms, 90)))
+    if with_e2e:
+        e2e = time_e2e(W, dev, max(20, min(K, 256)))
+        res["e2e"] = e2e
+        res["e2e_val"] = reduce_sum(e2e["bytes"], world) / reduce_max(e2e["seconds"], world) / 1e9
+        if e2e["direct"] is not None:
+            e2e["direct_val"] = (reduce_sum(e2e["direct"]["bytes"], world) /
+                                 reduce_max(e2e["direct"]["seconds"], world) / 1e9)
+    return res
+
+
+class PrefillHostIO:
+    """The prefill part's per-step inputs (q, qo_indptr, kv_lens, block
+    tables) in one pinned host buffer with 256-byte aligned fields, copied
+    to a device buffer of the same layout; its output read back into pinned
+    host memory."""
+
+    def __init__(self, P, dev):
+        pb = P.pb
+        self.P = P
+        src = {"q": pb.q, "qo_indptr": pb.qo_indptr, "kv_lens": pb.kv_lens,
+               "block_tables": pb.block_tables}
+        offs, total = {}, 0
+        for k, t in src.items():
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for k, t in src.items():
+            n = t.numel() * t.element_size()
+            self.host[offs[k]:offs[k] + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+        self.dev_all = torch.empty(total, dtype=torch.uint8, device=dev)
+        self.buf = {k: self.dev_all[offs[k]:offs[k] + t.numel() * t.element_size()]
+                    .view(t.dtype).view(t.shape) for k, t in src.items()}
+        self.out_h = torch.empty(P.out.shape, dtype=P.out.dtype).pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for t in src.values())
+        self.d2h = self.out_h.numel() * self.out_h.element_size()
+
+    def step(self):
+        P, b = self.P, self.buf
+        self.dev_all.copy_(self.host, non_blocking=True)
+        P.pkv.pkv_prefill_attention_ragged(P.desc, b["q"], b["qo_indptr"], P.pb.k_cache,
+                                           P.pb.v_cache, b["block_tables"], b["kv_lens"],
+                                           P.spec.sm_scale, P.out,
+                                           qo_indptr_host=P.pb.qo_indptr_host,
+                                           kv_lens_host=P.pb.kv_lens_host)
+        self.out_h.copy_(P.out, non_blocking=True)
 
 
 def time_e2e(W, dev, steps):
     """The same step through the public API with host buffers: each step
-    copies its inputs from pinned host memory (one copy of one packed buffer),
-    runs the decode step (append + decode), and reads the output back to the
-    host."""
+    copies its inputs from pinned host memory (one copy of one packed buffer
+    per part), runs the decode step (append + decode) and, in the mixed step,
+    the prefill, and reads the outputs back to the host."""
     pkv = W.pkv
     # A step's inputs sit in one pinned host buffer (256-byte aligned fields)
     # and go over in one copy into one device buffer with the same layout.
@@ -454,8 +559,9 @@ def time_e2e(W, dev, steps):
         nbytes = t.numel() * t.element_size()
         devbuf[k] = dev_all[offs[k]:offs[k] + nbytes].view(t.dtype).view(t.shape)
     out_h = torch.empty(W.out.shape, dtype=W.out.dtype).pin_memory()
-    h2d = sum(src0[k].numel() * src0[k].element_size() for k in names)
-    d2h = out_h.numel() * out_h.element_size()
+    pio = PrefillHostIO(W.prefill, dev) if W.prefill is not None else None
+    h2d = sum(src0[k].numel() * src0[k].element_size() for k in names) + (pio.h2d if pio else 0)
+    d2h = out_h.numel() * out_h.element_size() + (pio.d2h if pio else 0)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream  # the raw handle, passed to the API calls
 
@@ -485,9 +591,9 @@ def time_e2e(W, dev, steps):
                                      devbuf["block_tables"], devbuf["context_lens"], W.max_ctx,
                                      W.spec.sm_scale, W.out, None, W.ws, window=w,
                                      chunk_blocks=W.chunk, k_scale=b.k_scale, v_scale=b.v_scale)
-        if W.prefill is not None:
-            W.prefill.run()
         out_h.copy_(W.out, non_blocking=True)
+        if pio is not None:
+            pio.step()
         stream.synchronize()   # the host reads the step's result
 
     for i in range(8):
@@ -501,10 +607,11 @@ def time_e2e(W, dev, steps):
     if not W.fused:
         return res
 
-    # The same step with the per-step arrays left in pinned host memory: the
-    # decode step reads q, k_new, v_new, the tables and lengths over the host
-    # link and writes the output into pinned host memory (no copy-engine
-    # transfers), then the host syncs and reads the output.
+    # The same step with the decode's per-step arrays left in pinned host
+    # memory: the decode step reads q, k_new, v_new, the tables and lengths
+    # over the host link and writes the output into pinned host memory (no
+    # copy-engine transfers); the prefill part of a mixed step still copies
+    # its inputs in and its output out.  Then the host syncs and reads.
     views = []
     for hb in host:
         views.append({k: hb[offs[k]:offs[k] + src0[k].numel() * src0[k].element_size()]
@@ -522,8 +629,8 @@ def time_e2e(W, dev, steps):
     def step_direct(i):
         for li in range(len(W.layers)):
             direct[(i % W.n_inst, li)]()
-        if W.prefill is not None:
-            W.prefill.run()
+        if pio is not None:
+            pio.step()
         stream.synchronize()   # the host reads the step's result (already in out_h)
 
     for i in range(8):
@@ -535,7 +642,7 @@ def time_e2e(W, dev, steps):
     return res
 
 
-def e2e_line(e, copy_val):
+def e2e_line(e, copy_val, mixed=False):
     """The e2e object of the bench line.  Both variants move every step's
     inputs host -> device and its output device -> host inside the timed
     step; the headline is the faster public-API path, the other sits beside
@@ -546,6 +653,10 @@ def e2e_line(e, copy_val):
                       "bind_decode_step), D2H of the output (copy engine), host sync"}
     base = {"unit": "GB/s", "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
             "steps": e["steps"]}
+    if mixed:
+        base["prefill_part"] = ("each step also copies the prefill part's q, qo_indptr, kv_lens "
+                                "and block tables H2D (one packed pinned buffer, copy engine), "
+                                "runs the ragged prefill, and copies its output D2H")
     if e.get("direct_val") is None:
         return dict(base, value=copies["value"], note=copies["note"])
     return dict(base, value=round(e["direct_val"], 2),
@@ -973,6 +1084,34 @@ def main_next(args, rank, world, local):
                2, clocks)
 
 
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (~8 TB/s)
+
+MIXED_STEP_NAME = ("Llama-3-8B-shaped mixed step: 120 decodes (ctx 1024-32768) + 8x512-token "
+                   "causal prefill chunks over cached prefixes 0-8192, 32/8 heads, D128, bf16")
+
+
+def workload_name(config):
+    from paged_kv_attention_21_gb300 import workloads as wl
+    return MIXED_STEP_NAME if config == 4 else wl.CONFIGS[config].name
+
+
+def decode_roofline(r, peak, peak_kind, fused, config):
+    achieved = r["dom_bytes"] / (r["dom_ms"] / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": kernel_traffic_per_launch("decode_kernel", config),
+            "kernel": ("decode_kernel (append+RoPE, split-KV GQA decode and merge, one launch)"
+                       if fused else "decode_kernel (split-KV GQA decode, merge fused)"),
+            "peak_source": "%s hbm_gbs" % peak_kind,
+            "algorithmic_bytes_per_launch": int(r["dom_bytes"]),
+            "avg_launch_ms": round(r["dom_ms"], 5),
+            "p10_launch_ms": round(r["dec_p10"], 5), "p90_launch_ms": round(r["dec_p90"], 5),
+            "median_launch_gbs": round(r["per_launch_gbs"], 1),
+            "timed_by": "CUDA events around the decode launch of every %d-th step of every "
+                        "timed window's last graph replay" % r["ev_stride"]}
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args.gpus)
@@ -983,12 +1122,18 @@ def main():
     if args.part != "step":
         return main_next(args, rank, world, local)
     r = time_pkv(args, rank, world, local)
+    carry = None
+    if args.config == 4 and not args.no_carry:
+        # the Qwen2.5-3B-shaped decode step, carried beside the headline: its
+        # short (~30 us) launches show the start-up and tail costs
+        carry = time_pkv(args, rank, world, local, config=2, steps=640, min_seconds=0.5,
+                         with_e2e=False)
     if rank != 0:
         return
     W = r["W"]
     peak, peak_kind = measured_peaks()
     value = r["total_bytes"] / r["elapsed_s"] / 1e9
-    achieved = r["dom_bytes"] / (r["dom_ms"] / 1e3) / 1e9
+    roof = decode_roofline(r, peak, peak_kind, W.fused, args.config)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -997,35 +1142,68 @@ def main():
         "steps": r["K"],
         "warmup": max(3, args.warmup),
         "ms_per_step": round(r["elapsed_s"] * 1e3 / r["K"], 5),
+        "ms_per_step_p10": round(r["win_p10"] / r["K"], 5),
+        "ms_per_step_p90": round(r["win_p90"] / r["K"], 5),
+        "windows": r["windows"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16" if W.spec.kv_dtype == "bf16" else "e4m3 KV, bf16 q/o, fp32 accumulate",
         "data": "synthetic: seeded N(0,1) K/V/q, uniform context lengths, scattered block tables",
-        "config": workload_config(W),
+        "config": workload_config(W, {"workload": workload_name(args.config),
+                                      "timing": "%d back-to-back windows of %d steps (CUDA "
+                                                "events, graph replays); ms_per_step is the "
+                                                "median window" % (r["windows"], r["K"])}),
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
+        "pct_nominal_hbm": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "attention_tokens_per_s": round(r["total_tokens"] / r["elapsed_s"], 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": decode_traffic_per_launch(args.config),
-                     "kernel": ("decode_kernel (append+RoPE, split-KV GQA decode and merge, "
-                                "one launch)" if W.fused else
-                                "decode_kernel (split-KV GQA decode, merge fused)"),
-                     "peak_source": "%s hbm_gbs" % peak_kind,
-                     "algorithmic_bytes_per_launch": int(r["dom_bytes"]),
-                     "avg_launch_ms": round(r["dom_ms"], 5),
-                     "timed_by": "CUDA events around the decode launch of every %d-th step of "
-                                 "the timed graph replays" % r["ev_stride"]},
-        "e2e": e2e_line(r["e2e"], r["e2e_val"]),
+        "roofline": roof,
+        "e2e": e2e_line(r["e2e"], r["e2e_val"], W.prefill is not None),
         "gpu_launches": r["launches"],
+        "gpu_launches_per_step": r["launches_per_step"],
         "clocks": r["clocks"],
     }
+    roof["decode"] = {k: v for k, v in roof.items() if k != "decode"}
     if W.prefill is not None:
-        line["prefill"] = {"tokens": W.prefill.tokens, "flops": W.prefill.flops}
+        tpeak, tkind = measured_tensor_peak()
+        tsus, _ = measured_tensor_peak(sustained=True)
+        P = W.prefill
+        tflops = P.flops / (r["pre_ms"] / 1e3) / 1e12
+        roof["prefill"] = {
+            "bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak, "unit": "TFLOP/s",
+            "frac": round(tflops / tpeak, 4), "frac_of_sustained": round(tflops / tsus, 4),
+            "traffic": kernel_traffic_per_launch("prefill_tc_kernel", 4),
+            "kernel": "prefill_tc_kernel (tcgen05, two query tiles per CTA)",
+            "peak_source": "%s bf16_tflops (burst); frac_of_sustained against "
+                           "bf16_tflops_sustained" % tkind,
+            "algorithmic_flops_per_launch": int(P.flops),
+            "avg_launch_ms": round(r["pre_ms"], 5),
+            "p10_launch_ms": round(r["pre_p10"], 5), "p90_launch_ms": round(r["pre_p90"], 5),
+            "timed_by": "CUDA events around the prefill launch of every %d-th step of every "
+                        "timed window's last graph replay" % r["ev_stride"]}
+        line["prefill"] = {"tokens": P.tokens, "flops": P.flops, "kv_bytes": P.kv_bytes}
+    if carry is not None:
+        cW = carry["W"]
+        cv = carry["total_bytes"] / carry["elapsed_s"] / 1e9
+        croof = decode_roofline(carry, peak, peak_kind, cW.fused, 2)
+        line["qwen25_3b_decode"] = {
+            "workload": workload_name(2), "value": round(cv, 2), "unit": "GB/s",
+            "steps": carry["K"], "windows": carry["windows"],
+            "ms_per_step": round(carry["elapsed_s"] * 1e3 / carry["K"], 5),
+            "frac_per_step": round(cv / world / peak, 4),
+            "frac_per_launch": croof["frac"], "avg_launch_ms": croof["avg_launch_ms"],
+            "median_launch_gbs": croof["median_launch_gbs"],
+            "algorithmic_bytes_per_launch": croof["algorithmic_bytes_per_launch"],
+            "traffic": croof["traffic"],
+            "l2": "4 batches over disjoint pool regions rotate step by step"}
     if not args.no_cpu_baseline:
-        v, desc, thr = oracle_sample(W, args.cpu_seconds, os.cpu_count() or 1)
+        ncores = os.cpu_count() or 1
+        v, desc, thr = oracle_sample(W, args.cpu_seconds, ncores)
+        v1, desc1, _ = oracle_sample(W, max(2.0, args.cpu_seconds / 3), 1)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": thr,
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc,
+                                "single_core": {"value": round(v1, 4), "unit": "GB/s",
+                                                "cores": 1, "sample": desc1}}
     print(json.dumps(line), flush=True)
 
 
@@ -1089,14 +1267,14 @@ def main_reference(args, rank, world, local):
         ntok += nt
     sec = time.perf_counter() - t0
     value = nbytes / sec / 1e9
-    sample = ("per step %d of the first %d sequences of one %s batch (all query heads)"
+    sample = ("per step %d of the first %d decode sequences of one %s batch (all query heads)"
               % (nseq_step, nseq, spec.name))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": round(sec * 1e3 / max(1, args.steps), 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic: the same seeded workload", "config": {
-                "workload": spec.name, "sample": sample},
+                "workload": workload_name(args.config), "sample": sample},
             "attention_tokens_per_s": round(ntok / sec, 2),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
                              "kind": "oracle", "sample": sample},

@@ -340,10 +340,13 @@ size_t pkv_cascade_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
- *   - Every call shares the one array and it keeps the last call's contents;
- *     the call clears the merge tickets it needs on `stream` before the
- *     kernel.  Calls that overlap on the GPU (different streams, or several
- *     host threads) race on the array: serialise them.
+ *   - Every call shares the one array and it keeps the last call's contents.
+ *     A plan of more than four chunks per (sequence, KV head) merges through
+ *     tickets kept in the array: such a call first clears them on `stream`
+ *     (cudaMemsetAsync, which allocates nothing).  Plans of two to four
+ *     chunks merge in shared memory and one-chunk plans need no scratch.
+ *     Calls that overlap on the GPU (different streams, or several host
+ *     threads) race on the array: serialise them.
  * Arguments are those of pkv_decode_attention without workspace and
  * workspace_bytes. */
 pkv_status pkv_decode_attention_static(const pkv_cache_desc *desc, const void *q,
@@ -358,6 +361,19 @@ pkv_status pkv_decode_attention_static(const pkv_cache_desc *desc, const void *q
 
 /* Message for the last non-OK status on this thread ("" if none). */
 const char *pkv_last_error(void);
+
+/* Testing only (no counterpart on the pages): make the library's bounded
+ * waits give up on purpose, to exercise their failure path without a fault.
+ * kernels: bit 0 arms the decode kernel (pkv_decode_attention / _step /
+ * _static), bit 1 the tcgen05 prefill kernel; 0 disarms (the default).
+ * While armed, every launch of those kernels replaces the first pipeline wait
+ * of one warp of its first CTA by a wait on a barrier that nothing arrives
+ * on, which gives up after limit_us (1 .. 1000000).  The kernel then drains
+ * the copies and MMAs it issued (they all complete), sets
+ * PKV_DEVERR_TIMEOUT, writes o = 0 / lse = -inf for the affected state and
+ * returns; every merge ticket is left at zero.  Process-wide, not for use
+ * in production. */
+pkv_status pkv_test_inject_wait_timeout(int32_t kernels, uint32_t limit_us);
 
 /* Host, synchronous: copy the current device's error word (PKV_DEVERR_*
  * bits set by kernels since the last reset) to *flags_out; reset != 0

@@ -102,6 +102,7 @@ def load_library():
             "pkv_copy_blocks": (ctypes.c_int, [D, P, P, P, P, i32, P]),
             "pkv_last_error": (ctypes.c_char_p, []),
             "pkv_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32]),
+            "pkv_test_inject_wait_timeout": (ctypes.c_int, [i32, ctypes.c_uint32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -323,6 +324,12 @@ def pkv_device_errors(reset: bool = True) -> int:
     v = ctypes.c_uint32()
     _check(load_library().pkv_device_errors(ctypes.byref(v), int(bool(reset))))
     return int(v.value)
+
+
+def pkv_test_inject_wait_timeout(kernels: int, limit_us: int = 0) -> None:
+    """Testing only: arm (kernels bit 0 decode, bit 1 tcgen05 prefill) or
+    disarm (0) the library's give-up path of one bounded wait per launch."""
+    _check(load_library().pkv_test_inject_wait_timeout(int(kernels), int(limit_us)))
 
 
 def pkv_last_error() -> str:

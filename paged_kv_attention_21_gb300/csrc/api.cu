@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/pkv.h"
@@ -28,6 +29,11 @@ __device__ uint32_t g_pkv_device_error;
 namespace {
 
 thread_local char g_last_error[512] = "";
+
+// Test hook (pkv_test_inject_wait_timeout): bit 0 arms the decode kernel,
+// bit 1 the tcgen05 prefill kernel; off (0) unless a test sets it.
+std::atomic<int32_t> g_inject_kernels{0};
+std::atomic<uint32_t> g_inject_limit_us{0};
 
 pkv_status fail(pkv_status st, const char* fmt, ...) {
     va_list ap;
@@ -449,12 +455,19 @@ struct StepIn {
     int32_t max_pos;
 };
 
+// Where the decode's split states live: the caller's workspace, or the
+// library's fixed scratch array (pkv_decode_attention_static).
+enum class Scratch { kCaller, kStatic };
+
+pkv_status static_scratch(void** out, size_t* bytes);
+
 pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_cache,
                        const void* v_cache, const float* k_scale, const float* v_scale,
                        const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
                        int32_t max_context_len, float sm_scale, int32_t window, const float* sinks,
                        int32_t chunk_blocks, void* out, float* lse_out, void* workspace,
-                       size_t workspace_bytes, pkv_stream_t stream, const StepIn* step) {
+                       size_t workspace_bytes, pkv_stream_t stream, const StepIn* step,
+                       Scratch scratch = Scratch::kCaller) {
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
@@ -490,6 +503,17 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
     st = plan_decode(desc, num_seqs, max_context_len, window, sms, chunk_blocks, &chunk, &splits);
     if (st != PKV_OK) return st;
     const DecodeWs ws = decode_ws_layout(desc, num_seqs, splits);
+    if (scratch == Scratch::kStatic) {
+        size_t cap = 0;
+        st = static_scratch(&workspace, &cap);
+        if (st != PKV_OK) return st;
+        if (ws.total > cap)
+            return fail(PKV_ERR_WORKSPACE,
+                        "this batch needs %zu bytes of decode scratch, more than the %zu-byte static "
+                        "array; use pkv_decode_attention with a workspace, or a larger chunk_blocks",
+                        ws.total, cap);
+        workspace_bytes = cap;
+    }
     if (ws.total > 0) {
         if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", ws.total);
         if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -501,6 +525,15 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
     if (st != PKV_OK) return st;
     st = pool_map(v_cache, desc, &vmap, kMapTileRows);
     if (st != PKV_OK) return st;
+    if (scratch == Scratch::kStatic && ws.total > 0 && pkv::decode_uses_tickets(splits)) {
+        // The static array keeps whatever the last call left there, which may
+        // be another layout's partial states: a plan that merges through
+        // tickets clears them first (cluster plans never read them).
+        const size_t pairs = size_t(num_seqs) * desc->num_kv_heads;
+        cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + ws.counters, 0,
+                                        pairs * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "clear static decode tickets");
+    }
     pkv::DecodeArgs a{};
     a.q = q;
     a.out = out;
@@ -529,6 +562,8 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
     a.fp8 = fp8 ? 1 : 0;
     a.num_blocks = desc->num_blocks;
     a.sm_scale = sm_scale;
+    a.inject_timeout = g_inject_kernels.load() & 1;
+    a.inject_limit_us = g_inject_limit_us.load();
     if (step) {
         a.k_new = step->k_new;
         a.v_new = step->v_new;
@@ -728,6 +763,8 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     CUtensorMap qmap;
     st = q_map(q, total_q_tokens, desc, G, QT, &qmap);
     if (st != PKV_OK) return st;
+    a.inject_timeout = (g_inject_kernels.load() >> 1) & 1;
+    a.inject_limit_us = g_inject_limit_us.load();
     cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PKV_OK;
@@ -1051,6 +1088,16 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
     return PKV_OK;
 }
 
+pkv_status pkv_test_inject_wait_timeout(int32_t kernels, uint32_t limit_us) {
+    g_last_error[0] = 0;
+    if (kernels < 0 || kernels > 3) return fail(PKV_ERR_INVALID_ARG, "kernels mask %d outside [0, 3]", kernels);
+    if (kernels && (limit_us < 1 || limit_us > 1000000))
+        return fail(PKV_ERR_INVALID_ARG, "limit_us %u outside [1, 1000000]", limit_us);
+    g_inject_limit_us.store(limit_us);
+    g_inject_kernels.store(kernels);
+    return PKV_OK;
+}
+
 pkv_status pkv_device_errors(uint32_t* flags_out, int32_t reset) {
     g_last_error[0] = 0;
     if (!flags_out) return fail(PKV_ERR_INVALID_ARG, "flags_out is NULL");
@@ -1092,7 +1139,7 @@ void* g_static_ptr[kMaxDevices] = {};
 // Device address of the scratch array on the current device, looked up once
 // per device with that device current.  In host code the array's name is
 // only a host-side stand-in, so the address must come from the runtime.
-pkv_status static_scratch(void** out) {
+pkv_status static_scratch(void** out, size_t* bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -1105,6 +1152,7 @@ pkv_status static_scratch(void** out) {
         g_static_ptr[dev] = p;
     }
     *out = g_static_ptr[dev];
+    *bytes = kStaticScratchBytes;
     return PKV_OK;
 }
 
@@ -1116,78 +1164,7 @@ extern "C" pkv_status pkv_decode_attention_static(
     const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float sm_scale,
     int32_t window, const float* sinks, int32_t chunk_blocks, void* out, float* lse_out,
     pkv_stream_t stream) {
-    g_last_error[0] = 0;
-    pkv_status st = check_desc(desc);
-    if (st != PKV_OK) return st;
-    if (num_seqs < 0 || num_seqs > 65535)
-        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
-    if (num_seqs == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
-    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
-    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
-    st = check_ring_window(desc, window, max_context_len);
-    if (st != PKV_OK) return st;
-    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
-        return fail(PKV_ERR_INVALID_ARG, "q, out and the pools must be 16-byte aligned");
-    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
-    uint32_t* err = nullptr;
-    int sms = 0;
-    st = device_state(&err, &sms);
-    if (st != PKV_OK) return st;
-    int chunk = 0, splits = 0;
-    st = plan_decode(desc, num_seqs, max_context_len, window, sms, chunk_blocks, &chunk, &splits);
-    if (st != PKV_OK) return st;
-    const DecodeWs ws = decode_ws_layout(desc, num_seqs, splits);
-    if (ws.total > kStaticScratchBytes)
-        return fail(PKV_ERR_WORKSPACE,
-                    "this batch needs %zu bytes of decode scratch, more than the %zu-byte static "
-                    "array; use pkv_decode_attention with a workspace, or a larger chunk_blocks",
-                    ws.total, kStaticScratchBytes);
-    void* scratch = nullptr;
-    st = static_scratch(&scratch);
-    if (st != PKV_OK) return st;
-    CUtensorMap kmap, vmap;
-    st = pool_map(k_cache, desc, &kmap, kMapTileRows);
-    if (st != PKV_OK) return st;
-    st = pool_map(v_cache, desc, &vmap, kMapTileRows);
-    if (st != PKV_OK) return st;
-    uint8_t* wsb = static_cast<uint8_t*>(scratch);
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (ws.total > 0) {
-        // the tickets must start at zero; the array keeps whatever the last call left
-        const size_t pairs = size_t(num_seqs) * desc->num_kv_heads;
-        cudaError_t e = cudaMemsetAsync(wsb + ws.counters, 0, pairs * sizeof(uint32_t), s);
-        if (e != cudaSuccess) return cuda_fail(e, "clear static decode tickets");
-    }
-    pkv::DecodeArgs a{};
-    a.q = q;
-    a.out = out;
-    a.lse_out = lse_out;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
-    a.sinks = sinks;
-    a.ring = desc->ring_blocks;
-    a.counters = ws.total ? reinterpret_cast<uint32_t*>(wsb + ws.counters) : nullptr;
-    a.part_lse = ws.total ? reinterpret_cast<float*>(wsb + ws.lse) : nullptr;
-    a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;
-    a.err = err;
-    a.num_seqs = num_seqs;
-    a.hq = desc->num_q_heads;
-    a.hkv = desc->num_kv_heads;
-    a.group = desc->num_q_heads / desc->num_kv_heads;
-    a.d = desc->head_dim;
-    a.mbps = desc->max_blocks_per_seq;
-    a.window = window;
-    a.chunk_blocks = chunk;
-    a.max_splits = splits;
-    a.max_ctx = max_context_len;
-    a.fp8 = fp8 ? 1 : 0;
-    a.num_blocks = desc->num_blocks;
-    a.sm_scale = sm_scale;
-    cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    return PKV_OK;
+    return decode_impl(desc, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                       max_context_len, sm_scale, window, sinks, chunk_blocks, out, lse_out, nullptr, 0,
+                       stream, nullptr, Scratch::kStatic);
 }

@@ -113,14 +113,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete; false if the wall
-// clock limit ran out first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// clock limit ran out first, or -- with `abort` set -- once *abort becomes
+// non-zero (another warp of the CTA has given up).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs,
+                                          const volatile int* abort = nullptr) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 255u) == 0u) {
+            if (global_timer_ns() - t0 > limit_ns) return false;
+            if (abort && *abort) return false;
+        }
     }
+}
+
+// Test hook (off unless a test arms it through pkv_test_inject_wait_timeout):
+// the first pipeline wait of one warp of CTA (0, 0, 0) is replaced by a wait
+// on a barrier that nothing arrives on, with a short limit, so that the
+// kernel's give-up path runs while every copy it issued still lands.
+__device__ __forceinline__ bool is_first_cta() {
+    return blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 }
 
 // ------------------------------------------- programmatic dependent launch --

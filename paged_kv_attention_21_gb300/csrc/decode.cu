@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     __shared__ float s_m[kW][16];
     __shared__ float s_l[kW][16];
     __shared__ int s_flag;
+    __shared__ __align__(8) uint64_t probe;  // test hook: a barrier nothing arrives on
 
     // Shared-memory set-up touches nothing the previous kernel writes: it
     // runs before the wait, while that kernel drains.
@@ -472,6 +473,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
         s_flag = 0;
+        if (a.inject_timeout) mbar_init(&probe, 1);
     }
     // With defer_wait the grid-dependency wait moves to every exit: the work
     // overlaps the previous kernel, and this grid still completes only after
@@ -635,11 +637,14 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
 
 
     bool failed = false;
+    const bool inject = a.inject_timeout != 0 && warp == 0 && is_first_cta();
     int k = 0;
     for (; k < my_n; ++k) {
         const int st = k % C::kStages;
         const uint32_t ph = (k / C::kStages) & 1;
-        const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[warp][st], ph));
+        const bool ready = __all_sync(
+            0xFFFFFFFFu, (inject && k == 0) ? mbar_wait(&probe, 0, 1000ull * a.inject_limit_us)
+                                            : mbar_wait(&bars[warp][st], ph));
         if (!ready) {
             failed = true;
             break;
@@ -661,8 +666,9 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         }
     }
     if (failed) {
-        // drain the loads still in flight (bounded), then report
-        for (int kk = k + 1; kk < min(my_n, k + C::kStages); ++kk)
+        // drain the loads still in flight -- the stage that gave up and the
+        // ones after it (bounded) -- so that no copy lands after exit, then report
+        for (int kk = k; kk < min(my_n, k + C::kStages); ++kk)
             (void)mbar_wait(&bars[warp][kk % C::kStages], (kk / C::kStages) & 1);
         if (lane == 0) {
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -719,7 +725,8 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
             f[w] = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
             L += f[w] * s_l[w][r];
         }
-        float inv = L > 0.f ? (kFp8 ? a.v_scale[kvh] : 1.f) / L : 0.f;
+        // a failed chunk contributes nothing: weight 0, lse = -inf
+        float inv = L > 0.f && !cta_failed ? (kFp8 ? a.v_scale[kvh] : 1.f) / L : 0.f;
         // a failed chunk's state is excluded from the merge by lse = -inf
         float lse = L > 0.f && !cta_failed ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
         if (a.sinks && nsplit == 1 && r < G) {
@@ -735,13 +742,15 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         s_l[0][r] = lse;
     }
     __syncthreads();
-    if (!cta_failed) {
+    {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
             const int r = idx / D;
             const int d = idx % D;
             float ov = 0.f;
+            if (!cta_failed) {
 #pragma unroll
-            for (int w = 0; w < kW; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
+                for (int w = 0; w < kW; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
+            }
             if (nsplit == 1) {
                 const size_t oi = (static_cast<size_t>(seq) * a.hq + kvh * G + r) * D + d;
                 if (a.out_f32)
@@ -963,6 +972,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
 }
 
 }  // namespace
+
+bool decode_uses_tickets(int splits) { return splits > kMaxClusterSplits; }
 
 int decode_smem_bytes(int d, int fp8) {
     if (d == 64) return fp8 ? DecodeCfg<64, true>::kSmemBytes : DecodeCfg<64, false>::kSmemBytes;

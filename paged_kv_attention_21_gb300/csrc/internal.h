@@ -110,9 +110,16 @@ struct DecodeArgs {
     // stream writes (that kernel only waited for its own predecessors), so
     // it starts without the grid-dependency wait and takes it before exiting
     int32_t defer_wait;
+    // test hook: inject_timeout != 0 makes warp 0 of CTA (0, 0, 0) give up
+    // its first pipeline wait after inject_limit_us (see common.cuh)
+    int32_t inject_timeout;
+    uint32_t inject_limit_us;
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
+// True when a plan of `splits` chunks per (sequence, KV head) merges through
+// the workspace tickets (more chunks than one cluster merges).
+bool decode_uses_tickets(int splits);
 
 constexpr int kPrefillOrderMax = 256;  // sequences the prefill launch can reorder
 struct PrefillArgs {
@@ -138,6 +145,10 @@ struct PrefillArgs {
     // (sequence, KV head) (<= kSqMaxSplits; > 1 launches clusters) and m16
     // row tiles per CTA (rows = q_len * group <= 16 * this)
     int32_t sq_chunk, sq_splits, sq_row_tiles;
+    // test hook: inject_timeout != 0 makes the MMA warp of CTA (0, 0, 0) of
+    // the tcgen05 kernel give up its first K-tile wait after inject_limit_us
+    int32_t inject_timeout;
+    uint32_t inject_limit_us;
 };
 constexpr int kSqMaxRowTiles = 4;   // 64 query rows (tokens x heads of a KV group)
 constexpr int kSqMaxSplits = 4;     // chunks per (sequence, KV head): one cluster

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t bar_p_full[kTcQTiles];
     __shared__ __align__(8) uint64_t bar_o_done[kTcQTiles];
     __shared__ __align__(8) uint64_t bar_pair[kTcQTiles][4][3];  // per tile and quadrant: parity 0/1, final
+    __shared__ __align__(8) uint64_t bar_mma_fin;  // every MMA this CTA issued is complete
+    __shared__ __align__(8) uint64_t probe;        // test hook: a barrier nothing arrives on
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     __shared__ float s_red_max[kTcQTiles][2][2][kTcM];  // [tile][parity][column half][row]
@@ -189,6 +191,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int qd = 0; qd < 4; ++qd)
                 for (int i = 0; i < 3; ++i) mbar_init(&bar_pair[x][qd][i], 64);
         }
+        mbar_init(&bar_mma_fin, 1);
+        if (a.inject_timeout) mbar_init(&probe, 1);
         s_fail = 0;
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
@@ -205,9 +209,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = s_tmem;
 
     const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
+    // Waits give up at the time limit, or as soon as another warp has given
+    // up (s_fail); the drains at the end wait for copies and MMAs in flight
+    // regardless of s_fail.
+    const volatile int* abort = &s_fail;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        int k_issued = 0, v_issued = 0;   // K / V tiles whose loads were issued
         if (n_tiles > 0) {
             if (lane == 0) {
                 int nq = 0;
@@ -254,7 +263,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int blk0 = (t_begin + j) * kTcBlocks;
                     const int st = j % C::kKStages;
                     int ok = 1;
-                    if (lane == 0) ok = mbar_wait(&bar_k_empty[st], ((j / C::kKStages) & 1) ^ 1) ? 1 : 0;
+                    if (lane == 0)
+                        ok = mbar_wait(&bar_k_empty[st], ((j / C::kKStages) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
                         if (lane == 0) atomicOr(&s_fail, 1);
@@ -278,12 +288,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             kvh, ids[b]);
                         }
                     }
+                    k_issued = j + 1;
                 }
                 if (j >= 1) {
                     const int i = j - 1;
                     const int st = i % C::kVStages;
                     int ok = 1;
-                    if (lane == 0) ok = mbar_wait(&bar_v_empty[st], ((i / C::kVStages) & 1) ^ 1) ? 1 : 0;
+                    if (lane == 0)
+                        ok = mbar_wait(&bar_v_empty[st], ((i / C::kVStages) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
                         if (lane == 0) atomicOr(&s_fail, 1);
@@ -309,14 +321,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             kvh, ids[b]);
                         }
                     }
+                    v_issued = i + 1;
                 }
             }
+            // drain: the last load issued into each stage (and Q) has landed
+            // before this CTA may exit -- immediate unless a wait gave up
+            if (lane == 0) {
+                (void)mbar_wait(&bar_q, 0);
+                for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+                    (void)mbar_wait(&bar_k[j % C::kKStages], (j / C::kKStages) & 1);
+                for (int i = max(0, v_issued - C::kVStages); i < v_issued; ++i)
+                    (void)mbar_wait(&bar_v[i % C::kVStages], (i / C::kVStages) & 1);
+            }
+            __syncwarp();
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN, false, false);
         constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTcM, D, false, true);
-        bool ok = n_tiles > 0 ? mbar_wait(&bar_q, 0) : true;
+        bool ok = n_tiles > 0 ? mbar_wait(&bar_q, 0, kWaitLimitNs, abort) : true;
         ok = __all_sync(0xFFFFFFFFu, ok);
         auto active = [&](int x, int j) { return j >= jlo[x] && j < jhi[x]; };
         // S_x(j) = Q_x K_j^T once PV_x(j-1) is done (it reads P_x(j-1) from the
@@ -327,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint8_t* sQ = smem + C::kOffQ + x * C::kQBytes;
             const uint8_t* sK = smem + C::kOffK + ks * C::kKBytes;
             if (j > jlo[x]) {
-                const bool r = mbar_wait(&bar_o_done[x], (j - 1 - jlo[x]) & 1);
+                const bool r = mbar_wait(&bar_o_done[x], (j - 1 - jlo[x]) & 1, kWaitLimitNs, abort);
                 if (!__all_sync(0xFFFFFFFFu, r)) return false;
                 tc::fence_after_sync();
             }
@@ -348,8 +371,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // O_x += P_x(j) V_j with P read from the first 64 columns of S_x
         auto issue_pv = [&](int x, int j) -> bool {
             const int vs = j % C::kVStages;
-            const bool r1 = mbar_wait(&bar_p_full[x], (j - jlo[x]) & 1);
-            const bool r2 = mbar_wait(&bar_v[vs], (j / C::kVStages) & 1);
+            const bool r1 = mbar_wait(&bar_p_full[x], (j - jlo[x]) & 1, kWaitLimitNs, abort);
+            const bool r2 = r1 && mbar_wait(&bar_v[vs], (j / C::kVStages) & 1, kWaitLimitNs, abort);
             if (!__all_sync(0xFFFFFFFFu, r1 && r2)) return false;
             tc::fence_after_sync();
             if (lane == 0) {
@@ -373,7 +396,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; ok && j <= n_tiles; ++j) {
             if (j < n_tiles) {
                 const int ks = j % C::kKStages;
-                const bool r = mbar_wait(&bar_k[ks], (j / C::kKStages) & 1);
+                const bool inject = a.inject_timeout != 0 && j == 0 && is_first_cta();
+                const bool r = inject ? mbar_wait(&probe, 0, 1000ull * a.inject_limit_us, abort)
+                                      : mbar_wait(&bar_k[ks], (j / C::kKStages) & 1, kWaitLimitNs, abort);
                 if (!__all_sync(0xFFFFFFFFu, r) || *reinterpret_cast<volatile int*>(&s_fail)) {
                     ok = false;
                     break;
@@ -409,6 +434,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
             atomicOr(&s_fail, 1);
         }
+        // drain: every MMA this thread issued is complete before TMEM is
+        // freed and the CTA exits (immediate unless a wait gave up)
+        if (lane == 0) tc::commit(&bar_mma_fin);
+        __syncwarp();
+        (void)mbar_wait(&bar_mma_fin, 0);
+        tc::fence_after_sync();
     } else {
         // -------------------------------------------------------------- softmax
         // Warp w (2..17) serves query tile x = (w - 2) / 8 and reads TMEM lane
@@ -438,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // slot 0/1 for the per-tile max exchange (by tile parity), 2 at the end
         auto pair_sync = [&](int slot, uint32_t parity) {
             mbar_arrive(&bar_pair[x][quad][slot]);
-            return mbar_wait(&bar_pair[x][quad][slot], parity);
+            return mbar_wait(&bar_pair[x][quad][slot], parity, kWaitLimitNs, abort);
         };
         float m_used = -INFINITY;
         float l = 0.f;                             // this half's share of the row sum
@@ -446,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < nx; ++i) {
             const int j = j0 + i;
             const int k0 = (t_begin + j) * kTcN;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_s_full[x], i & 1)) ||
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_s_full[x], i & 1, kWaitLimitNs, abort)) ||
                 *reinterpret_cast<volatile int*>(&s_fail)) {
                 ok = false;
                 break;
@@ -501,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool zero_v = k0 + kTcN > kv_len && (x == 0 || j < jlo[0] || j >= jhi[0]);
             if (zero_v) {
                 const int st = j % C::kVStages;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_v[st], (j / C::kVStages) & 1))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_v[st], (j / C::kVStages) & 1, kWaitLimitNs, abort))) {
                     ok = false;
                     break;
                 }
@@ -572,27 +603,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(&bar_p_full[x]);
         }
         if (ok && nx > 0) {
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done[x], (nx - 1) & 1));
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done[x], (nx - 1) & 1, kWaitLimitNs, abort));
             tc::fence_after_sync();
         }
         // every softmax thread reaches this exchange (failure or not; the wait is bounded)
         s_red_sum[x][half][r] = l;
         if (!__all_sync(0xFFFFFFFFu, pair_sync(2, 0))) ok = false;
         const float l_row = l + s_red_sum[x][half ^ 1][r];
-        if (!ok) {
-            if (lane == 0) {
-                flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                atomicOr(&s_fail, 1);
-            }
-        } else if (sp.ntok > 0) {
-            // epilogue: this half's O columns / l -> bf16 (or fp32); lse by half 0
-            const float inv = l_row > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / l_row : 0.f;
+        if (!ok && lane == 0) {
+            flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            atomicOr(&s_fail, 1);
+        }
+        if (sp.ntok > 0) {
+            // epilogue: this half's O columns / l -> bf16 (or fp32); lse by half 0.
+            // A tile that gave up writes o = 0 and lse = -inf.
+            const float inv = ok && l_row > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / l_row : 0.f;
             const size_t orow0 = (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D + half * (D / 2);
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + orow0;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 float v[32];
-                if (nx > 0) {
+                if (nx > 0 && ok) {
                     tc::ld32(lane_base + C::col_o(x) + half * (D / 2) + c * 32, v);
                     tc::wait_ld();
                 } else {
@@ -617,7 +648,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (row_ok && a.lse_out && half == 0)
                 a.lse_out[static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G] =
-                    l_row > 0.f ? (m_used + __log2f(l_row)) * 0.6931471805599453f : -INFINITY;
+                    ok && l_row > 0.f ? (m_used + __log2f(l_row)) * 0.6931471805599453f : -INFINITY;
         }
     }
 

@@ -312,8 +312,9 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
         }
     }
     if (failed) {
-        // drain the loads still in flight (bounded), then report
-        for (int kk = k + 1; kk < min(my_n, k + kSqStages); ++kk)
+        // drain the loads still in flight -- the stage that gave up and the
+        // ones after it (bounded) -- so that no copy lands after exit, then report
+        for (int kk = k; kk < min(my_n, k + kSqStages); ++kk)
             (void)mbar_wait(&bars[warp][kk % kSqStages], (kk / kSqStages) & 1);
         if (lane == 0) {
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -359,20 +360,23 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
             f[w] = s_m[w][r] == -INFINITY ? 0.f : fast_exp2(s_m[w][r] - M);
             L += f[w] * s_l[w][r];
         }
-        const float inv = L > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / L : 0.f;
+        // a failed chunk contributes nothing: weight 0, lse = -inf
+        const float inv = L > 0.f && !cta_failed ? (a.v_scale ? a.v_scale[kvh] : 1.f) / L : 0.f;
         const float lse = L > 0.f && !cta_failed ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
         for (int w = 0; w < kSqWarps; ++w) s_m[w][r] = f[w] * inv;
         s_l[0][r] = lse;
     }
     __syncthreads();
-    if (!cta_failed) {
+    {
         for (int idx = threadIdx.x; idx < trows * D; idx += kSqThreads) {
             const int r = idx / D;
             const int d = idx % D;
             float ov = 0.f;
+            if (!cta_failed) {
 #pragma unroll
-            for (int w = 0; w < kSqWarps; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
+                for (int w = 0; w < kSqWarps; ++w) ov += s_m[w][r] * comb[(w * 16 + r) * C::kCombStride + d];
+            }
             if (nsplit == 1) {
                 const int R = 16 * tile + r;
                 const size_t orow = static_cast<size_t>(q0 + R / G) * a.hq + kvh * G + R % G;

@@ -83,25 +83,48 @@ def compact_pool(k_cache, v_cache, tables, seqs):
     return k, v, new_tabs
 
 
-def assert_close(got: torch.Tensor, ref: np.ndarray, what: str, max_err=MAX_ERR, mean_err=MEAN_ERR):
-    """Attention tolerance for a bf16 output.  The kernel's result is bf16 (the
-    API's output format), the oracle's fp32, so the comparison separates the
-    computation from the final rounding:
+PARITY_LOG = os.environ.get("PKV_PARITY_LOG")
+
+
+def _log_parity(rec):
+    if PARITY_LOG:
+        import json
+        with open(PARITY_LOG, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, what: str, max_err=MAX_ERR, mean_err=MEAN_ERR,
+                 literal=True):
+    """Attention tolerance for a bf16 output against the fp32 oracle.
+
+    The literal figures -- max |out - ref| <= 1e-2 and mean |out - ref| <=
+    1e-3 against the unrounded fp32 oracle -- are computed for every call,
+    logged (PKV_PARITY_LOG), and asserted unless `literal` is False.  A test
+    passes literal=False only where the bf16 output format alone can break
+    them (outputs of magnitude >= 4, whose half-ulp exceeds 1e-2, or O(1)
+    outputs from a handful of keys, whose rounding alone averages ~1e-3); the
+    format-aware bounds below hold everywhere:
       * max: |out - ref| <= 1e-2 + half a bf16 ulp of ref (2^-8 |ref|), the
         rounding of the output format itself;
       * mean: |out - bf16(ref)| averaged <= 1e-3, with bf16(ref) the oracle's
-        result rounded by the oracle's own RNE encoder (the rounding alone
-        averages ~1e-3 on O(1) outputs)."""
+        result rounded by the oracle's own RNE encoder."""
     g = got.float().cpu().numpy()
     assert np.all(np.isfinite(g)), "%s: non-finite output" % what
     ref = np.asarray(ref, dtype=np.float32)
     raw = np.abs(g - ref)
+    ref_b = oracle.f32_from_bf16(oracle.bf16_from_f32(ref))
+    err = np.abs(g - ref_b)
+    _log_parity({"what": what, "literal_max": float(raw.max()), "literal_mean": float(raw.mean()),
+                 "mean_vs_bf16_ref": float(err.mean()), "max_abs_ref": float(np.abs(ref).max()),
+                 "n": int(raw.size), "literal_asserted": bool(literal)})
     bound = max_err + np.abs(ref) * 2.0 ** -8
     assert np.all(raw <= bound), "%s: max|err| %.3g beyond 1e-2 + half ulp (worst excess %.3g)" % (
         what, raw.max(), (raw - bound).max())
-    ref_b = oracle.f32_from_bf16(oracle.bf16_from_f32(ref))
-    err = np.abs(g - ref_b)
     assert err.mean() <= mean_err, "%s: mean|err| %.3g (<= %g)" % (what, err.mean(), mean_err)
+    if literal:
+        assert raw.max() <= max_err, "%s: literal max|err| %.3g > %g" % (what, raw.max(), max_err)
+        assert raw.mean() <= mean_err, "%s: literal mean|err| %.3g > %g" % (what, raw.mean(),
+                                                                             mean_err)
     return float(raw.max()), float(err.mean())
 
 

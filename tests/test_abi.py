@@ -220,3 +220,14 @@ def test_workspace_size_layout(lib):
     a256 = lambda x: (x + 255) // 256 * 256
     assert sz == a256(pairs * 4) + a256(pairs * S * G * 4) + a256(pairs * S * G * D * 4)
     assert pkv.pkv_decode_workspace_size(d, B, ctx, -1, 129) == 0  # chunk > 128 rejected
+
+
+def test_wait_timeout_hook_validates_its_arguments(lib):
+    """The test hook is off by default and checks its arguments on the host."""
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_test_inject_wait_timeout(4, 1000)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_test_inject_wait_timeout(1, 0)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_test_inject_wait_timeout(1, 2000000)
+    pkv.pkv_test_inject_wait_timeout(0)

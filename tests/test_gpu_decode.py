@@ -29,7 +29,10 @@ def _check_batch(spec, b, d, window=-1, chunks=(0,)):
                                  b.tables_host, b.lens_host, window, ks, vs)
     for chunk in chunks:
         out, lse, ws = gpu_decode(desc, d, b.max_context_len, spec.sm_scale, window, chunk)
-        assert_close(out, ref, "%s chunk=%d window=%d" % (spec.name, chunk, window))
+        # window 1: every output is one value row, so the literal figures
+        # measure the bf16 rounding of O(1) values alone (~1.2e-3 mean)
+        assert_close(out, ref, "%s chunk=%d window=%d" % (spec.name, chunk, window),
+                     literal=window != 1)
         assert_lse_close(lse, ref_lse, spec.name)
         assert int(ws[:b.lens_host.size * spec.num_kv_heads * 4].count_nonzero()) == 0, \
             "ticket counters must be left at zero"
