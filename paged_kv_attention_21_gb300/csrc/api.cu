@@ -110,6 +110,7 @@ struct MapKey {
 enum MapKind {
     kMapBlockRows = 0,  // {D, 16, Hkv, num_blocks}, box {inner, 16, 1, 1}
     kMapTileRows = 1,   // bf16 only: {64, D/64, 16, Hkv, num_blocks}, box {64, D/64, 16, 1, 1}
+    kMapTileGroups = 2, // bf16 only: {64, 8, D/64, 2, num_blocks * Hkv}, box {64, 8, D/64, 2, 1}
 };
 
 struct MapEntry {
@@ -153,7 +154,20 @@ pkv_status pool_map(const void* pool, const pkv_cache_desc* desc, CUtensorMap* o
     const cuuint64_t nb = static_cast<cuuint64_t>(desc->num_blocks);
     CUtensorMap map;
     CUresult r;
-    if (kind == kMapTileRows) {
+    if (kind == kMapTileGroups) {
+        // one box per (block, head) tile, written as [row group g][64-column
+        // slice s][8 rows][128 bytes]: every (g, s) slab is one 1024-byte
+        // 128-byte-swizzle atom, so the tile is a K-major (K) or MN-major (V)
+        // MMA operand whose 8-row groups sit a uniform (D/64) KiB apart, across
+        // the tiles of consecutive blocks too
+        const cuuint64_t dims[5] = {64, 8, D / 64, 2, nb * hkv};
+        const cuuint64_t strides[4] = {D * elem, 64 * elem, 8 * D * elem, rows * D * elem};
+        const cuuint32_t boxdim[5] = {64, 8, static_cast<cuuint32_t>(D / 64), 2, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims, strides,
+               boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (kind == kMapTileRows) {
         // one box per (block, head): 16 rows x D/64 slices of 128 bytes, so a
         // row's slices sit side by side (row r, slice h at 128 (r D/64 + h)),
         // each swizzled by its 128-byte unit index
@@ -697,9 +711,9 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
         tables = g.stage_tables;
     }
     CUtensorMap kmap, vmap;
-    st = pool_map(kpool, &staged, &kmap);
+    st = pool_map(kpool, &staged, &kmap, kMapTileGroups);
     if (st != PKV_OK) return st;
-    st = pool_map(vpool, &staged, &vmap);
+    st = pool_map(vpool, &staged, &vmap, kMapTileGroups);
     if (st != PKV_OK) return st;
     pkv::PrefillArgs a{};
     // at most 64 query rows (tokens x heads of a group) per sequence: the
@@ -987,9 +1001,9 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
     {
         const int QT = pkv::prefill_tc_q_tile(G);
         CUtensorMap kmap, vmap, qmap;
-        st = pool_map(k_cache, desc, &kmap);
+        st = pool_map(k_cache, desc, &kmap, kMapTileGroups);
         if (st != PKV_OK) return st;
-        st = pool_map(v_cache, desc, &vmap);
+        st = pool_map(v_cache, desc, &vmap, kMapTileGroups);
         if (st != PKV_OK) return st;
         st = q_map(q, num_seqs, desc, G, QT, &qmap);
         if (st != PKV_OK) return st;

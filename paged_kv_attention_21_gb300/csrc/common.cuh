@@ -267,6 +267,37 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed pairs of fp32 (one 64-bit register pair) and the sm_100-class
+// two-wide fp32 arithmetic on them: one instruction for two lanes of work.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// max of three fp32 values in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a [rows][128 B]
 // tile stored with the 128-byte swizzle (chunk index XOR row % 8), the
 // layout TMA writes for CU_TENSOR_MAP_SWIZZLE_128B on a 1024-B aligned tile.

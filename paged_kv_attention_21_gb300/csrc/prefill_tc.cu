@@ -44,7 +44,9 @@ constexpr int kTcM = 128;                         // query rows per tile
 constexpr int kTcN = 128;                         // keys per KV tile
 constexpr int kTcBlocks = kTcN / kBlockSize;      // 8 blocks per KV tile
 constexpr int kTcQTiles = 2;                      // query tiles per CTA (A, B)
-constexpr int kTcWarps = 2 + 8 * kTcQTiles;       // producer, MMA issuer, 8 softmax warps per tile
+constexpr int kTcSmWarps = 4;                     // softmax warps per query tile: one thread per row
+constexpr int kTcVWarp = 2 + kTcSmWarps * kTcQTiles;  // the V producer, after the softmax warps
+constexpr int kTcWarps = kTcVWarp + 1;  // K producer, MMA issuer, softmax warps, V producer
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;         // log2 of the largest stale-max factor
 
@@ -54,6 +56,8 @@ struct TcCfg {
     static constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes
     static constexpr int kQBytes = kHalves * kHalfBytes;  // one Q tile
     static constexpr int kKBytes = kHalves * kHalfBytes;  // 128 keys x D (K or V tile)
+    static constexpr int kBlkBytes = kBlockSize * D * 2;   // one (block, head) tile: one TMA box
+    static constexpr int kGrpBytes = kHalves * 1024;       // between 8-row groups of a K / V tile
     static constexpr int kKStages = 2;
     static constexpr int kVStages = 2;
     static constexpr int kOffQ = 0;
@@ -119,13 +123,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t bar_s_full[kTcQTiles];
     __shared__ __align__(8) uint64_t bar_p_full[kTcQTiles];
     __shared__ __align__(8) uint64_t bar_o_done[kTcQTiles];
-    __shared__ __align__(8) uint64_t bar_pair[kTcQTiles][4][3];  // per tile and quadrant: parity 0/1, final
     __shared__ __align__(8) uint64_t bar_mma_fin;  // every MMA this CTA issued is complete
     __shared__ __align__(8) uint64_t probe;        // test hook: a barrier nothing arrives on
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    __shared__ float s_red_max[kTcQTiles][2][2][kTcM];  // [tile][parity][column half][row]
-    __shared__ float s_red_sum[kTcQTiles][2][kTcM];     // [tile][column half][row]
 
     pdl_wait();
     pdl_launch_dependents();
@@ -186,10 +187,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int x = 0; x < kTcQTiles; ++x) {
             mbar_init(&bar_s_full[x], 1);
-            mbar_init(&bar_p_full[x], 8);
+            mbar_init(&bar_p_full[x], kTcSmWarps);
             mbar_init(&bar_o_done[x], 1);
-            for (int qd = 0; qd < 4; ++qd)
-                for (int i = 0; i < 3; ++i) mbar_init(&bar_pair[x][qd][i], 64);
         }
         mbar_init(&bar_mma_fin, 1);
         if (a.inject_timeout) mbar_init(&probe, 1);
@@ -214,11 +213,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // regardless of s_fail.
     const volatile int* abort = &s_fail;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        int k_issued = 0, v_issued = 0;   // K / V tiles whose loads were issued
+    if (warp == 0 || warp == kTcVWarp) {
+        // ----------------------------------------------------------- producers
+        // Warp 0 loads Q and the K tiles, warp kTcVWarp the V tiles: one
+        // thread issues a TMA copy only every ~200 cycles, so the two rings
+        // are fed in parallel.  Each (block, head) tile is one 5-D box, laid
+        // out [row group][64-column slice][8 rows][128 B] (see the tensor map).
+        const bool is_v = warp == kTcVWarp;
+        int issued = 0;   // tiles whose loads were issued
         if (n_tiles > 0) {
-            if (lane == 0) {
+            if (!is_v && lane == 0) {
                 int nq = 0;
 #pragma unroll
                 for (int x = 0; x < kTcQTiles; ++x) nq += span[x].ntok > 0 ? 1 : 0;
@@ -232,7 +236,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     h * 64, kvh * G, q0 + span[x].tok0);
                 }
             }
-            // order of loads: K_0, K_1, V_0, K_2, V_1, ... -- K one tile ahead of V.
             // Block ids: lane l holds block l % 8 of tile l / 8 of a group of four
             // tiles; the next group is read one group ahead, so the table read is
             // never on the load path.  An id is checked when its group comes up.
@@ -250,88 +253,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             int ids_cur = check_ids(read_ids(0));
             int ids_next = read_ids(1);
-            int ids_old = 0;  // the group before ids_cur (V lags K by one tile)
-            for (int j = 0; j <= n_tiles; ++j) {
-                bool switched = false;
-                if (j < n_tiles) {
-                    if (j > 0 && (j & 3) == 0) {
-                        ids_old = ids_cur;
-                        ids_cur = check_ids(ids_next);
-                        ids_next = read_ids((j >> 2) + 1);
-                        switched = true;
-                    }
-                    const int blk0 = (t_begin + j) * kTcBlocks;
-                    const int st = j % C::kKStages;
-                    int ok = 1;
-                    if (lane == 0)
-                        ok = mbar_wait(&bar_k_empty[st], ((j / C::kKStages) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
-                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                    if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
-                        if (lane == 0) atomicOr(&s_fail, 1);
-                        break;
-                    }
-                    const int nvalid = min(kTcBlocks, nblk_seq - blk0);
-                    uint8_t* sK = smem + C::kOffK + st * C::kKBytes;
-                    int ids[kTcBlocks];
-#pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b)
-                        ids[b] = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + b);
-                    if (lane == 0) {
-                        fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(&bar_k[st], nvalid * kBlockSize * D * 2);
-#pragma unroll
-                        for (int b = 0; b < kTcBlocks; ++b) {
-                            if (b >= nvalid) break;
-#pragma unroll
-                            for (int h = 0; h < C::kHalves; ++h)
-                                tma_load_4d(sK + h * C::kHalfBytes + b * 2048, &kmap, &bar_k[st], h * 64, 0,
-                                            kvh, ids[b]);
-                        }
-                    }
-                    k_issued = j + 1;
+            const CUtensorMap* map = is_v ? &vmap : &kmap;
+            for (int j = 0; j < n_tiles; ++j) {
+                if (j > 0 && (j & 3) == 0) {
+                    ids_cur = check_ids(ids_next);
+                    ids_next = read_ids((j >> 2) + 1);
                 }
-                if (j >= 1) {
-                    const int i = j - 1;
-                    const int st = i % C::kVStages;
-                    int ok = 1;
-                    if (lane == 0)
-                        ok = mbar_wait(&bar_v_empty[st], ((i / C::kVStages) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
-                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                    if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
-                        if (lane == 0) atomicOr(&s_fail, 1);
-                        break;
-                    }
-                    const int blk0 = (t_begin + i) * kTcBlocks;
-                    const int nvalid = min(kTcBlocks, nblk_seq - blk0);
-                    uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
-                    const int src = switched ? ids_old : ids_cur;
-                    int ids[kTcBlocks];
-#pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b)
-                        ids[b] = __shfl_sync(0xFFFFFFFFu, src, (i & 3) * kTcBlocks + b);
-                    if (lane == 0) {
-                        fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(&bar_v[st], nvalid * kBlockSize * D * 2);
-#pragma unroll
-                        for (int b = 0; b < kTcBlocks; ++b) {
-                            if (b >= nvalid) break;
-#pragma unroll
-                            for (int h = 0; h < C::kHalves; ++h)
-                                tma_load_4d(sV + h * C::kHalfBytes + b * 2048, &vmap, &bar_v[st], h * 64, 0,
-                                            kvh, ids[b]);
-                        }
-                    }
-                    v_issued = i + 1;
+                const int blk0 = (t_begin + j) * kTcBlocks;
+                const int st = j % C::kKStages;
+                uint64_t* full = is_v ? &bar_v[st] : &bar_k[st];
+                uint64_t* empty = is_v ? &bar_v_empty[st] : &bar_k_empty[st];
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(empty, ((j / C::kKStages) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
+                    if (lane == 0) atomicOr(&s_fail, 1);
+                    break;
                 }
+                const int nvalid = min(kTcBlocks, nblk_seq - blk0);
+                uint8_t* dst = smem + (is_v ? C::kOffV : C::kOffK) + st * C::kKBytes;
+                int ids[kTcBlocks];
+#pragma unroll
+                for (int b = 0; b < kTcBlocks; ++b)
+                    ids[b] = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + b);
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(full, nvalid * C::kBlkBytes);
+#pragma unroll
+                    for (int b = 0; b < kTcBlocks; ++b) {
+                        if (b >= nvalid) break;
+                        tma_load_5d(dst + b * C::kBlkBytes, map, full, 0, 0, 0, 0, ids[b] * a.hkv + kvh);
+                    }
+                }
+                issued = j + 1;
             }
             // drain: the last load issued into each stage (and Q) has landed
             // before this CTA may exit -- immediate unless a wait gave up
             if (lane == 0) {
-                (void)mbar_wait(&bar_q, 0);
-                for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
-                    (void)mbar_wait(&bar_k[j % C::kKStages], (j / C::kKStages) & 1);
-                for (int i = max(0, v_issued - C::kVStages); i < v_issued; ++i)
-                    (void)mbar_wait(&bar_v[i % C::kVStages], (i / C::kVStages) & 1);
+                if (!is_v) (void)mbar_wait(&bar_q, 0);
+                for (int j = max(0, issued - C::kKStages); j < issued; ++j)
+                    (void)mbar_wait(is_v ? &bar_v[j % C::kKStages] : &bar_k[j % C::kKStages],
+                                    (j / C::kKStages) & 1);
             }
             __syncwarp();
         }
@@ -360,7 +322,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int h = kk >> 2;
                     const uint32_t ko = (kk & 3) * 32;
                     const uint64_t ad = tc::smem_desc(smem_u32(sQ + h * C::kHalfBytes) + ko, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(smem_u32(sK + h * C::kHalfBytes) + ko, 16, 1024);
+                    // K: slice h of every 8-row group, groups C::kGrpBytes apart
+                    const uint64_t bd = tc::smem_desc(smem_u32(sK + h * 1024) + ko, 16, C::kGrpBytes);
                     tc::mma_bf16(tmem + C::col_s(x), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&bar_s_full[x]);
@@ -379,12 +342,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint8_t* sV = smem + C::kOffV + vs * C::kKBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcN / 16; ++kk) {
-                    // P column group kk holds keys 64 c + 32 h + 16 s with h = kk / 4,
-                    // c = (kk / 2) % 2, s = kk % 2 (the softmax layout below).
-                    // V, MN-major: 16 keys per k-step = 2 groups of 8 rows (SBO 1024);
-                    // the two 64-column halves of head_dim are C::kHalfBytes apart (LBO)
-                    const int vrow = 64 * ((kk >> 1) & 1) + 32 * (kk >> 2) + 16 * (kk & 1);
-                    const uint64_t bd = tc::smem_desc(smem_u32(sV) + vrow * 128, C::kHalfBytes, 1024);
+                    // P columns 8 kk .. 8 kk + 7 hold keys 16 kk .. 16 kk + 15 (two
+                    // bf16 per column, the lower key in the low half): block kk of
+                    // the tile.  V, MN-major: its 2 groups of 8 rows C::kGrpBytes
+                    // apart (SBO); the 64-column slices of head_dim 1024 B apart (LBO)
+                    const uint64_t bd = tc::smem_desc(smem_u32(sV) + kk * C::kBlkBytes, 1024, C::kGrpBytes);
                     tc::mma_bf16_tmem_a(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, bd, kIdescPV,
                                         (j > jlo[x] || kk > 0) ? 1u : 0u);
                 }
@@ -442,18 +404,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_after_sync();
     } else {
         // -------------------------------------------------------------- softmax
-        // Warp w (2..17) serves query tile x = (w - 2) / 8 and reads TMEM lane
-        // quadrant w % 4; two warps share each quadrant.  Half h = ((w - 2) / 4) % 2
-        // owns the S columns 64 c + 32 h + [0, 32) for c = 0, 1 (keys k0 + the
-        // same offsets) and O columns [h D/2, (h+1) D/2).  The pair exchanges row
-        // maxima through shared memory; row sums stay per half.  Scores are
-        // streamed from TMEM twice (max, then exponentials): P for chunk c goes
-        // to columns 32 h + 16 c + [0, 16), which this half has already read, so
-        // P_x fills columns [0, 64) of S_x.
+        // Warp w (2..9) serves query tile x = (w - 2) / 4 and reads TMEM lane
+        // quadrant w % 4: each thread owns one row (its TMEM lane) and all 128
+        // key columns of a tile, so the row max and sum need no exchange.
+        // Per KV tile: load the 128 scores, take the masked row max, lazily
+        // rescale (only when the max grows by more than 2^8), form P = 2^(x - m)
+        // in fp32 (packed f32x2 arithmetic, ex2 on the MUFU), accumulate the row
+        // sum, and write P as bf16 pairs over columns [0, 64) of the tile's S.
         const int sw = warp - 2;
-        const int x = sw >> 3;                     // query tile
+        const int x = sw / kTcSmWarps;             // query tile
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = (sw >> 2) & 1;            // key / O column half
         const int r = quad * 32 + lane;            // the row this thread owns
         const int t = r / G;
         const TileSpan sp = x ? span[1] : span[0];
@@ -464,15 +424,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float scale_log2 = a.sm_scale * 1.4426950408889634f * (a.k_scale ? a.k_scale[kvh] : 1.f);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const uint32_t s_base = lane_base + C::col_s(x);
-        const int grp_tid = (sw & 7) * 32 + lane;  // 0..255 within the tile's softmax group
-        // the two warps of this quadrant meet on an mbarrier (bounded wait):
-        // slot 0/1 for the per-tile max exchange (by tile parity), 2 at the end
-        auto pair_sync = [&](int slot, uint32_t parity) {
-            mbar_arrive(&bar_pair[x][quad][slot]);
-            return mbar_wait(&bar_pair[x][quad][slot], parity, kWaitLimitNs, abort);
-        };
+        const int grp_tid = (sw % kTcSmWarps) * 32 + lane;  // 0..127 within the tile's softmax group
         float m_used = -INFINITY;
-        float l = 0.f;                             // this half's share of the row sum
+        float l = 0.f;                             // the row sum
         bool ok = true;
         for (int i = 0; i < nx; ++i) {
             const int j = j0 + i;
@@ -485,37 +439,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_after_sync();
             const bool full_vis = (!a.causal || k0 + kTcN - 1 <= sp.pos_min) && (k0 + kTcN <= kv_len) &&
                                   (a.window <= 0 || k0 > sp.pos_max - a.window);
-            // Row max.  Tiles wholly visible to the CTA (all but the diagonal and
-            // the window edge) take the max of the raw scores, scaled once;
-            // masked tiles scale and mask every score.
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float sv[kTcN];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float xs[32];
-                tc::ld32(s_base + 64 * c + 32 * half, xs);
-                tc::wait_ld();
-                if (full_vis) {
+            for (int c = 0; c < kTcN / 32; ++c)
+                tc::ld32(s_base + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+            tc::wait_ld();
+            // Row max.  Tiles wholly visible to the row (all but the diagonal
+            // and the window edge) take the max of the raw scores, scaled once;
+            // the others scale and mask every score (masked scores become -inf).
+            float mx;
+            if (full_vis) {
+                float m8[8];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], xs[e]);
-                } else {
-                    const int kb = k0 + 64 * c + 32 * half;
+                for (int e = 0; e < 8; ++e) m8[e] = sv[e];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int key = kb + e;
-                        const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                         (a.window <= 0 || key > pos - a.window);
-                        m4[e & 3] = fmaxf(m4[e & 3], vis ? xs[e] * scale_log2 : -INFINITY);
-                    }
+                for (int e = 8; e < kTcN; e += 16) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) m8[u] = fmax3(m8[u], sv[e + u], sv[e + 8 + u]);
+                }
+                mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                mx *= scale_log2;  // scale_log2 > 0: the max commutes with it
+            } else {
+                mx = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < kTcN; ++e) {
+                    const int key = k0 + e;
+                    const bool vis = key < kv_len && (!a.causal || key <= pos) &&
+                                     (a.window <= 0 || key > pos - a.window);
+                    sv[e] = vis ? sv[e] * scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sv[e]);
                 }
             }
-            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            if (full_vis) mx *= scale_log2;  // scale_log2 > 0: the max commutes with it
-            s_red_max[x][i & 1][half][r] = mx;
-            if (!__all_sync(0xFFFFFFFFu, pair_sync(i & 1, (i >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            mx = fmaxf(mx, s_red_max[x][i & 1][half ^ 1][r]);
             // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + kRescaleThreshold ||
@@ -538,58 +492,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 uint8_t* sV = smem + C::kOffV + st * C::kKBytes;
                 const int first = max(0, kv_len - k0);
-                // 8 warps x 32 lanes zero rows [first, 128) of every half
-                for (int row = first + (grp_tid >> 3); row < kTcN; row += 32) {
+                // 4 warps x 32 lanes zero key rows [first, 128), every slice (row t:
+                // block t / 16, group (t / 8) % 2, row t % 8 of that group)
+                for (int row = first + (grp_tid >> 3); row < kTcN; row += 16) {
+                    uint8_t* rp = sV + (row >> 4) * C::kBlkBytes + ((row >> 3) & 1) * C::kGrpBytes + (row & 7) * 128 +
+                                  (grp_tid & 7) * 16;
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h)
-                        *reinterpret_cast<uint4*>(sV + h * C::kHalfBytes + row * 128 + (grp_tid & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(rp + h * 1024) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
             }
-            // P = 2^(x - m) in fp32 (the row sum l stays exact to fp32), packed to
-            // bf16 pairs (the lower key in the low half)
+            // P = 2^(x - m) in fp32 (the row sum stays exact to fp32), packed to
+            // bf16 pairs (the lower key in the low half): keys 32 c .. 32 c + 31
+            // go to P columns 16 c .. 16 c + 15
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t scl = pack_f32x2(full_vis ? scale_log2 : 1.f, full_vis ? scale_log2 : 1.f);
+            const uint64_t neg = pack_f32x2(-mu, -mu);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float xs[32];
-                tc::ld32(s_base + 64 * c + 32 * half, xs);
-                tc::wait_ld();
+            for (int c = 0; c < kTcN / 32; ++c) {
                 uint32_t pk[16];
-                if (full_vis) {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const float p0 = fast_exp2(fmaf(xs[2 * u], scale_log2, -mu));
-                        const float p1 = fast_exp2(fmaf(xs[2 * u + 1], scale_log2, -mu));
-                        s4[u & 3] += p0 + p1;
-                        pk[u] = pack2<false>(p0, p1);
-                    }
-                } else {
-                    const int kb = k0 + 64 * c + 32 * half;
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        float pp[2];
-#pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            const int key = kb + 2 * u + v;
-                            const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                             (a.window <= 0 || key > pos - a.window);
-                            pp[v] = vis ? fast_exp2(fmaf(xs[2 * u + v], scale_log2, -mu)) : 0.f;
-                        }
-                        s4[u & 3] += pp[0] + pp[1];
-                        pk[u] = pack2<false>(pp[0], pp[1]);
-                    }
+                for (int u = 0; u < 16; ++u) {
+                    const uint64_t xv = fma_f32x2(pack_f32x2(sv[32 * c + 2 * u], sv[32 * c + 2 * u + 1]), scl, neg);
+                    float x0, x1;
+                    unpack_f32x2(xv, x0, x1);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    const uint64_t pp = pack_f32x2(p0, p1);
+                    acc[u & 3] = add_f32x2(acc[u & 3], pp);
+                    pk[u] = pack2<false>(p0, p1);
                 }
-                tc::st16u(s_base + 32 * half + 16 * c, pk);
+                tc::st16u(s_base + 16 * c, pk);
             }
-            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            {
+                float a0, a1, b0, b1, c0, c1, d0, d1;
+                unpack_f32x2(add_f32x2(acc[0], acc[1]), a0, a1);
+                unpack_f32x2(add_f32x2(acc[2], acc[3]), b0, b1);
+                (void)c0; (void)c1; (void)d0; (void)d1;
+                l += (a0 + a1) + (b0 + b1);
+            }
             // PV_x(j-1) is done (S_x(j) was issued after it), so O may be rescaled
             if (i > 0 && __any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     float v[32];
-                    const uint32_t col = lane_base + C::col_o(x) + half * (D / 2) + c * 32;
+                    const uint32_t col = lane_base + C::col_o(x) + c * 32;
                     tc::ld32(col, v);
                     tc::wait_ld();
 #pragma unroll
@@ -606,25 +555,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o_done[x], (nx - 1) & 1, kWaitLimitNs, abort));
             tc::fence_after_sync();
         }
-        // every softmax thread reaches this exchange (failure or not; the wait is bounded)
-        s_red_sum[x][half][r] = l;
-        if (!__all_sync(0xFFFFFFFFu, pair_sync(2, 0))) ok = false;
-        const float l_row = l + s_red_sum[x][half ^ 1][r];
         if (!ok && lane == 0) {
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
             atomicOr(&s_fail, 1);
         }
         if (sp.ntok > 0) {
-            // epilogue: this half's O columns / l -> bf16 (or fp32); lse by half 0.
-            // A tile that gave up writes o = 0 and lse = -inf.
-            const float inv = ok && l_row > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / l_row : 0.f;
-            const size_t orow0 = (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D + half * (D / 2);
+            // epilogue: the row's O / l -> bf16 (or fp32), and its lse.  A tile
+            // that gave up writes o = 0 and lse = -inf.
+            const float inv = ok && l > 0.f ? (a.v_scale ? a.v_scale[kvh] : 1.f) / l : 0.f;
+            const size_t orow0 = (static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G) * D;
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + orow0;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 float v[32];
                 if (nx > 0 && ok) {
-                    tc::ld32(lane_base + C::col_o(x) + half * (D / 2) + c * 32, v);
+                    tc::ld32(lane_base + C::col_o(x) + c * 32, v);
                     tc::wait_ld();
                 } else {
 #pragma unroll
@@ -646,9 +591,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (row_ok && a.lse_out && half == 0)
+            if (row_ok && a.lse_out)
                 a.lse_out[static_cast<size_t>(q0 + sp.tok0 + t) * a.hq + kvh * G + r % G] =
-                    ok && l_row > 0.f ? (m_used + __log2f(l_row)) * 0.6931471805599453f : -INFINITY;
+                    ok && l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
     }
 
