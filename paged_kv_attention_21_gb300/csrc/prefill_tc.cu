@@ -58,6 +58,8 @@ struct TcCfg {
     static constexpr int kKBytes = kHalves * kHalfBytes;  // 128 keys x D (K or V tile)
     static constexpr int kBlkBytes = kBlockSize * D * 2;   // one (block, head) tile: one TMA box
     static constexpr int kGrpBytes = kHalves * 1024;       // between 8-row groups of a K / V tile
+    // a third K stage (224 KiB in all at D = 128) measured no faster: the
+    // per-tile chain S -> softmax -> PV of each query tile sets the pace
     static constexpr int kKStages = 2;
     static constexpr int kVStages = 2;
     static constexpr int kOffQ = 0;
@@ -260,11 +262,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ids_next = read_ids((j >> 2) + 1);
                 }
                 const int blk0 = (t_begin + j) * kTcBlocks;
-                const int st = j % C::kKStages;
+                const int nst = is_v ? C::kVStages : C::kKStages;
+                const int st = j % nst;
                 uint64_t* full = is_v ? &bar_v[st] : &bar_k[st];
                 uint64_t* empty = is_v ? &bar_v_empty[st] : &bar_k_empty[st];
                 int ok = 1;
-                if (lane == 0) ok = mbar_wait(empty, ((j / C::kKStages) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
+                if (lane == 0) ok = mbar_wait(empty, ((j / nst) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                 if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
                     if (lane == 0) atomicOr(&s_fail, 1);
@@ -272,28 +275,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const int nvalid = min(kTcBlocks, nblk_seq - blk0);
                 uint8_t* dst = smem + (is_v ? C::kOffV : C::kOffK) + st * C::kKBytes;
-                int ids[kTcBlocks];
-#pragma unroll
-                for (int b = 0; b < kTcBlocks; ++b)
-                    ids[b] = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + b);
+                // lane b < 8 holds block b of this tile
+                const int id = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + (lane & (kTcBlocks - 1)));
                 if (lane == 0) {
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(full, nvalid * C::kBlkBytes);
-#pragma unroll
-                    for (int b = 0; b < kTcBlocks; ++b) {
-                        if (b >= nvalid) break;
-                        tma_load_5d(dst + b * C::kBlkBytes, map, full, 0, 0, 0, 0, ids[b] * a.hkv + kvh);
-                    }
                 }
+                __syncwarp();
+                // every block's copy is issued by its own lane, in one instruction
+                if (lane < nvalid) tma_load_5d(dst + lane * C::kBlkBytes, map, full, 0, 0, 0, 0, id * a.hkv + kvh);
                 issued = j + 1;
             }
             // drain: the last load issued into each stage (and Q) has landed
             // before this CTA may exit -- immediate unless a wait gave up
             if (lane == 0) {
                 if (!is_v) (void)mbar_wait(&bar_q, 0);
-                for (int j = max(0, issued - C::kKStages); j < issued; ++j)
-                    (void)mbar_wait(is_v ? &bar_v[j % C::kKStages] : &bar_k[j % C::kKStages],
-                                    (j / C::kKStages) & 1);
+                const int nst = is_v ? C::kVStages : C::kKStages;
+                for (int j = max(0, issued - nst); j < issued; ++j)
+                    (void)mbar_wait(is_v ? &bar_v[j % nst] : &bar_k[j % nst], (j / nst) & 1);
             }
             __syncwarp();
         }
