@@ -797,7 +797,8 @@ def main_prefill(args, rank, world, local):
                    "q_tokens": P.tokens, "causal": True,
                    "l2": L2_NOTE},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "traffic": kernel_traffic_per_launch("prefill_tc_kernel", 4),
                      "kernel": "prefill_tc_kernel (tcgen05, two query tiles per CTA)",
                      "peak_source": "%s bf16_tflops (burst)" % kind,
                      "algorithmic_flops_per_launch": int(P.flops),
