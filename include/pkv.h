@@ -258,7 +258,7 @@ pkv_status pkv_decode_plan(const pkv_cache_desc *desc, int32_t num_seqs,
  *              (may be NULL) for bf16 pools.  For e4m3 pools it holds a bf16
  *              copy of the batch's visible blocks (exact: every e4m3 code is a
  *              bf16 value), staged by the call before the attention kernel.
- * No ring cache (PKV_ERR_UNSUPPORTED). */
+ * No ring cache (PKV_ERR_UNSUPPORTED): a ring takes pkv_prefill_ring_commit. */
 pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *q,
                                         const int32_t *qo_indptr, const void *k_cache,
                                         const void *v_cache, const float *k_scale,
@@ -269,6 +269,45 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *
                                         int32_t causal, int32_t window, void *out,
                                         float *lse_out, void *workspace,
                                         size_t workspace_bytes, pkv_stream_t stream);
+
+/* ---- f4: ragged prefill over a sliding-window ring cache, with the cache
+ * commit (RustInfer, "Status": Tensor Core prefill over full or chunked
+ * inputs followed by a stream-ordered cache commit; SWA with a 128-token
+ * ring cache).  desc->ring_blocks = R > 0: position p of sequence s lives in
+ * table entry (p / 16) % R.  Sequence s brings q_len = qo_indptr[s+1] -
+ * qo_indptr[s] new tokens at positions [kv_len - q_len, kv_len); the keys
+ * before them are already in the ring, the chunk's own K (after RoPE) and V
+ * come in k_chunk / v_chunk, not yet in the cache -- a chunk may be longer
+ * than the ring.  Query i (at position kv_len - q_len + i) attends keys t <=
+ * its position with t > position - window: exactly what
+ * pkv_prefill_attention_ragged computes over a linear cache that holds the
+ * whole sequence (e4m3 rings: the chunk's keys quantised as
+ * pkv_append_rope quantises them).  Then the call commits the chunk: its
+ * last R * 16 tokens are written into the ring as pkv_append_rope writes
+ * them (no rotation), leaving the ring ready for the next decode step.
+ * Three launches on `stream`: staging of each sequence's visible window
+ * (ring keys and chunk keys, bf16; e4m3 codes widened exactly) into the
+ * workspace, the commit, and the prefill over the staged copy.
+ *   k_chunk, v_chunk: bf16 [total_q_tokens][Hkv][D].
+ *   block_tables: int32 [num_seqs][max_blocks_per_seq], the first R entries
+ *               the ring's blocks.  kv_lens (device) and kv_lens_host: the
+ *               lengths after the chunk.  qo_indptr_host and kv_lens_host
+ *               are required.
+ *   window   : > 0, with every window fitting the ring (PKV_ERR_INVALID_ARG).
+ *   workspace: >= pkv_prefill_ring_workspace_size(desc, num_seqs, window,
+ *               max q_len) bytes, 256-byte aligned, no initial contents.
+ * Other arguments as in pkv_prefill_attention_ragged. */
+pkv_status pkv_prefill_ring_commit(const pkv_cache_desc *desc, const void *q, const int32_t *qo_indptr,
+                                   const void *k_chunk, const void *v_chunk, void *k_cache, void *v_cache,
+                                   const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                                   const int32_t *kv_lens, int32_t num_seqs, int32_t total_q_tokens,
+                                   const int32_t *qo_indptr_host, const int32_t *kv_lens_host,
+                                   float sm_scale, int32_t window, void *out, float *lse_out,
+                                   void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Host: workspace bytes pkv_prefill_ring_commit needs; 0 for invalid arguments. */
+size_t pkv_prefill_ring_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs, int32_t window,
+                                       int32_t max_q_len);
 
 /* Host: workspace bytes pkv_prefill_attention_ragged needs: 0 for bf16 pools;
  * for e4m3, a staging copy of num_seqs * max_blocks_per_seq blocks in bf16. */

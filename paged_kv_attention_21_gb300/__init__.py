@@ -103,6 +103,9 @@ def load_library():
             "pkv_last_error": (ctypes.c_char_p, []),
             "pkv_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32]),
             "pkv_test_inject_wait_timeout": (ctypes.c_int, [i32, ctypes.c_uint32]),
+            "pkv_prefill_ring_commit": (ctypes.c_int, [D, P, P, P, P, P, P, P, P, P, P, i32, i32, P, P,
+                                                       f32, i32, P, P, P, ctypes.c_size_t, P]),
+            "pkv_prefill_ring_workspace_size": (ctypes.c_size_t, [D, i32, i32, i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -290,6 +293,26 @@ def pkv_prefill_attention_ragged(desc, q, qo_indptr, k_cache, v_cache, block_tab
         ctypes.byref(desc), _ptr(q), _ptr(qo_indptr), _ptr(k_cache), _ptr(v_cache),
         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(kv_lens), int(kv_lens.shape[0]),
         int(q.shape[0]), _ptr(qh), _ptr(kh), float(sm_scale), int(bool(causal)), int(window),
+        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_prefill_ring_workspace_size(desc, num_seqs, window, max_q_len):
+    return int(load_library().pkv_prefill_ring_workspace_size(ctypes.byref(desc), int(num_seqs),
+                                                              int(window), int(max_q_len)))
+
+
+def pkv_prefill_ring_commit(desc, q, qo_indptr, k_chunk, v_chunk, k_cache, v_cache, block_tables,
+                            kv_lens, sm_scale, window, out, qo_indptr_host, kv_lens_host,
+                            workspace, lse=None, k_scale=None, v_scale=None, stream=None):
+    """Ragged prefill over a ring cache, then the commit of the chunk's K/V
+    (k_chunk / v_chunk, bf16 [total_q][Hkv][D], K after RoPE) into the ring."""
+    qh = np.ascontiguousarray(qo_indptr_host, np.int32)
+    kh = np.ascontiguousarray(kv_lens_host, np.int32)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().pkv_prefill_ring_commit(
+        ctypes.byref(desc), _ptr(q), _ptr(qo_indptr), _ptr(k_chunk), _ptr(v_chunk), _ptr(k_cache),
+        _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(kv_lens),
+        int(kv_lens.shape[0]), int(q.shape[0]), _ptr(qh), _ptr(kh), float(sm_scale), int(window),
         _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
 
 

@@ -626,21 +626,26 @@ size_t pkv_prefill_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,
     return prefill_stage_ws(desc, num_seqs).total;
 }
 
-pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* q,
-                                        const int32_t* qo_indptr, const void* k_cache,
-                                        const void* v_cache, const float* k_scale,
-                                        const float* v_scale, const int32_t* block_tables,
-                                        const int32_t* kv_lens, int32_t num_seqs,
-                                        int32_t total_q_tokens, const int32_t* qo_indptr_host,
-                                        const int32_t* kv_lens_host, float sm_scale,
-                                        int32_t causal, int32_t window, void* out,
-                                        float* lse_out, void* workspace,
-                                        size_t workspace_bytes, pkv_stream_t stream) {
-    g_last_error[0] = 0;
+}  // extern "C"
+
+namespace {
+
+// The ragged prefill.  scaled_codes: the bf16 pools hold e4m3 codes widened
+// exactly (a staged e4m3 cache); k_scale / v_scale are then folded in as for
+// an e4m3 pool.
+pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t* qo_indptr,
+                        const void* k_cache, const void* v_cache, const float* k_scale,
+                        const float* v_scale, const int32_t* block_tables, const int32_t* kv_lens,
+                        int32_t num_seqs, int32_t total_q_tokens, const int32_t* qo_indptr_host,
+                        const int32_t* kv_lens_host, float sm_scale, int32_t causal, int32_t window,
+                        void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                        pkv_stream_t stream, bool scaled_codes) {
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
-    if (desc->ring_blocks > 0) return fail(PKV_ERR_UNSUPPORTED, "prefill reads linear tables (no ring cache)");
+    if (desc->ring_blocks > 0)
+        return fail(PKV_ERR_UNSUPPORTED, "prefill reads linear tables; a ring cache takes pkv_prefill_ring_commit");
     const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (scaled_codes && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "scaled codes need k_scale and v_scale");
     if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
     if (num_seqs < 0 || num_seqs > 65535)
         return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
@@ -726,8 +731,8 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     }
     const bool short_q = qo_indptr_host && max_q * G <= pkv::kSqMaxRowTiles * 16 &&
                          plan_short_query(kv_bound, max_q, window, &sq_chunk, &sq_splits);
-    a.k_scale = fp8 ? k_scale : nullptr;
-    a.v_scale = fp8 ? v_scale : nullptr;
+    a.k_scale = fp8 || scaled_codes ? k_scale : nullptr;
+    a.v_scale = fp8 || scaled_codes ? v_scale : nullptr;
     a.q = q;
     a.out = out;
     a.lse_out = lse_out;
@@ -782,6 +787,144 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
     cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PKV_OK;
+}
+
+// Staging blocks per sequence of a ring-cache prefill: the chunk's window
+// reaches window - 1 keys before its first token, from a block boundary.
+int ring_stage_cap(int window, int max_q) { return (window - 1 + max_q + 15) / 16 + 1; }
+
+struct RingWs {
+    size_t tables, lens, k, v, total;
+};
+RingWs ring_ws_layout(const pkv_cache_desc* d, int num_seqs, int cap) {
+    RingWs w{};
+    const size_t blocks = size_t(num_seqs) * cap;
+    const size_t block_bytes = size_t(d->num_kv_heads) * d->block_size * d->head_dim * 2;
+    w.tables = 0;
+    w.lens = align256(blocks * sizeof(int32_t));
+    w.k = w.lens + align256(size_t(num_seqs) * sizeof(int32_t));
+    w.v = w.k + align256(blocks * block_bytes);
+    w.total = w.v + align256(blocks * block_bytes);
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* q,
+                                        const int32_t* qo_indptr, const void* k_cache,
+                                        const void* v_cache, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_tables,
+                                        const int32_t* kv_lens, int32_t num_seqs,
+                                        int32_t total_q_tokens, const int32_t* qo_indptr_host,
+                                        const int32_t* kv_lens_host, float sm_scale,
+                                        int32_t causal, int32_t window, void* out,
+                                        float* lse_out, void* workspace,
+                                        size_t workspace_bytes, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    return prefill_impl(desc, q, qo_indptr, k_cache, v_cache, k_scale, v_scale, block_tables, kv_lens,
+                        num_seqs, total_q_tokens, qo_indptr_host, kv_lens_host, sm_scale, causal, window,
+                        out, lse_out, workspace, workspace_bytes, stream, false);
+}
+
+size_t pkv_prefill_ring_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs, int32_t window,
+                                       int32_t max_q_len) {
+    if (check_desc(desc) != PKV_OK || num_seqs <= 0 || window <= 0 || max_q_len < 1) return 0;
+    return ring_ws_layout(desc, num_seqs, ring_stage_cap(window, max_q_len)).total;
+}
+
+pkv_status pkv_prefill_ring_commit(const pkv_cache_desc* desc, const void* q, const int32_t* qo_indptr,
+                                   const void* k_chunk, const void* v_chunk, void* k_cache, void* v_cache,
+                                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                   const int32_t* kv_lens, int32_t num_seqs, int32_t total_q_tokens,
+                                   const int32_t* qo_indptr_host, const int32_t* kv_lens_host,
+                                   float sm_scale, int32_t window, void* out, float* lse_out,
+                                   void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    g_last_error[0] = 0;
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (desc->ring_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "pkv_prefill_ring_commit needs a ring cache");
+    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
+    if (num_seqs < 0 || num_seqs > 65535)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range [0, 65535]", num_seqs);
+    if (total_q_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "total_q_tokens < 0");
+    if (num_seqs == 0 || total_q_tokens == 0) return PKV_OK;
+    if (!q || !qo_indptr || !k_chunk || !v_chunk || !k_cache || !v_cache || !block_tables || !kv_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "null device pointer");
+    if (!qo_indptr_host || !kv_lens_host)
+        return fail(PKV_ERR_INVALID_ARG, "a ring-cache prefill needs qo_indptr_host and kv_lens_host");
+    // a window the ring holds: any position's window fits in ring_blocks blocks
+    st = check_ring_window(desc, window, 1);
+    if (st != PKV_OK) return st;
+    if (qo_indptr_host[0] != 0 || qo_indptr_host[num_seqs] != total_q_tokens)
+        return fail(PKV_ERR_INVALID_ARG, "qo_indptr_host must run from 0 to total_q_tokens");
+    int max_q = 0;
+    std::vector<int32_t> stage_lens_host(static_cast<size_t>(num_seqs));
+    for (int s = 0; s < num_seqs; ++s) {
+        const int ql = qo_indptr_host[s + 1] - qo_indptr_host[s];
+        if (ql < 0) return fail(PKV_ERR_INVALID_ARG, "qo_indptr_host decreases at %d", s);
+        if (kv_lens_host[s] < ql) return fail(PKV_ERR_INVALID_ARG, "sequence %d: kv_len %d < q_len %d", s,
+                                              kv_lens_host[s], ql);
+        max_q = std::max(max_q, ql);
+        const int lo = std::max(0, kv_lens_host[s] - ql - window + 1);
+        stage_lens_host[static_cast<size_t>(s)] = kv_lens_host[s] - (lo - lo % 16);
+    }
+    const int cap = ring_stage_cap(window, max_q);
+    const RingWs ws = ring_ws_layout(desc, num_seqs, cap);
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", ws.total);
+    if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (workspace_bytes < ws.total)
+        return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, ws.total);
+    if (int64_t(num_seqs) * cap > 0x7FFFFFFFLL) return fail(PKV_ERR_UNSUPPORTED, "staging table too large");
+    uint32_t* err = nullptr;
+    st = device_state(&err, nullptr);
+    if (st != PKV_OK) return st;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    pkv::RingStageArgs g{};
+    g.k_cache = k_cache;
+    g.v_cache = v_cache;
+    g.k_scale = k_scale;
+    g.v_scale = v_scale;
+    g.block_tables = block_tables;
+    g.qo_indptr = qo_indptr;
+    g.kv_lens = kv_lens;
+    g.k_chunk = k_chunk;
+    g.v_chunk = v_chunk;
+    g.stage_tables = reinterpret_cast<int32_t*>(wsb + ws.tables);
+    g.stage_lens = reinterpret_cast<int32_t*>(wsb + ws.lens);
+    g.k_stage = reinterpret_cast<uint16_t*>(wsb + ws.k);
+    g.v_stage = reinterpret_cast<uint16_t*>(wsb + ws.v);
+    g.k_ring_out = k_cache;
+    g.v_ring_out = v_cache;
+    g.num_seqs = num_seqs;
+    g.hkv = desc->num_kv_heads;
+    g.d = desc->head_dim;
+    g.mbps = desc->max_blocks_per_seq;
+    g.ring = desc->ring_blocks;
+    g.window = window;
+    g.cap = cap;
+    g.fp8 = fp8 ? 1 : 0;
+    g.total_q = total_q_tokens;
+    g.num_blocks = desc->num_blocks;
+    g.err = err;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // 1. the window's keys, ring and chunk, into a linear bf16 staging copy
+    cudaError_t e = pkv::launch_stage_ring(g, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ring staging launch");
+    // 2. the stream-ordered cache commit: the chunk's surviving tokens into the ring
+    e = pkv::launch_commit_ring(g, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ring commit launch");
+    // 3. the ragged prefill over the staging copy
+    pkv_cache_desc staged = *desc;
+    staged.kv_dtype = PKV_KV_BF16;
+    staged.ring_blocks = 0;
+    staged.num_blocks = static_cast<int64_t>(num_seqs) * cap;
+    staged.max_blocks_per_seq = cap;
+    return prefill_impl(&staged, q, qo_indptr, g.k_stage, g.v_stage, k_scale, v_scale, g.stage_tables,
+                        g.stage_lens, num_seqs, total_q_tokens, qo_indptr_host, stage_lens_host.data(),
+                        sm_scale, 1, window, out, lse_out, nullptr, 0, stream, fp8);
 }
 
 pkv_status pkv_append_rope(const pkv_cache_desc* desc, void* k_cache, void* v_cache,

@@ -320,3 +320,174 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace pkv
+
+namespace pkv {
+
+// ------------------------------------------------- ring-cache prefill --
+//
+// Staging: one warp per (sequence, staging block, head, row); lane l moves
+// D/32 elements of the K row and of the V row.  Position p = start + 16 b +
+// row comes from the ring below the chunk, from the chunk's own K/V inside
+// it (e4m3 rings: quantised as the append quantises, then widened), and is
+// zero past kv_len.
+
+__device__ __forceinline__ int ring_start(int kv_len, int q_len, int window) {
+    const int lo = max(0, kv_len - q_len - window + 1);
+    return lo - lo % kBlockSize;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits_of(float x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<const uint16_t*>(&b);
+}
+
+__device__ __forceinline__ float e4m3_value(uint8_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) stage_ring_kernel(RingStageArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int EPL = D / 32;  // elements per lane
+    const int lane = threadIdx.x & 31;
+    const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long per_seq = static_cast<long long>(a.cap) * a.hkv * kBlockSize;
+    const int s = static_cast<int>(w / per_seq);
+    if (s >= a.num_seqs) return;
+    const long long rem = w % per_seq;
+    const int b = static_cast<int>(rem / (a.hkv * kBlockSize));
+    const int h = static_cast<int>((rem / kBlockSize) % a.hkv);
+    const int row = static_cast<int>(rem % kBlockSize);
+    const int q0 = a.qo_indptr[s];
+    const int q_len = a.qo_indptr[s + 1] - q0;
+    const int kv_len = a.kv_lens[s];
+    const int start = ring_start(kv_len, q_len, a.window);
+    const int prefix = kv_len - q_len;
+    if (lane == 0 && h == 0 && row == 0) {
+        a.stage_tables[static_cast<size_t>(s) * a.cap + b] = s * a.cap + b;
+        if (b == 0) a.stage_lens[s] = kv_len - start;
+    }
+    const int p = start + b * kBlockSize + row;
+    const size_t dst = ((static_cast<size_t>(s) * a.cap + b) * a.hkv + h) * kBlockSize * D + row * D;
+    uint16_t kv[2][EPL];
+    if (p < prefix && p >= 0) {
+        const int entry = (p / kBlockSize) % a.ring;
+        const int blk = a.block_tables[static_cast<size_t>(s) * a.mbps + entry];
+        if (blk < 0 || blk >= a.num_blocks) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) kv[0][e] = kv[1][e] = 0;
+        } else {
+            const size_t src = ((static_cast<size_t>(blk) * a.hkv + h) * kBlockSize + p % kBlockSize) * D;
+#pragma unroll
+            for (int pool = 0; pool < 2; ++pool) {
+                const void* base = pool ? a.v_cache : a.k_cache;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    const int c = lane + 32 * e;
+                    kv[pool][e] = a.fp8 ? bf16_bits_of(e4m3_value(static_cast<const uint8_t*>(base)[src + c]))
+                                        : static_cast<const uint16_t*>(base)[src + c];
+                }
+            }
+        }
+    } else if (p >= prefix && p < kv_len) {
+        const size_t src = (static_cast<size_t>(q0 + p - prefix) * a.hkv + h) * D;
+#pragma unroll
+        for (int pool = 0; pool < 2; ++pool) {
+            const uint16_t* x = static_cast<const uint16_t*>(pool ? a.v_chunk : a.k_chunk) + src;
+            const float sc = a.fp8 ? (pool ? a.v_scale[h] : a.k_scale[h]) : 1.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const uint16_t v = x[lane + 32 * e];
+                if (a.fp8) {
+                    const float f = __uint_as_float(static_cast<uint32_t>(v) << 16);
+                    const uint8_t code = __nv_cvt_float_to_fp8(__fdiv_rn(f, sc), __NV_SATFINITE, __NV_E4M3);
+                    kv[pool][e] = bf16_bits_of(e4m3_value(code));
+                } else {
+                    kv[pool][e] = v;
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) kv[0][e] = kv[1][e] = 0;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        a.k_stage[dst + lane + 32 * e] = kv[0][e];
+        a.v_stage[dst + lane + 32 * e] = kv[1][e];
+    }
+}
+
+// Commit: one warp per (chunk token, head); the tokens at positions >=
+// kv_len - ring * 16 (the ones the ring keeps, each in its own slot) are
+// written into the ring as the append writes them (K already rotated).
+template <int D>
+__global__ void __launch_bounds__(256) commit_ring_kernel(RingStageArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int EPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long t = w / a.hkv;
+    const int h = static_cast<int>(w % a.hkv);
+    if (t >= a.total_q) return;
+    // the sequence of chunk row t: the last s with qo_indptr[s] <= t
+    int lo = 0, hi = a.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.qo_indptr[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    const int q0 = a.qo_indptr[s];
+    const int q_len = a.qo_indptr[s + 1] - q0;
+    if (t >= q0 + q_len) return;  // a row past the batch's last sequence
+    const int kv_len = a.kv_lens[s];
+    const int p = kv_len - q_len + static_cast<int>(t - q0);
+    if (p < 0 || p < kv_len - a.ring * kBlockSize) return;  // overwritten within this chunk
+    const int entry = (p / kBlockSize) % a.ring;
+    const int blk = a.block_tables[static_cast<size_t>(s) * a.mbps + entry];
+    if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+        return;
+    }
+    const size_t src = (static_cast<size_t>(t) * a.hkv + h) * D;
+    const size_t dst = ((static_cast<size_t>(blk) * a.hkv + h) * kBlockSize + p % kBlockSize) * D;
+#pragma unroll
+    for (int pool = 0; pool < 2; ++pool) {
+        const uint16_t* x = static_cast<const uint16_t*>(pool ? a.v_chunk : a.k_chunk) + src;
+        if (a.fp8) {
+            uint8_t* c = static_cast<uint8_t*>(pool ? a.v_ring_out : a.k_ring_out) + dst;
+            const float sc = pool ? a.v_scale[h] : a.k_scale[h];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const float f = __uint_as_float(static_cast<uint32_t>(x[lane + 32 * e]) << 16);
+                c[lane + 32 * e] = __nv_cvt_float_to_fp8(__fdiv_rn(f, sc), __NV_SATFINITE, __NV_E4M3);
+            }
+        } else {
+            uint16_t* c = static_cast<uint16_t*>(pool ? a.v_ring_out : a.k_ring_out) + dst;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) c[lane + 32 * e] = x[lane + 32 * e];
+        }
+    }
+}
+
+cudaError_t launch_stage_ring(const RingStageArgs& a, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(a.num_seqs) * a.cap * a.hkv * kBlockSize;
+    if (warps == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
+    return a.d == 64 ? launch_pdl(stage_ring_kernel<64>, grid, dim3(256), 0, stream, a)
+                     : launch_pdl(stage_ring_kernel<128>, grid, dim3(256), 0, stream, a);
+}
+
+cudaError_t launch_commit_ring(const RingStageArgs& a, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(a.total_q) * a.hkv;
+    if (warps == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
+    return a.d == 64 ? launch_pdl(commit_ring_kernel<64>, grid, dim3(256), 0, stream, a)
+                     : launch_pdl(commit_ring_kernel<128>, grid, dim3(256), 0, stream, a);
+}
+
+}  // namespace pkv

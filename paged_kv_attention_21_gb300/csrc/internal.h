@@ -69,6 +69,40 @@ struct StageArgs {
 };
 cudaError_t launch_stage_fp8(const StageArgs& a, cudaStream_t stream);
 
+// Ring-cache prefill (RustInfer, "Status": Tensor Core prefill over an SWA
+// ring cache, followed by a stream-ordered cache commit).  Sequence s has
+// q_len = qo_indptr[s+1] - qo_indptr[s] new tokens at positions [kv_len -
+// q_len, kv_len); its earlier keys live in a ring of `ring` table entries
+// (position p in entry (p / 16) % ring).  Staging copies, per sequence, the
+// keys at positions [start, kv_len) that the chunk's window can see --
+// start = the block floor of max(0, kv_len - q_len - window + 1) -- into
+// staging blocks s * cap .. s * cap + cap - 1 (bf16; e4m3 codes become their
+// exact bf16 values, the chunk's own e4m3 keys are quantised first), so the
+// prefill runs over a linear table of kv_len - start keys.  The commit then
+// writes the chunk's last ring * 16 tokens into the ring.
+struct RingStageArgs {
+    const void* k_cache;   // the ring pools, bf16 or e4m3
+    const void* v_cache;
+    const float* k_scale;  // e4m3 only
+    const float* v_scale;
+    const int32_t* block_tables;  // [num_seqs][mbps], ring entries in the first `ring`
+    const int32_t* qo_indptr;
+    const int32_t* kv_lens;
+    const void* k_chunk;   // bf16 [total_q][hkv][d]: the chunk's K (after RoPE) and V
+    const void* v_chunk;
+    uint16_t* k_stage;     // bf16 [num_seqs * cap][hkv][16][d]
+    uint16_t* v_stage;
+    int32_t* stage_tables; // [num_seqs][cap]
+    int32_t* stage_lens;   // [num_seqs]: kv_len - start
+    void* k_ring_out;      // the pools again, written by the commit
+    void* v_ring_out;
+    int32_t num_seqs, hkv, d, mbps, ring, window, cap, fp8, total_q;
+    int64_t num_blocks;
+    uint32_t* err;
+};
+cudaError_t launch_stage_ring(const RingStageArgs& a, cudaStream_t stream);
+cudaError_t launch_commit_ring(const RingStageArgs& a, cudaStream_t stream);
+
 struct MergeArgs {
     const float* o_parts;
     const float* lse_parts;
