@@ -902,7 +902,8 @@ def main_next(args, rank, world, local):
                              head_dim=spec.head_dim, num_blocks=cb.k_cache.shape[0],
                              max_blocks_per_seq=cb.prefix_tables.shape[1])
         max_suffix = int(cb.suffix_host.max())
-        ws = torch.zeros(max(pkv.pkv_cascade_workspace_size(desc, B, max_suffix), 256),
+        ws = torch.zeros(max(pkv.pkv_cascade_workspace_size(desc, spec.groups, B,
+                                                            int(cb.prefix_host.max()), max_suffix), 256),
                          dtype=torch.uint8, device=dev)
         out = torch.empty_like(cb.q)
         run = lambda: pkv.pkv_cascade_decode(desc, cb.q, cb.k_cache, cb.v_cache, cb.group_indptr,

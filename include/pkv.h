@@ -346,22 +346,33 @@ pkv_status pkv_merge_states(const float *o_parts, const float *lse_parts, int32_
  *               and prefix_lens_host: int32 [num_groups], tokens in [0, table capacity].
  *   suffix_tables: int32 [num_seqs][max_blocks_per_seq]; suffix_lens: int32
  *               [num_seqs], each in [1, max_suffix_len] (the new token is in the suffix).
+ *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL), as in
+ *               pkv_decode_attention; the groups' prefix blocks are then
+ *               staged as exact bf16 copies in the workspace first.
+ *   window   : <= 0 for full attention; > 0 a sliding window over each
+ *               sequence's positions (its query at prefix + suffix_len - 1
+ *               sees keys t > that position - window).  A window reaches at
+ *               most window - 1 prefix keys, the last ones, and they differ
+ *               per sequence: the prefix pass is then the split-KV decode
+ *               over the group's prefix table, each sequence from its own
+ *               window start.
  *   workspace : >= pkv_cascade_workspace_size(...) bytes, 256-byte aligned,
  *               zero-filled before its first use (it holds the decode tickets).
- * bf16 pools only (PKV_ERR_UNSUPPORTED for e4m3); no sliding window. */
+ * No ring cache (PKV_ERR_UNSUPPORTED). */
 pkv_status pkv_cascade_decode(const pkv_cache_desc *desc, const void *q, const void *k_cache,
-                              const void *v_cache, int32_t num_groups, const int32_t *group_indptr,
+                              const void *v_cache, const float *k_scale, const float *v_scale,
+                              int32_t num_groups, const int32_t *group_indptr,
                               const int32_t *group_indptr_host, const int32_t *prefix_tables,
                               const int32_t *prefix_lens, const int32_t *prefix_lens_host,
                               int32_t num_seqs, const int32_t *suffix_tables,
                               const int32_t *suffix_lens, int32_t max_suffix_len, float sm_scale,
-                              void *out, float *lse_out, void *workspace, size_t workspace_bytes,
-                              pkv_stream_t stream);
+                              int32_t window, void *out, float *lse_out, void *workspace,
+                              size_t workspace_bytes, pkv_stream_t stream);
 
-/* Host: workspace bytes pkv_cascade_decode needs (planning uses the current
- * device's SM count); 0 for invalid arguments. */
-size_t pkv_cascade_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
-                                  int32_t max_suffix_len);
+/* Host: workspace bytes pkv_cascade_decode needs for these bounds (planning
+ * uses the current device's SM count); 0 for invalid arguments. */
+size_t pkv_cascade_workspace_size(const pkv_cache_desc *desc, int32_t num_groups, int32_t num_seqs,
+                                  int32_t max_prefix_len, int32_t max_suffix_len, int32_t window);
 
 /* ---- decode with no workspace argument (no counterpart on the pages) ---
  * The same computation as pkv_decode_attention, for callers that cannot

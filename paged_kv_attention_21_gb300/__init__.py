@@ -96,9 +96,9 @@ def load_library():
             "pkv_decode_attention_static": (ctypes.c_int, [D, P, P, P, P, P, P, P, i32, i32, f32,
                                                            i32, P, i32, P, P, P]),
             "pkv_merge_states": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, P, P]),
-            "pkv_cascade_workspace_size": (ctypes.c_size_t, [D, i32, i32]),
-            "pkv_cascade_decode": (ctypes.c_int, [D, P, P, P, i32, P, P, P, P, P, i32, P, P, i32, f32,
-                                                  P, P, P, ctypes.c_size_t, P]),
+            "pkv_cascade_workspace_size": (ctypes.c_size_t, [D, i32, i32, i32, i32, i32]),
+            "pkv_cascade_decode": (ctypes.c_int, [D, P, P, P, P, P, i32, P, P, P, P, P, i32, P, P, i32,
+                                                  f32, i32, P, P, P, ctypes.c_size_t, P]),
             "pkv_copy_blocks": (ctypes.c_int, [D, P, P, P, P, i32, P]),
             "pkv_last_error": (ctypes.c_char_p, []),
             "pkv_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32]),
@@ -324,22 +324,26 @@ def pkv_merge_states(o_parts, lse_parts, out, lse_out=None, stream=None):
                                            _stream(stream)))
 
 
-def pkv_cascade_workspace_size(desc, num_seqs, max_suffix_len):
-    return int(load_library().pkv_cascade_workspace_size(ctypes.byref(desc), int(num_seqs),
-                                                         int(max_suffix_len)))
+def pkv_cascade_workspace_size(desc, num_groups, num_seqs, max_prefix_len, max_suffix_len,
+                               window=-1):
+    return int(load_library().pkv_cascade_workspace_size(
+        ctypes.byref(desc), int(num_groups), int(num_seqs), int(max_prefix_len),
+        int(max_suffix_len), int(window)))
 
 
 def pkv_cascade_decode(desc, q, k_cache, v_cache, group_indptr, group_indptr_host, prefix_tables,
                        prefix_lens, prefix_lens_host, suffix_tables, suffix_lens, max_suffix_len,
-                       sm_scale, out, lse=None, workspace=None, stream=None):
+                       sm_scale, out, lse=None, workspace=None, window=-1, k_scale=None,
+                       v_scale=None, stream=None):
     gh = np.ascontiguousarray(group_indptr_host, np.int32)
     ph = np.ascontiguousarray(prefix_lens_host, np.int32)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().pkv_cascade_decode(
-        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), int(gh.shape[0] - 1),
-        _ptr(group_indptr), _ptr(gh), _ptr(prefix_tables), _ptr(prefix_lens), _ptr(ph),
-        int(q.shape[0]), _ptr(suffix_tables), _ptr(suffix_lens), int(max_suffix_len),
-        float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        int(gh.shape[0] - 1), _ptr(group_indptr), _ptr(gh), _ptr(prefix_tables), _ptr(prefix_lens),
+        _ptr(ph), int(q.shape[0]), _ptr(suffix_tables), _ptr(suffix_lens), int(max_suffix_len),
+        float(sm_scale), int(window), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def pkv_device_errors(reset: bool = True) -> int:

@@ -1060,46 +1060,68 @@ pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_
 // query sees the whole prefix), which reads each prefix block once for the
 // whole group; each sequence's own suffix goes through the decode kernel;
 // the two fp32 (o, lse) states merge exactly as split-KV partials do.
+// e4m3 pools: the groups' prefix blocks are first staged as bf16 (exact),
+// and the prefix pass folds the scales in.  With a sliding window a query
+// sees at most window - 1 prefix keys, the last ones before its suffix, and
+// they differ per sequence: the prefix pass is then the decode kernel over
+// the group's prefix table with each sequence's own window start.
 
 namespace {
 struct CascadeWs {
-    size_t o, lse, dec, dec_bytes, total;
+    size_t o, lse, dec, dec_bytes, pre, pre_bytes, stage, stage_bytes, total;
+    int stage_mbps;
 };
-CascadeWs cascade_ws_layout(const pkv_cache_desc* d, int num_seqs, int max_suffix_len, int sms) {
+CascadeWs cascade_ws_layout(const pkv_cache_desc* d, int num_groups, int num_seqs, int max_prefix_len,
+                            int max_suffix_len, int window, int sms) {
     CascadeWs w{};
     const size_t rows = size_t(num_seqs) * d->num_q_heads;
     w.o = 0;
     w.lse = align256(2 * rows * d->head_dim * sizeof(float));
     w.dec = w.lse + align256(2 * rows * sizeof(float));
     int c = 0, sp = 0;
-    w.dec_bytes = 0;
-    if (plan_decode(d, num_seqs, std::max(max_suffix_len, 1), -1, sms, 0, &c, &sp) == PKV_OK)
+    if (plan_decode(d, num_seqs, std::max(max_suffix_len, 1), window, sms, 0, &c, &sp) == PKV_OK)
         w.dec_bytes = decode_ws_layout(d, num_seqs, sp).total;
-    w.total = w.dec + w.dec_bytes;
+    w.pre = w.dec + align256(w.dec_bytes);
+    if (window > 0 && max_prefix_len > 0 &&
+        plan_decode(d, num_seqs, max_prefix_len, window, sms, 0, &c, &sp) == PKV_OK)
+        w.pre_bytes = decode_ws_layout(d, num_seqs, sp).total;
+    w.stage = w.pre + align256(w.pre_bytes);
+    w.stage_mbps = std::max(1, (max_prefix_len + 15) / 16);
+    if (window <= 0 && d->kv_dtype == PKV_KV_FP8_E4M3 && max_prefix_len > 0) {
+        const size_t blocks = size_t(num_groups) * w.stage_mbps;
+        const size_t block_bytes = size_t(d->num_kv_heads) * d->block_size * d->head_dim * 2;
+        w.stage_bytes = align256(blocks * sizeof(int32_t)) + 2 * align256(blocks * block_bytes);
+    }
+    w.total = w.stage + w.stage_bytes;
     return w;
 }
 }  // namespace
 
-size_t pkv_cascade_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_suffix_len) {
-    if (check_desc(desc) != PKV_OK || num_seqs <= 0 || max_suffix_len < 1) return 0;
+size_t pkv_cascade_workspace_size(const pkv_cache_desc* desc, int32_t num_groups, int32_t num_seqs,
+                                  int32_t max_prefix_len, int32_t max_suffix_len, int32_t window) {
+    if (check_desc(desc) != PKV_OK || num_groups <= 0 || num_seqs <= 0 || max_suffix_len < 1 ||
+        max_prefix_len < 0)
+        return 0;
     int sms = 0;
     if (device_state(nullptr, &sms) != PKV_OK) return 0;
-    return cascade_ws_layout(desc, num_seqs, max_suffix_len, sms).total;
+    return cascade_ws_layout(desc, num_groups, num_seqs, max_prefix_len, max_suffix_len, window, sms).total;
 }
 
 pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const void* k_cache,
-                              const void* v_cache, int32_t num_groups, const int32_t* group_indptr,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              int32_t num_groups, const int32_t* group_indptr,
                               const int32_t* group_indptr_host, const int32_t* prefix_tables,
                               const int32_t* prefix_lens, const int32_t* prefix_lens_host,
                               int32_t num_seqs, const int32_t* suffix_tables,
                               const int32_t* suffix_lens, int32_t max_suffix_len, float sm_scale,
-                              void* out, float* lse_out, void* workspace, size_t workspace_bytes,
-                              pkv_stream_t stream) {
+                              int32_t window, void* out, float* lse_out, void* workspace,
+                              size_t workspace_bytes, pkv_stream_t stream) {
     g_last_error[0] = 0;
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (desc->ring_blocks > 0) return fail(PKV_ERR_UNSUPPORTED, "cascade decode reads linear tables (no ring cache)");
-    if (desc->kv_dtype != PKV_KV_BF16) return fail(PKV_ERR_UNSUPPORTED, "cascade decode reads bf16 pools only");
+    const bool fp8 = desc->kv_dtype == PKV_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
     if (num_seqs < 0 || num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d out of range", num_seqs);
     if (num_seqs == 0) return PKV_OK;
     if (num_groups < 1 || num_groups > num_seqs)
@@ -1115,19 +1137,20 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         return fail(PKV_ERR_INVALID_ARG, "max_suffix_len %d outside [1, %d]", max_suffix_len, cap);
     if (group_indptr_host[0] != 0 || group_indptr_host[num_groups] != num_seqs)
         return fail(PKV_ERR_INVALID_ARG, "group_indptr_host must run from 0 to num_seqs");
-    int max_group = 0;
+    int max_group = 0, max_prefix = 0;
     for (int g = 0; g < num_groups; ++g) {
         const int n = group_indptr_host[g + 1] - group_indptr_host[g];
         if (n < 0) return fail(PKV_ERR_INVALID_ARG, "group_indptr_host decreases at %d", g);
         max_group = std::max(max_group, n);
         if (prefix_lens_host[g] < 0 || prefix_lens_host[g] > cap)
             return fail(PKV_ERR_INVALID_ARG, "group %d: prefix length %d outside [0, %d]", g, prefix_lens_host[g], cap);
+        max_prefix = std::max(max_prefix, prefix_lens_host[g]);
     }
     uint32_t* err = nullptr;
     int sms = 0;
     st = device_state(&err, &sms);
     if (st != PKV_OK) return st;
-    const CascadeWs ws = cascade_ws_layout(desc, num_seqs, max_suffix_len, sms);
+    const CascadeWs ws = cascade_ws_layout(desc, num_groups, num_seqs, max_prefix, max_suffix_len, window, sms);
     if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", ws.total);
     if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     if (workspace_bytes < ws.total)
@@ -1141,47 +1164,124 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
 
     // part 0: every group's queries over its shared prefix
     bool prefix_launched = false;
-    {
-        const int QT = pkv::prefill_tc_q_tile(G);
-        CUtensorMap kmap, vmap, qmap;
-        st = pool_map(k_cache, desc, &kmap, kMapTileGroups);
+    if (window > 0 && max_prefix > 0) {
+        // each sequence over the prefix keys its window reaches (decode kernel)
+        int chunk = 0, splits = 0;
+        st = plan_decode(desc, num_seqs, max_prefix, window, sms, 0, &chunk, &splits);
         if (st != PKV_OK) return st;
-        st = pool_map(v_cache, desc, &vmap, kMapTileGroups);
+        const DecodeWs dws = decode_ws_layout(desc, num_seqs, splits);
+        CUtensorMap kmap, vmap;
+        st = pool_map(k_cache, desc, &kmap, kMapTileRows);
+        if (st != PKV_OK) return st;
+        st = pool_map(v_cache, desc, &vmap, kMapTileRows);
+        if (st != PKV_OK) return st;
+        uint8_t* dwb = wsb + ws.pre;
+        pkv::DecodeArgs a{};
+        a.q = q;
+        a.out_f32 = o_parts;
+        a.lse_out = lse_parts;
+        a.block_tables = prefix_tables;
+        a.context_lens = prefix_lens;
+        a.group_indptr = group_indptr;
+        a.group_suffix_lens = suffix_lens;
+        a.num_groups = num_groups;
+        a.k_scale = k_scale;
+        a.v_scale = v_scale;
+        a.counters = dws.total ? reinterpret_cast<uint32_t*>(dwb + dws.counters) : nullptr;
+        a.part_lse = dws.total ? reinterpret_cast<float*>(dwb + dws.lse) : nullptr;
+        a.part_o = dws.total ? reinterpret_cast<float*>(dwb + dws.o) : nullptr;
+        a.err = err;
+        a.num_seqs = num_seqs;
+        a.hq = desc->num_q_heads;
+        a.hkv = desc->num_kv_heads;
+        a.group = G;
+        a.d = desc->head_dim;
+        a.mbps = desc->max_blocks_per_seq;
+        a.window = window;
+        a.chunk_blocks = chunk;
+        a.max_splits = splits;
+        a.max_ctx = max_prefix;
+        a.fp8 = fp8 ? 1 : 0;
+        a.num_blocks = desc->num_blocks;
+        a.sm_scale = sm_scale;
+        cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
+        prefix_launched = true;
+    } else if (window <= 0) {
+        const int QT = pkv::prefill_tc_q_tile(G);
+        // e4m3 pools: the groups' prefix blocks as exact bf16 copies
+        pkv_cache_desc pd = *desc;
+        const void* kpool = k_cache;
+        const void* vpool = v_cache;
+        const int32_t* ptables = prefix_tables;
+        if (fp8 && max_prefix > 0) {
+            const size_t blocks = size_t(num_groups) * ws.stage_mbps;
+            const size_t block_bytes = size_t(desc->num_kv_heads) * desc->block_size * desc->head_dim * 2;
+            uint8_t* sb = wsb + ws.stage;
+            pkv::StageArgs g{};
+            g.k_cache = static_cast<const uint8_t*>(k_cache);
+            g.v_cache = static_cast<const uint8_t*>(v_cache);
+            g.block_tables = prefix_tables;
+            g.kv_lens = prefix_lens;
+            g.stage_tables = reinterpret_cast<int32_t*>(sb);
+            g.k_stage = reinterpret_cast<uint16_t*>(sb + align256(blocks * sizeof(int32_t)));
+            g.v_stage = reinterpret_cast<uint16_t*>(sb + align256(blocks * sizeof(int32_t)) +
+                                                    align256(blocks * block_bytes));
+            g.num_seqs = num_groups;
+            g.mbps = desc->max_blocks_per_seq;
+            g.stage_mbps = ws.stage_mbps;
+            g.hkv = desc->num_kv_heads;
+            g.d = desc->head_dim;
+            g.num_blocks = desc->num_blocks;
+            g.err = err;
+            cudaError_t e = pkv::launch_stage_fp8(g, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cascade prefix staging launch");
+            pd.kv_dtype = PKV_KV_BF16;
+            pd.num_blocks = static_cast<int64_t>(blocks);
+            pd.max_blocks_per_seq = ws.stage_mbps;
+            kpool = g.k_stage;
+            vpool = g.v_stage;
+            ptables = g.stage_tables;
+        }
+        CUtensorMap kmap, vmap, qmap;
+        st = pool_map(kpool, &pd, &kmap, kMapTileGroups);
+        if (st != PKV_OK) return st;
+        st = pool_map(vpool, &pd, &vmap, kMapTileGroups);
         if (st != PKV_OK) return st;
         st = q_map(q, num_seqs, desc, G, QT, &qmap);
         if (st != PKV_OK) return st;
         pkv::PrefillArgs a{};
         a.q = q;
+        a.k_scale = fp8 ? k_scale : nullptr;
+        a.v_scale = fp8 ? v_scale : nullptr;
         a.out = nullptr;
         a.out_f32 = o_parts;
         a.lse_out = lse_parts;
         a.qo_indptr = group_indptr;
         a.kv_lens = prefix_lens;
-        a.block_tables = prefix_tables;
+        a.block_tables = ptables;
         a.err = err;
         a.num_seqs = num_groups;
         a.hq = desc->num_q_heads;
         a.hkv = desc->num_kv_heads;
         a.group = G;
         a.d = desc->head_dim;
-        a.mbps = desc->max_blocks_per_seq;
+        a.mbps = pd.max_blocks_per_seq;
         a.causal = 0;
         a.window = -1;
         a.max_qtiles = (max_group + QT - 1) / QT;
         a.q_tile = QT;
         a.total_q = num_seqs;
-        a.num_blocks = desc->num_blocks;
+        a.num_blocks = pd.num_blocks;
         a.sm_scale = sm_scale;
-        int max_prefix = 0;
-        for (int g = 0; g < num_groups; ++g) max_prefix = std::max(max_prefix, prefix_lens_host[g]);
         int sq_chunk = 0, sq_splits = 0;
         if (a.max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
             plan_short_query(max_prefix, max_group, -1, &sq_chunk, &sq_splits)) {
             // a group's queries (at most 64 rows) over its prefix: short-query kernel
             CUtensorMap tkmap, tvmap;
-            st = pool_map(k_cache, desc, &tkmap, kMapTileRows);
+            st = pool_map(kpool, &pd, &tkmap, kMapTileRows);
             if (st != PKV_OK) return st;
-            st = pool_map(v_cache, desc, &tvmap, kMapTileRows);
+            st = pool_map(vpool, &pd, &tvmap, kMapTileRows);
             if (st != PKV_OK) return st;
             a.sq_chunk = sq_chunk;
             a.sq_splits = sq_splits;
@@ -1198,7 +1298,7 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
     // part 1: each sequence over its own suffix
     {
         int chunk = 0, splits = 0;
-        st = plan_decode(desc, num_seqs, max_suffix_len, -1, sms, 0, &chunk, &splits);
+        st = plan_decode(desc, num_seqs, max_suffix_len, window, sms, 0, &chunk, &splits);
         if (st != PKV_OK) return st;
         const DecodeWs dws = decode_ws_layout(desc, num_seqs, splits);
         CUtensorMap kmap, vmap;
@@ -1214,6 +1314,8 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.lse_out = lse_parts + rows;
         a.block_tables = suffix_tables;
         a.context_lens = suffix_lens;
+        a.k_scale = k_scale;
+        a.v_scale = v_scale;
         a.counters = dws.total ? reinterpret_cast<uint32_t*>(dwb + dws.counters) : nullptr;
         a.part_lse = dws.total ? reinterpret_cast<float*>(dwb + dws.lse) : nullptr;
         a.part_o = dws.total ? reinterpret_cast<float*>(dwb + dws.o) : nullptr;
@@ -1224,11 +1326,11 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.group = G;
         a.d = desc->head_dim;
         a.mbps = desc->max_blocks_per_seq;
-        a.window = -1;
+        a.window = window;
         a.chunk_blocks = chunk;
         a.max_splits = splits;
         a.max_ctx = max_suffix_len;
-        a.fp8 = 0;
+        a.fp8 = fp8 ? 1 : 0;
         a.num_blocks = desc->num_blocks;
         a.sm_scale = sm_scale;
         // the suffix pass reads nothing the prefix pass writes: it runs under
@@ -1238,8 +1340,11 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         cudaError_t e = pkv::launch_decode(a, kmap, vmap, s);
         if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
     }
-    // the two states, merged per (sequence, head)
-    pkv::MergeArgs m{o_parts, lse_parts, out, lse_out, 2, num_seqs, desc->num_q_heads, desc->head_dim};
+    // the two states, merged per (sequence, head); without a prefix pass the
+    // suffix state alone
+    pkv::MergeArgs m{prefix_launched ? o_parts : o_parts + rows * desc->head_dim,
+                     prefix_launched ? lse_parts : lse_parts + rows, out, lse_out, prefix_launched ? 2 : 1,
+                     num_seqs, desc->num_q_heads, desc->head_dim};
     cudaError_t e = pkv::launch_merge(m, s);
     if (e != cudaSuccess) return cuda_fail(e, "cascade merge launch");
     return PKV_OK;

@@ -229,11 +229,12 @@ __global__ void __launch_bounds__(256) stage_fp8_kernel(StageArgs a) {
     pdl_launch_dependents();
     const int j = blockIdx.x;
     const int s = blockIdx.y;
+    const int smbps = a.stage_mbps > 0 ? a.stage_mbps : a.mbps;
     int kv_len = a.kv_lens[s];
-    kv_len = min(kv_len, a.mbps * kBlockSize);  // the prefill kernel flags an overlong length
+    kv_len = min(kv_len, smbps * kBlockSize);  // the prefill kernel flags an overlong length
     if (j >= (kv_len + kBlockSize - 1) / kBlockSize) return;
     const int src = a.block_tables[static_cast<size_t>(s) * a.mbps + j];
-    const size_t dst = static_cast<size_t>(s) * a.mbps + j;
+    const size_t dst = static_cast<size_t>(s) * smbps + j;
     if (threadIdx.x == 0) a.stage_tables[dst] = static_cast<int32_t>(dst);
     if (src < 0 || src >= a.num_blocks) {
         if (threadIdx.x == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
@@ -268,7 +269,8 @@ __global__ void __launch_bounds__(256) stage_fp8_kernel(StageArgs a) {
 
 cudaError_t launch_stage_fp8(const StageArgs& a, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
-    return launch_pdl(stage_fp8_kernel, dim3(a.mbps, a.num_seqs), dim3(256), 0, stream, a);
+    return launch_pdl(stage_fp8_kernel, dim3(a.stage_mbps > 0 ? a.stage_mbps : a.mbps, a.num_seqs), dim3(256),
+                      0, stream, a);
 }
 
 // ---------------------------------------------------------------- merge --

@@ -497,7 +497,22 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     // Without a window a chunk's blocks do not depend on the context length:
     // read this warp's block ids (lane k: the k-th one) while the length is
     // still in flight.  Entries past the sequence's end are read but unused.
-    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.mbps;
+    // Windowed cascade prefix pass: sequence seq reads the shared prefix of
+    // its group (table row and length of the group; its own query position
+    // is prefix + suffix_len - 1, so its window starts there).
+    int row = seq;
+    if (a.group_indptr) {
+        int g_lo = 0, g_hi = a.num_groups - 1;
+        while (g_lo < g_hi) {
+            const int mid = (g_lo + g_hi + 1) >> 1;
+            if (a.group_indptr[mid] <= seq)
+                g_lo = mid;
+            else
+                g_hi = mid - 1;
+        }
+        row = g_lo;
+    }
+    const int32_t* bt = a.block_tables + static_cast<size_t>(row) * a.mbps;
     int phys = 0;
     if (a.window <= 0) {
         const int lb = split * a.chunk_blocks + warp + lane * kW;
@@ -508,7 +523,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const bool ring_lanes = a.ring > 0 && a.ring <= 32;
     int ring_id = 0;
     if (ring_lanes && lane < a.ring) ring_id = bt[lane];
-    int ctx = a.context_lens[seq];
+    int ctx = a.context_lens[row];
     // the split plan (and the workspace) covers contexts up to max_ctx, which
     // the host checked against the table capacity
     bool clamped = false;
@@ -517,7 +532,12 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         ctx = a.max_ctx;
         clamped = true;
     }
-    const int lo = (a.window > 0 && ctx > a.window) ? ctx - a.window : 0;
+    int lo = (a.window > 0 && ctx > a.window) ? ctx - a.window : 0;
+    if (a.group_indptr) {
+        // the query at position ctx + suffix - 1 sees prefix keys t >= ctx + suffix - window
+        lo = max(0, ctx + a.group_suffix_lens[seq] - a.window);
+        if (lo >= ctx) ctx = 0;
+    }
     if (ctx <= 0) {  // no visible key: o = 0, lse = -inf
         if (split == 0) {
             const size_t o0 = (static_cast<size_t>(seq) * a.hq + kvh * G) * D;

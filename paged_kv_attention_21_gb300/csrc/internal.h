@@ -52,18 +52,20 @@ struct CopyArgs {
 };
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 
-// e4m3 -> bf16 staging of the visible blocks of a batch (FP8 prefill): block
-// j < ceil(kv_lens[s] / 16) of sequence s goes to staging block s * mbps + j,
-// and the staging table gets that id.  Exact: every e4m3 code is a bf16 value.
+// e4m3 -> bf16 staging of the visible blocks of a batch (FP8 prefill, e4m3
+// cascade prefixes): block j < ceil(kv_lens[s] / 16) of sequence s goes to
+// staging block s * stage_mbps + j, and the staging table gets that id.
+// Exact: every e4m3 code is a bf16 value.
 struct StageArgs {
     const uint8_t* k_cache;   // e4m3 pools
     const uint8_t* v_cache;
     const int32_t* block_tables;
     const int32_t* kv_lens;
-    uint16_t* k_stage;        // bf16 staging pools [num_seqs * mbps][Hkv][16][D]
+    uint16_t* k_stage;        // bf16 staging pools [num_seqs * stage_mbps][Hkv][16][D]
     uint16_t* v_stage;
-    int32_t* stage_tables;    // [num_seqs][mbps]
+    int32_t* stage_tables;    // [num_seqs][stage_mbps]
     int32_t num_seqs, mbps, hkv, d;
+    int32_t stage_mbps;       // staging blocks per sequence (<= mbps; 0: mbps)
     int64_t num_blocks;
     uint32_t* err;
 };
@@ -148,6 +150,13 @@ struct DecodeArgs {
     // its first pipeline wait after inject_limit_us (see common.cuh)
     int32_t inject_timeout;
     uint32_t inject_limit_us;
+    // Windowed cascade prefix pass (group_indptr != null): sequence s reads
+    // table row and context length g, its group (group_indptr[g] <= s <
+    // group_indptr[g + 1]), with visible keys [ctx + group_suffix_lens[s] -
+    // window, ctx): the prefix keys its query's window reaches.
+    const int32_t* group_indptr;
+    const int32_t* group_suffix_lens;
+    int32_t num_groups;
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
