@@ -254,10 +254,13 @@ pkv_status pkv_decode_plan(const pkv_cache_desc *desc, int32_t num_seqs,
  *              it the plan assumes full tables.
  *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL): k = code * k_scale[h],
  *              v = code * v_scale[h] (InferX, "The kernels underneath": FP8 KV cache).
- *   workspace: >= pkv_prefill_workspace_size(...) bytes, 256-byte aligned; 0
- *              (may be NULL) for bf16 pools.  For e4m3 pools it holds a bf16
- *              copy of the batch's visible blocks (exact: every e4m3 code is a
- *              bf16 value), staged by the call before the attention kernel.
+ *   workspace: >= pkv_prefill_workspace_size(...) bytes, 256-byte aligned, or
+ *              NULL.  Only an e4m3 batch that runs the short-query kernel uses
+ *              it: a bf16 copy of the batch's visible blocks (exact: every e4m3
+ *              code is a bf16 value), staged by the call before that kernel.
+ *              The tcgen05 kernel converts each e4m3 K / V tile to f16 in
+ *              shared memory (exact) and runs f16 MMAs, q rounded to f16
+ *              (exact for |q| in [2^-14, 65504]); it takes no workspace.
  * No ring cache (PKV_ERR_UNSUPPORTED): a ring takes pkv_prefill_ring_commit. */
 pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *q,
                                         const int32_t *qo_indptr, const void *k_cache,
@@ -309,8 +312,9 @@ pkv_status pkv_prefill_ring_commit(const pkv_cache_desc *desc, const void *q, co
 size_t pkv_prefill_ring_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs, int32_t window,
                                        int32_t max_q_len);
 
-/* Host: workspace bytes pkv_prefill_attention_ragged needs: 0 for bf16 pools;
- * for e4m3, a staging copy of num_seqs * max_blocks_per_seq blocks in bf16. */
+/* Host: workspace bytes pkv_prefill_attention_ragged may need: 0 for bf16
+ * pools; for e4m3, a staging copy of num_seqs * max_blocks_per_seq blocks in
+ * bf16, used only when the batch runs the short-query kernel. */
 size_t pkv_prefill_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
                                   int32_t total_q_tokens);
 

@@ -680,13 +680,25 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
     uint32_t* err = nullptr;
     st = device_state(&err, nullptr);
     if (st != PKV_OK) return st;
-    // e4m3 pools: the batch's visible blocks are staged as bf16 (exact) in the
-    // workspace, and the kernel reads the staged pool with the scales folded in
+    // at most 64 query rows (tokens x heads of a group) per sequence: the
+    // decode-shaped short-query kernel (needs the host query lengths)
+    int sq_chunk = 0, sq_splits = 0;
+    int kv_bound = desc->max_blocks_per_seq * desc->block_size;
+    if (kv_lens_host) {
+        kv_bound = 0;
+        for (int s2 = 0; s2 < num_seqs; ++s2) kv_bound = std::max(kv_bound, kv_lens_host[s2]);
+    }
+    const bool short_q = qo_indptr_host && max_q * G <= pkv::kSqMaxRowTiles * 16 &&
+                         plan_short_query(kv_bound, max_q, window, &sq_chunk, &sq_splits);
+    // e4m3 pools: the tcgen05 kernel converts every K / V tile to f16 in shared
+    // memory.  The short-query kernel reads bf16 tiles: for it the batch's
+    // visible blocks are staged as bf16 (exact) in the workspace, and it reads
+    // the staged pool with the scales folded in.
     pkv_cache_desc staged = *desc;
     const void* kpool = k_cache;
     const void* vpool = v_cache;
     const int32_t* tables = block_tables;
-    if (fp8) {
+    if (fp8 && short_q) {
         const PrefillStageWs sw = prefill_stage_ws(desc, num_seqs);
         if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", sw.total);
         if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -715,22 +727,7 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
         vpool = g.v_stage;
         tables = g.stage_tables;
     }
-    CUtensorMap kmap, vmap;
-    st = pool_map(kpool, &staged, &kmap, kMapTileGroups);
-    if (st != PKV_OK) return st;
-    st = pool_map(vpool, &staged, &vmap, kMapTileGroups);
-    if (st != PKV_OK) return st;
     pkv::PrefillArgs a{};
-    // at most 64 query rows (tokens x heads of a group) per sequence: the
-    // decode-shaped short-query kernel (needs the host query lengths)
-    int sq_chunk = 0, sq_splits = 0;
-    int kv_bound = desc->max_blocks_per_seq * desc->block_size;
-    if (kv_lens_host) {
-        kv_bound = 0;
-        for (int s2 = 0; s2 < num_seqs; ++s2) kv_bound = std::max(kv_bound, kv_lens_host[s2]);
-    }
-    const bool short_q = qo_indptr_host && max_q * G <= pkv::kSqMaxRowTiles * 16 &&
-                         plan_short_query(kv_bound, max_q, window, &sq_chunk, &sq_splits);
     a.k_scale = fp8 || scaled_codes ? k_scale : nullptr;
     a.v_scale = fp8 || scaled_codes ? v_scale : nullptr;
     a.q = q;
@@ -779,9 +776,17 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
         if (e != cudaSuccess) return cuda_fail(e, "short-query launch");
         return PKV_OK;
     }
-    CUtensorMap qmap;
+    // tcgen05 kernel: bf16 pools through the tile-group view (one 128-byte
+    // swizzled box per (block, head), already an MMA operand); e4m3 pools
+    // through the row view (one unswizzled box of codes per (block, head))
+    CUtensorMap kmap, vmap, qmap;
+    st = pool_map(k_cache, desc, &kmap, fp8 ? kMapBlockRows : kMapTileGroups);
+    if (st != PKV_OK) return st;
+    st = pool_map(v_cache, desc, &vmap, fp8 ? kMapBlockRows : kMapTileGroups);
+    if (st != PKV_OK) return st;
     st = q_map(q, total_q_tokens, desc, G, QT, &qmap);
     if (st != PKV_OK) return st;
+    a.fp8 = fp8 ? 1 : 0;
     a.inject_timeout = (g_inject_kernels.load() >> 1) & 1;
     a.inject_limit_us = g_inject_limit_us.load();
     cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));

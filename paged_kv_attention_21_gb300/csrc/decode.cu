@@ -87,15 +87,6 @@ __device__ __forceinline__ uint32_t kv_off(int r, int chunk) {
     return static_cast<uint32_t>(u * 128 + (((chunk & 7) ^ (u & 7)) << 4));
 }
 
-// Four e4m3 codes (one 32-bit word, lowest byte first) -> two f16x2 words,
-// exactly (every e4m3 value is an f16 value).
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-}
-
 // One (block, head) tile of K or V into shared memory.
 template <bool kFp8>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int kvh,

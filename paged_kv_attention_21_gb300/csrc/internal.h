@@ -178,6 +178,9 @@ struct PrefillArgs {
     uint32_t* err;
     int32_t num_seqs, hq, hkv, group, d, mbps, causal, window, max_qtiles, q_tile;
     int32_t total_q;  // rows of q / out
+    // tcgen05 kernel: fp8 != 0 reads e4m3 pools (tensor maps of one unswizzled
+    // box per (block, head)) and converts each tile to f16 in shared memory
+    int32_t fp8;
     int64_t num_blocks;
     float sm_scale;
     // ordered != 0: grid z index i runs sequence seq_order[i], the host's

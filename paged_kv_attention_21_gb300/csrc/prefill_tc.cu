@@ -56,7 +56,7 @@ constexpr int kTcWarps = kTcVWarp + 1;  // K producer, MMA issuer, softmax warps
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;         // log2 of the largest stale-max factor
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct TcCfg {
     static constexpr int kHalves = D / 64;             // 64-column (128-byte) halves of a row
     static constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes
@@ -71,7 +71,15 @@ struct TcCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTcQTiles * kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
-    static constexpr int kBodyBytes = kOffV + kVStages * kKBytes;
+    // e4m3 pools: eight one-block slots of codes for K and eight for V (one
+    // (block, head) box each, [16 rows][D bytes]); a producer converts slot b
+    // into block b of its f16 ring stage, then refills the slot with block b
+    // of the next tile, so seven loads stay in flight behind each conversion
+    static constexpr int kStgBlkBytes = kBlockSize * D;    // one (block, head) box of codes
+    static constexpr int kStgBytes = kFp8 ? kTcBlocks * kStgBlkBytes : 0;
+    static constexpr int kOffSK = kOffV + kVStages * kKBytes;
+    static constexpr int kOffSV = kOffSK + kStgBytes;
+    static constexpr int kBodyBytes = kOffSV + kStgBytes;
     // at least 120 KB so that one CTA owns an SM (and all 512 TMEM columns)
     static constexpr int kSmemBytes = (kBodyBytes + 1024 > 120 * 1024) ? kBodyBytes + 1024 : 120 * 1024;
     static constexpr uint32_t kTmemCols = 512;            // S_A | S_B | O_A | O_B
@@ -114,12 +122,45 @@ __device__ __forceinline__ TileSpan tile_span(int tok0, int q_len, int QT, int k
     return t;
 }
 
+// One (block, head) box of e4m3 codes ([16 rows][D bytes], as the unswizzled
+// TMA box writes it) -> that block's f16 rows in a ring stage, in the layout
+// the tile-group box writes for 16-bit pools: [8-row group][64-column slice]
+// [8 rows][128 B, 16-byte chunks swizzled by the row].  Lane l converts the
+// 8 codes of chunk l % (D/8) in rows l / (D/8), + 32 / (D/8), ...: a row's
+// codes are read by consecutive lanes and its chunks land in distinct banks.
+// e4m3 -> f16 is exact.
 template <int D>
+__device__ __forceinline__ void convert_e4m3_block(const uint8_t* codes, uint8_t* dst, int lane) {
+    using C = TcCfg<D, true>;
+    constexpr int kCh = D / 8;                    // 16-byte f16 chunks of a key row
+    constexpr int kRowsPerPass = 32 / kCh;
+    constexpr int kPasses = kBlockSize / kRowsPerPass;
+    const int cg = lane % kCh;
+    const int r0 = lane / kCh;
+    // all of the lane's codes first: the loads overlap, and no store of the
+    // stage has to be ordered before a load of the slot
+    uint2 w[kPasses];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i)
+        w[i] = *reinterpret_cast<const uint2*>(codes + (r0 + i * kRowsPerPass) * D + cg * 8);
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+        const int t = r0 + i * kRowsPerPass;
+        uint4 o;
+        e4m3x4_to_f16x4(w[i].x, o.x, o.y);
+        e4m3x4_to_f16x4(w[i].y, o.z, o.w);
+        const int r = t & 7;
+        *reinterpret_cast<uint4*>(dst + (t >> 3) * C::kGrpBytes + (cg >> 3) * 1024 + r * 128 +
+                                  (((cg & 7) ^ r) << 4)) = o;
+    }
+}
+
+template <int D, bool kFp8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -132,6 +173,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t bar_p_full[kTcQTiles];
     __shared__ __align__(8) uint64_t bar_o_done[kTcQTiles];
     __shared__ __align__(8) uint64_t bar_mma_fin;  // every MMA this CTA issued is complete
+    __shared__ __align__(8) uint64_t bar_stg[2][kTcBlocks];  // e4m3: K / V code slot b has landed
+    __shared__ __align__(8) uint64_t bar_qc;       // e4m3: the softmax warps turned Q into f16
     __shared__ __align__(8) uint64_t probe;        // test hook: a barrier nothing arrives on
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
@@ -199,6 +242,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&bar_o_done[x], 1);
         }
         mbar_init(&bar_mma_fin, 1);
+        if constexpr (kFp8) {
+            for (int b = 0; b < kTcBlocks; ++b) {
+                mbar_init(&bar_stg[0][b], 1);
+                mbar_init(&bar_stg[1][b], 1);
+            }
+            mbar_init(&bar_qc, kTcSmWarps * kTcQTiles);
+        }
         if (a.inject_timeout) mbar_init(&probe, 1);
         s_fail = 0;
         tma_prefetch_desc(&qmap);
@@ -262,51 +312,119 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int ids_cur = check_ids(read_ids(0));
             int ids_next = read_ids(1);
             const CUtensorMap* map = is_v ? &vmap : &kmap;
-            for (int j = 0; j < n_tiles; ++j) {
-                if (j > 0 && (j & 3) == 0) {
-                    ids_cur = check_ids(ids_next);
-                    ids_next = read_ids((j >> 2) + 1);
-                }
-                const int blk0 = (t_begin + j) * kTcBlocks;
+            if constexpr (kFp8) {
+                // e4m3 pools: block b of every tile passes through code slot b.
+                // Lane b issues slot b's loads; the whole warp converts a
+                // landed slot into the tile's f16 ring stage, and lane b then
+                // loads block b of the next tile into it.
+                uint8_t* stg = smem + (is_v ? C::kOffSV : C::kOffSK);
+                uint64_t* sbar = bar_stg[is_v ? 1 : 0];
                 const int nst = is_v ? C::kVStages : C::kKStages;
-                const int st = j % nst;
-                uint64_t* full = is_v ? &bar_v[st] : &bar_k[st];
-                uint64_t* empty = is_v ? &bar_v_empty[st] : &bar_k_empty[st];
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(empty, ((j / nst) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
-                    if (lane == 0) atomicOr(&s_fail, 1);
-                    break;
+                int mylast = -1;   // lane b < 8: the last tile loaded into slot b
+                {   // tile 0: lane b < 8 loads its block b
+                    const int nv = min(kTcBlocks, nblk_seq - t_begin * kTcBlocks);
+                    const int id = __shfl_sync(0xFFFFFFFFu, ids_cur, lane & (kTcBlocks - 1));
+                    if (lane < nv) {
+                        mbar_arrive_expect_tx(&sbar[lane], C::kStgBlkBytes);
+                        tma_load_4d(stg + lane * C::kStgBlkBytes, map, &sbar[lane], 0, 0, kvh, id);
+                        mylast = 0;
+                    }
                 }
-                const int nvalid = min(kTcBlocks, nblk_seq - blk0);
-                uint8_t* dst = smem + (is_v ? C::kOffV : C::kOffK) + st * C::kKBytes;
-                // lane b < 8 holds block b of this tile
-                const int id = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + (lane & (kTcBlocks - 1)));
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int st = j % nst;
+                    uint64_t* full = is_v ? &bar_v[st] : &bar_k[st];
+                    uint64_t* empty = is_v ? &bar_v_empty[st] : &bar_k_empty[st];
+                    bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty, ((j / nst) & 1) ^ 1, kWaitLimitNs, abort));
+                    const int nvalid = min(kTcBlocks, nblk_seq - (t_begin + j) * kTcBlocks);
+                    const bool more = j + 1 < n_tiles;
+                    // rotate the block ids before the next tile's first load
+                    int id_next = 0, nv_next = 0;
+                    if (more) {
+                        if (((j + 1) & 3) == 0) {
+                            ids_cur = check_ids(ids_next);
+                            ids_next = read_ids(((j + 1) >> 2) + 1);
+                        }
+                        nv_next = min(kTcBlocks, nblk_seq - (t_begin + j + 1) * kTcBlocks);
+                        id_next = __shfl_sync(0xFFFFFFFFu, ids_cur,
+                                              ((j + 1) & 3) * kTcBlocks + (lane & (kTcBlocks - 1)));
+                    }
+                    uint8_t* dst = smem + (is_v ? C::kOffV : C::kOffK) + st * C::kKBytes;
+                    for (int b = 0; ok && b < nvalid; ++b) {
+                        // every lane reads the codes and writes the stage: all wait
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sbar[b], j & 1, kWaitLimitNs, abort));
+                        if (!ok) break;
+                        convert_e4m3_block<D>(stg + b * C::kStgBlkBytes, dst + b * C::kBlkBytes, lane);
+                        // the slot's codes are in registers (the stores depend
+                        // on them): the next copy into it may start
+                        __syncwarp();
+                        if (more && lane == b && b < nv_next) {
+                            mbar_arrive_expect_tx(&sbar[b], C::kStgBlkBytes);
+                            tma_load_4d(stg + b * C::kStgBlkBytes, map, &sbar[b], 0, 0, kvh, id_next);
+                            mylast = j + 1;
+                        }
+                    }
+                    if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
+                        if (lane == 0) atomicOr(&s_fail, 1);
+                        break;
+                    }
+                    // (only the last tile may have fewer than 8 blocks, so every
+                    // slot the next tile needs was refilled above)
+                    fence_proxy_async_smem();   // the stage's generic writes -> before the MMAs read it
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full);
+                }
+                // drain: every code load issued (and Q) has landed
+                if (lane < kTcBlocks && mylast >= 0) (void)mbar_wait(&sbar[lane], mylast & 1);
+                if (lane == 0 && !is_v) (void)mbar_wait(&bar_q, 0);
+                __syncwarp();
+            } else {
+                for (int j = 0; j < n_tiles; ++j) {
+                    if (j > 0 && (j & 3) == 0) {
+                        ids_cur = check_ids(ids_next);
+                        ids_next = read_ids((j >> 2) + 1);
+                    }
+                    const int blk0 = (t_begin + j) * kTcBlocks;
+                    const int nst = is_v ? C::kVStages : C::kKStages;
+                    const int st = j % nst;
+                    uint64_t* full = is_v ? &bar_v[st] : &bar_k[st];
+                    uint64_t* empty = is_v ? &bar_v_empty[st] : &bar_k_empty[st];
+                    int ok = 1;
+                    if (lane == 0) ok = mbar_wait(empty, ((j / nst) & 1) ^ 1, kWaitLimitNs, abort) ? 1 : 0;
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok || *reinterpret_cast<volatile int*>(&s_fail)) {
+                        if (lane == 0) atomicOr(&s_fail, 1);
+                        break;
+                    }
+                    const int nvalid = min(kTcBlocks, nblk_seq - blk0);
+                    uint8_t* dst = smem + (is_v ? C::kOffV : C::kOffK) + st * C::kKBytes;
+                    // lane b < 8 holds block b of this tile
+                    const int id = __shfl_sync(0xFFFFFFFFu, ids_cur, (j & 3) * kTcBlocks + (lane & (kTcBlocks - 1)));
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(full, nvalid * C::kBlkBytes);
+                    }
+                    __syncwarp();
+                    // every block's copy is issued by its own lane, in one instruction
+                    if (lane < nvalid) tma_load_5d(dst + lane * C::kBlkBytes, map, full, 0, 0, 0, 0, id * a.hkv + kvh);
+                    issued = j + 1;
+                }
+                // drain: the last load issued into each stage (and Q) has landed
+                // before this CTA may exit -- immediate unless a wait gave up
                 if (lane == 0) {
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(full, nvalid * C::kBlkBytes);
+                    if (!is_v) (void)mbar_wait(&bar_q, 0);
+                    const int nst = is_v ? C::kVStages : C::kKStages;
+                    for (int j = max(0, issued - nst); j < issued; ++j)
+                        (void)mbar_wait(is_v ? &bar_v[j % nst] : &bar_k[j % nst], (j / nst) & 1);
                 }
                 __syncwarp();
-                // every block's copy is issued by its own lane, in one instruction
-                if (lane < nvalid) tma_load_5d(dst + lane * C::kBlkBytes, map, full, 0, 0, 0, 0, id * a.hkv + kvh);
-                issued = j + 1;
             }
-            // drain: the last load issued into each stage (and Q) has landed
-            // before this CTA may exit -- immediate unless a wait gave up
-            if (lane == 0) {
-                if (!is_v) (void)mbar_wait(&bar_q, 0);
-                const int nst = is_v ? C::kVStages : C::kKStages;
-                for (int j = max(0, issued - nst); j < issued; ++j)
-                    (void)mbar_wait(is_v ? &bar_v[j % nst] : &bar_k[j % nst], (j / nst) & 1);
-            }
-            __syncwarp();
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
-        constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN, false, false);
-        constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTcM, D, false, true);
-        bool ok = n_tiles > 0 ? mbar_wait(&bar_q, 0, kWaitLimitNs, abort) : true;
+        // e4m3 pools: Q, K, V and P are all f16 (one operand type per MMA)
+        constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTcM, kTcN, false, false, kFp8);
+        constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTcM, D, false, true, kFp8);
+        bool ok = n_tiles > 0 ? mbar_wait(kFp8 ? &bar_qc : &bar_q, 0, kWaitLimitNs, abort) : true;
         ok = __all_sync(0xFFFFFFFFu, ok);
         auto active = [&](int x, int j) { return j >= jlo[x] && j < jhi[x]; };
         // S_x(j) = Q_x K_j^T, issued right behind PV_x(j-1): the MMAs run in
@@ -426,10 +544,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const uint32_t s_base = lane_base + C::col_s(x);
         const int grp_tid = (sw % kTcSmWarps) * 32 + lane;  // 0..127 within the tile's softmax group
+        bool ok = true;
+        if constexpr (kFp8) {
+            // e4m3 pools run f16 MMAs: each tile's softmax group turns its Q
+            // tile (bf16 as loaded) into f16 in place before the first S
+            if (n_tiles > 0) {
+                if (sp.ntok > 0) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_q, 0, kWaitLimitNs, abort));
+                    if (ok) {
+                        uint4* qt = reinterpret_cast<uint4*>(smem + C::kOffQ + x * C::kQBytes);
+                        for (int i = grp_tid; i < C::kQBytes / 16; i += kTcSmWarps * 32) {
+                            uint4 v = qt[i];
+                            v.x = pack2<true>(bf16_lo(v.x), bf16_hi(v.x));
+                            v.y = pack2<true>(bf16_lo(v.y), bf16_hi(v.y));
+                            v.z = pack2<true>(bf16_lo(v.z), bf16_hi(v.z));
+                            v.w = pack2<true>(bf16_lo(v.w), bf16_hi(v.w));
+                            qt[i] = v;
+                        }
+                        fence_proxy_async_smem();
+                    } else if (lane == 0) {
+                        atomicOr(&s_fail, 1);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_qc);
+            }
+        }
         float m_used = -INFINITY;
         float l = 0.f;                             // the row sum
-        bool ok = true;
-        for (int i = 0; i < nx; ++i) {
+        for (int i = 0; ok && i < nx; ++i) {
             const int j = j0 + i;
             const int k0 = (t_begin + j) * kTcN;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_s_full[x], i & 1, kWaitLimitNs, abort)) ||
@@ -523,7 +666,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const float p1 = fast_exp2(x1);
                     const uint64_t pp = pack_f32x2(p0, p1);
                     acc[u & 3] = add_f32x2(acc[u & 3], pp);
-                    pk[u] = pack2<false>(p0, p1);
+                    pk[u] = pack2<kFp8>(p0, p1);
                 }
                 tc::st16u(s_base + 16 * c, pk);
             }
@@ -606,12 +749,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kFp8>
 cudaError_t launch_prefill_tc_t(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, cudaStream_t stream) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, kFp8>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
-    auto kern = prefill_tc_kernel<D>;
+    auto kern = prefill_tc_kernel<D, kFp8>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -632,8 +775,11 @@ int prefill_tc_q_tile(int group) { return group >= 1 && group <= kTcM ? kTcM / g
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, cudaStream_t stream) {
-    return a.d == 64 ? launch_prefill_tc_t<64>(a, qmap, kmap, vmap, stream)
-                     : launch_prefill_tc_t<128>(a, qmap, kmap, vmap, stream);
+    if (a.fp8)
+        return a.d == 64 ? launch_prefill_tc_t<64, true>(a, qmap, kmap, vmap, stream)
+                         : launch_prefill_tc_t<128, true>(a, qmap, kmap, vmap, stream);
+    return a.d == 64 ? launch_prefill_tc_t<64, false>(a, qmap, kmap, vmap, stream)
+                     : launch_prefill_tc_t<128, false>(a, qmap, kmap, vmap, stream);
 }
 
 }  // namespace pkv

@@ -53,12 +53,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B, fp32 accumulate.
+// Instruction descriptor of kind::f16 with bf16 A/B (f16 A/B when f16 is
+// set: the two operands always share one type), fp32 accumulate.
 // a_mn / b_mn: operand stored MN-major (else K-major).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn, bool f16 = false) {
     return (1u << 4)                               // D format: f32
-           | (1u << 7)                             // A format: bf16
-           | (1u << 10)                            // B format: bf16
+           | (static_cast<uint32_t>(!f16) << 7)    // A format: bf16 (1) or f16 (0)
+           | (static_cast<uint32_t>(!f16) << 10)   // B format: bf16 (1) or f16 (0)
            | (static_cast<uint32_t>(a_mn) << 15)   // A major
            | (static_cast<uint32_t>(b_mn) << 16)   // B major
            | (static_cast<uint32_t>(N >> 3) << 17) // N / 8

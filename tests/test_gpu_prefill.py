@@ -195,7 +195,8 @@ def test_fp8_prefill_matches_oracle(hq, hkv, d, window, short):
     """Ragged causal prefill over e4m3 pools with per-head scales (InferX, "The
     kernels underneath": FP8 KV cache): against the oracle on the same codes.
     short: at most 64 query rows per sequence, so the staged pool is read by
-    the short-query kernel with the scales folded in."""
+    the short-query kernel with the scales folded in; otherwise the tcgen05
+    kernel converts the tiles itself, with no workspace."""
     from tests._cases import PagedCase
     rng = np.random.default_rng(80 + d + hq + (window > 0) + 7 * short)
     q_lens = [min(8, 64 // (hq // hkv)), 1, 3, 1, 1] if short else [64, 200, 77, 1, 1]
@@ -208,8 +209,10 @@ def test_fp8_prefill_matches_oracle(hq, hkv, d, window, short):
     q = t(case.q).view(torch.int16).view(torch.bfloat16) if case.q.dtype == np.uint16 else t(case.q)
     out = torch.full((T, hq, d), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.full((T, hq), float("nan"), device=DEV)
+    # the short-query kernel reads a bf16 staging copy in the workspace; the
+    # tcgen05 kernel converts e4m3 tiles in shared memory and takes none
     ws = torch.zeros(max(pkv.pkv_prefill_workspace_size(desc, len(case.lens), T), 256), dtype=torch.uint8,
-                     device=DEV)
+                     device=DEV) if short else None
     for _ in range(2):  # the staging workspace is reused
         pkv.pkv_prefill_attention_ragged(desc, q, t(case.qo), t(case.k_cache), t(case.v_cache), t(case.tables),
                                          t(case.lens), sm, out, lse, qo_indptr_host=case.qo,
@@ -221,3 +224,41 @@ def test_fp8_prefill_matches_oracle(hq, hkv, d, window, short):
         assert_close(out, ref, "fp8 prefill %d/%d/%d" % (hq, hkv, d))
         assert_lse_close(lse, ref_lse, "fp8 prefill")
     assert pkv.pkv_device_errors() == 0
+
+
+def test_fp8_mixed_step_workload_full_size():
+    """The Llama-3-8B-shaped prefill part over e4m3 pools (per-head scales: each
+    head's largest |value| / 448) through the tcgen05 kernel, which converts
+    the tiles in shared memory and takes no workspace: token by token against
+    the oracle on the same codes, for the longest and the shortest prefix."""
+    spec = wl.LLAMA3_8B_PREFILL
+    pb = wl.make_prefill_batch(spec, DEV)
+    ks = (pb.k_cache.float().abs().amax(dim=(0, 2, 3)) / 448.0).contiguous()
+    vs = (pb.v_cache.float().abs().amax(dim=(0, 2, 3)) / 448.0).contiguous()
+    k8 = (pb.k_cache.float() / ks.view(1, -1, 1, 1)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (pb.v_cache.float() / vs.view(1, -1, 1, 1)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                         head_dim=spec.head_dim, num_blocks=k8.shape[0],
+                         max_blocks_per_seq=pb.tables_host.shape[1], kv_dtype=pkv.KV_FP8_E4M3)
+    out = torch.full_like(pb.q, float("nan"))
+    lse = torch.full(pb.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    pkv.pkv_device_errors(reset=True)
+    pkv.pkv_prefill_attention_ragged(desc, pb.q, pb.qo_indptr, k8, v8, pb.block_tables, pb.kv_lens,
+                                     spec.sm_scale, out, lse, qo_indptr_host=pb.qo_indptr_host,
+                                     kv_lens_host=pb.kv_lens_host, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_errors() == 0
+    seqs = sorted({int(np.argmax(pb.prefix_host)), int(np.argmin(pb.prefix_host))})
+    k, v, tabs = compact_pool(k8, v8, pb.tables_host, seqs)
+    qo = pb.qo_indptr_host
+    rows = np.concatenate([np.arange(qo[s], qo[s + 1]) for s in seqs])
+    sub_qo = np.concatenate([[0], np.cumsum([qo[s + 1] - qo[s] for s in seqs])]).astype(np.int32)
+    ref, ref_lse = oracle.paged_attention(q=u16(pb.q)[rows], k_cache=k, v_cache=v, block_tables=tabs,
+                                          qo_indptr=sub_qo, kv_lens=pb.kv_lens_host[seqs],
+                                          num_q_heads=spec.num_q_heads,
+                                          num_kv_heads=spec.num_kv_heads, sm_scale=spec.sm_scale,
+                                          kv_dtype=1, k_scale=ks.cpu().numpy(),
+                                          v_scale=vs.cpu().numpy(), nthreads=NTHREADS)
+    sel = torch.from_numpy(rows).to(DEV)
+    assert_close(out[sel], ref, "mixed-step prefill over e4m3")
+    assert_lse_close(lse[sel], ref_lse, "mixed-step prefill over e4m3")
