@@ -351,8 +351,11 @@ pkv_status pkv_merge_states(const float *o_parts, const float *lse_parts, int32_
  *   suffix_tables: int32 [num_seqs][max_blocks_per_seq]; suffix_lens: int32
  *               [num_seqs], each in [1, max_suffix_len] (the new token is in the suffix).
  *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL), as in
- *               pkv_decode_attention; the groups' prefix blocks are then
- *               staged as exact bf16 copies in the workspace first.
+ *               pkv_decode_attention.  A prefix pass on the tcgen05 kernel
+ *               converts the e4m3 tiles in shared memory; one on the
+ *               short-query kernel (groups of at most 64 query rows) reads
+ *               the groups' prefix blocks staged as exact bf16 copies in the
+ *               workspace first.
  *   window   : <= 0 for full attention; > 0 a sliding window over each
  *               sequence's positions (its query at prefix + suffix_len - 1
  *               sees keys t > that position - window).  A window reaches at

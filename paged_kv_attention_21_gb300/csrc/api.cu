@@ -1214,12 +1214,20 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         prefix_launched = true;
     } else if (window <= 0) {
         const int QT = pkv::prefill_tc_q_tile(G);
-        // e4m3 pools: the groups' prefix blocks as exact bf16 copies
+        // a group's queries (at most 64 rows) over its prefix: the short-query
+        // kernel; more: the tcgen05 prefill (non-causal, fp32 state out)
+        const int max_qtiles = (max_group + QT - 1) / QT;
+        int sq_chunk = 0, sq_splits = 0;
+        const bool short_q = max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
+                             plan_short_query(max_prefix, max_group, -1, &sq_chunk, &sq_splits);
+        // e4m3 pools: the tcgen05 kernel converts each tile in shared memory;
+        // the short-query kernel reads the groups' prefix blocks as exact
+        // bf16 copies staged in the workspace
         pkv_cache_desc pd = *desc;
         const void* kpool = k_cache;
         const void* vpool = v_cache;
         const int32_t* ptables = prefix_tables;
-        if (fp8 && max_prefix > 0) {
+        if (fp8 && short_q && max_prefix > 0) {
             const size_t blocks = size_t(num_groups) * ws.stage_mbps;
             const size_t block_bytes = size_t(desc->num_kv_heads) * desc->block_size * desc->head_dim * 2;
             uint8_t* sb = wsb + ws.stage;
@@ -1248,13 +1256,6 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
             vpool = g.v_stage;
             ptables = g.stage_tables;
         }
-        CUtensorMap kmap, vmap, qmap;
-        st = pool_map(kpool, &pd, &kmap, kMapTileGroups);
-        if (st != PKV_OK) return st;
-        st = pool_map(vpool, &pd, &vmap, kMapTileGroups);
-        if (st != PKV_OK) return st;
-        st = q_map(q, num_seqs, desc, G, QT, &qmap);
-        if (st != PKV_OK) return st;
         pkv::PrefillArgs a{};
         a.q = q;
         a.k_scale = fp8 ? k_scale : nullptr;
@@ -1274,15 +1275,12 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.mbps = pd.max_blocks_per_seq;
         a.causal = 0;
         a.window = -1;
-        a.max_qtiles = (max_group + QT - 1) / QT;
+        a.max_qtiles = max_qtiles;
         a.q_tile = QT;
         a.total_q = num_seqs;
         a.num_blocks = pd.num_blocks;
         a.sm_scale = sm_scale;
-        int sq_chunk = 0, sq_splits = 0;
-        if (a.max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
-            plan_short_query(max_prefix, max_group, -1, &sq_chunk, &sq_splits)) {
-            // a group's queries (at most 64 rows) over its prefix: short-query kernel
+        if (short_q) {
             CUtensorMap tkmap, tvmap;
             st = pool_map(kpool, &pd, &tkmap, kMapTileRows);
             if (st != PKV_OK) return st;
@@ -1294,7 +1292,15 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
             cudaError_t e = pkv::launch_short_query(a, tkmap, tvmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
             prefix_launched = true;
-        } else if (a.max_qtiles > 0) {
+        } else if (max_qtiles > 0) {
+            CUtensorMap kmap, vmap, qmap;
+            st = pool_map(k_cache, desc, &kmap, fp8 ? kMapBlockRows : kMapTileGroups);
+            if (st != PKV_OK) return st;
+            st = pool_map(v_cache, desc, &vmap, fp8 ? kMapBlockRows : kMapTileGroups);
+            if (st != PKV_OK) return st;
+            st = q_map(q, num_seqs, desc, G, QT, &qmap);
+            if (st != PKV_OK) return st;
+            a.fp8 = fp8 ? 1 : 0;
             cudaError_t e = pkv::launch_prefill_tc(a, qmap, kmap, vmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
             prefix_launched = true;

@@ -91,6 +91,7 @@ def _concatenated(c, hkv, d):
 @pytest.mark.parametrize("hq,hkv,d,fp8,window,big", [
     (32, 8, 128, False, -1, False), (16, 2, 128, False, -1, False), (8, 2, 64, False, -1, False),
     (32, 8, 128, True, -1, False), (64, 8, 64, True, -1, False), (32, 8, 128, True, -1, True),
+    (64, 8, 64, True, -1, True),
     (32, 8, 128, False, 128, False), (16, 2, 128, False, 40, False), (64, 8, 64, True, 128, False),
     (8, 2, 64, True, 2000, False)])
 def test_cascade_equals_attention_over_the_concatenated_keys(hq, hkv, d, fp8, window, big):
