@@ -159,3 +159,53 @@ def test_prefill_wait_timeout_gives_up_cleanly():
     assert pkv.pkv_device_errors(reset=True) == 0
     assert_close(out2, ref, "prefill after the hook is disarmed")
     assert_lse_close(lse2, ref_lse, "prefill after the hook is disarmed")
+
+
+def test_fp8_prefill_wait_timeout_gives_up_cleanly():
+    """The same give-up over e4m3 pools: the producers convert code slots in
+    shared memory, so their drain (every code load issued, and Q) and the
+    softmax warps' Q conversion take part in it."""
+    import oracle
+    from tests._gpu import NTHREADS, u8
+    spec = _small()
+    pb = wl.make_prefill_batch(spec, "cpu", q_lens=[96, 1, 37, 130], prefixes=[0, 0, 515, 515])
+    ks = (pb.k_cache.float().abs().amax(dim=(0, 2, 3)) / 448.0).contiguous()
+    vs = (pb.v_cache.float().abs().amax(dim=(0, 2, 3)) / 448.0).contiguous()
+    k8 = (pb.k_cache.float() / ks.view(1, -1, 1, 1)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (pb.v_cache.float() / vs.view(1, -1, 1, 1)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                         head_dim=spec.head_dim, num_blocks=k8.shape[0],
+                         max_blocks_per_seq=pb.tables_host.shape[1], kv_dtype=pkv.KV_FP8_E4M3)
+    ref, ref_lse = oracle.paged_attention(
+        q=u16(pb.q), k_cache=u8(k8), v_cache=u8(v8), block_tables=pb.tables_host,
+        qo_indptr=pb.qo_indptr_host, kv_lens=pb.kv_lens_host, num_q_heads=spec.num_q_heads,
+        num_kv_heads=spec.num_kv_heads, sm_scale=spec.sm_scale, kv_dtype=1, k_scale=ks.numpy(),
+        v_scale=vs.numpy(), nthreads=NTHREADS)
+
+    def call():
+        out = torch.full((pb.total_q, spec.num_q_heads, spec.head_dim), float("nan"),
+                         dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((pb.total_q, spec.num_q_heads), float("nan"), device=DEV)
+        pkv.pkv_prefill_attention_ragged(desc, pb.q.to(DEV), torch.from_numpy(pb.qo_indptr_host).to(DEV),
+                                         k8.to(DEV), v8.to(DEV), torch.from_numpy(pb.tables_host).to(DEV),
+                                         torch.from_numpy(pb.kv_lens_host).to(DEV), spec.sm_scale, out, lse,
+                                         qo_indptr_host=pb.qo_indptr_host, kv_lens_host=pb.kv_lens_host,
+                                         k_scale=ks.to(DEV), v_scale=vs.to(DEV))
+        torch.cuda.synchronize()
+        return out, lse
+
+    pkv.pkv_device_errors(reset=True)
+    pkv.pkv_test_inject_wait_timeout(2, LIMIT_US)
+    try:
+        out, lse = call()
+    finally:
+        pkv.pkv_test_inject_wait_timeout(0)
+    assert pkv.pkv_device_errors(reset=True) & pkv.DEVERR_TIMEOUT
+    G = spec.num_q_heads // spec.num_kv_heads
+    assert torch.isfinite(out.float()).all()
+    assert_close(out[:, G:], ref[:, G:], "e4m3 prefill after a give-up")
+    assert_lse_close(lse[:, G:], ref_lse[:, G:], "e4m3 prefill after a give-up")
+    out2, lse2 = call()
+    assert pkv.pkv_device_errors(reset=True) == 0
+    assert_close(out2, ref, "e4m3 prefill after the hook is disarmed")
+    assert_lse_close(lse2, ref_lse, "e4m3 prefill after the hook is disarmed")
