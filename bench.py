@@ -54,10 +54,11 @@ def parse_args():
     p.add_argument("--no-carry", action="store_true",
                    help="skip the Qwen2.5-3B decode figures carried beside the mixed step")
     p.add_argument("--part", choices=["step", "prefill", "cascade", "verify", "cow", "ring",
-                                      "fp8-prefill"], default="step",
+                                      "ring-prefill", "fp8-prefill"], default="step",
                    help="step: the workload's whole step (default); prefill: the ragged causal "
                         "prefill part of workload 4 alone, timed against the tensor-core peak; "
-                        "cascade / verify / cow / ring / fp8-prefill: the next-step rows, each "
+                        "cascade / verify / cow / ring / ring-prefill / fp8-prefill: the next-step "
+                        "rows, each "
                         "on its own seeded workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk-blocks", type=int, default=0,
@@ -983,6 +984,9 @@ def main_next(args, rank, world, local):
       cow         copy-on-write of 4096 whole blocks of that pool, GB/s moved;
       ring        the FP8 workload's window-128 layer over a 9-block ring cache with sink
                   logits, one decode step (append + decode), KV GB/s;
+      ring-prefill the FP8 workload's window layer taking a 512-token prefill chunk per
+                  sequence over its 9-block ring: staging of the window, the cache commit
+                  and the ragged prefill, GB/s of the bytes the path must move;
       fp8-prefill the Llama-3-8B-shaped prefill part over e4m3 pools (tcgen05 prefill,
                   tiles converted to f16 in shared memory), TFLOP/s."""
     import paged_kv_attention_21_gb300 as pkv
@@ -1151,6 +1155,65 @@ def main_next(args, rank, world, local):
                     "kernel": "decode_kernel (fused append, ring tables, sinks)",
                     "peak_source": "%s hbm_gbs" % hbm_kind, "algorithmic_bytes_per_launch": nbytes},
                    1, clocks)
+        return
+
+    if part == "ring-prefill":
+        # 8 sequences of the FP8 workload's window layer each take a chunk of
+        # 512 prompt tokens over a cached prefix U[1024, 16384], through the
+        # ring cache: stage the window, commit the chunk, run the prefill
+        spec = wl.FP8_DECODE
+        R, window = wl.FP8_RING, wl.FP8_WINDOW
+        rng = np.random.default_rng(spec.seed + 13 + 7919 * rank)
+        B, ql = 8, 512
+        prefix = rng.integers(spec.ctx_lo, spec.ctx_hi + 1, size=B).astype(np.int32)
+        kv = (prefix + ql).astype(np.int32)
+        g = torch.Generator(device=dev).manual_seed(spec.seed + 13 + 7919 * rank)
+        shape = (B * R, spec.num_kv_heads, spec.block_size, spec.head_dim)
+        kc, ks = wl.fill_e4m3(shape, g, dev)
+        vc, vs = wl.fill_e4m3(shape, g, dev)
+        perm = rng.permutation(B * R).astype(np.int32).reshape(B, R)
+        tabs = torch.from_numpy(perm).to(dev)
+        T = B * ql
+        qo = np.arange(0, T + 1, ql, dtype=np.int32)
+        q = wl.fill_bf16((T, spec.num_q_heads, spec.head_dim), g, dev)
+        kch = wl.fill_bf16((T, spec.num_kv_heads, spec.head_dim), g, dev)
+        vch = wl.fill_bf16((T, spec.num_kv_heads, spec.head_dim), g, dev)
+        desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                             head_dim=spec.head_dim, num_blocks=B * R, max_blocks_per_seq=R,
+                             kv_dtype=pkv.KV_FP8_E4M3, ring_blocks=R)
+        ws = torch.empty(pkv.pkv_prefill_ring_workspace_size(desc, B, window, ql), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty_like(q)
+        qo_d = torch.from_numpy(qo).to(dev)
+        kv_d = torch.from_numpy(kv).to(dev)
+        run = lambda: pkv.pkv_prefill_ring_commit(desc, q, qo_d, kch, vch, kc, vc, tabs, kv_d,
+                                                  spec.sm_scale, window, out, qo, kv, ws,
+                                                  k_scale=ks, v_scale=vs)
+        times, clocks = _timed_launches(run, K, W, dev, flush)
+        ms = reduce_max(float(np.mean(times)), world)
+        if rank:
+            return
+        # bytes the path must move: the ring keys of each window below the
+        # chunk (e4m3 K and V), the chunk's K and V (bf16), the committed ring
+        # slots (e4m3 K and V), q in and o out (bf16)
+        H, D, Hq = spec.num_kv_heads, spec.head_dim, spec.num_q_heads
+        below = int(np.minimum(prefix, window - 1).sum())
+        committed = B * min(ql, R * spec.block_size)
+        nbytes = (below * H * D * 2 + T * H * D * 2 * 2 + committed * H * D * 2 +
+                  2 * T * Hq * D * 2)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        _part_line(args, world, "sliding-window (128) ring-cache prefill with the cache commit, "
+                   "GB/s of the bytes the path must move", gbs * world, "GB/s", times,
+                   "e4m3 ring, bf16 chunk K/V, q and o, fp32 accumulate",
+                   {"workload": "FP8 workload's window layer (64/8 heads, D64, 9-block ring per "
+                                "sequence): 8 sequences x 512-token chunks over prefixes "
+                                "U[1024,16384]", "q_tokens": T,
+                    "query_tokens_per_s": round(T / (ms / 1e3), 1)},
+                   {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4), "traffic": None,
+                    "kernel": "stage_ring_kernel + commit_ring_kernel + prefill_tc_kernel",
+                    "peak_source": "%s hbm_gbs" % hbm_kind, "algorithmic_bytes_per_launch": nbytes},
+                   3, clocks)
         return
 
     # fp8-prefill: workload 4's prefill part with its pools quantised to e4m3

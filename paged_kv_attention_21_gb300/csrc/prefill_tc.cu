@@ -604,15 +604,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 mx *= scale_log2;  // scale_log2 > 0: the max commutes with it
             } else {
-                mx = -INFINITY;
+                // the row sees keys [key_lo, key_hi]: one unsigned compare per score
+                const int key_hi = a.causal ? min(pos, kv_len - 1) : kv_len - 1;
+                const int key_lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+                const uint32_t cnt = key_hi >= key_lo ? static_cast<uint32_t>(key_hi + 1 - key_lo) : 0u;
+                const int base = k0 - key_lo;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int e = 0; e < kTcN; ++e) {
-                    const int key = k0 + e;
-                    const bool vis = key < kv_len && (!a.causal || key <= pos) &&
-                                     (a.window <= 0 || key > pos - a.window);
+                    const bool vis = static_cast<uint32_t>(base + e) < cnt;
                     sv[e] = vis ? sv[e] * scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[e]);
+                    m4[e & 3] = fmaxf(m4[e & 3], sv[e]);
                 }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
             // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
             const float m_new = fmaxf(m_used, mx);
