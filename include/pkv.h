@@ -254,13 +254,12 @@ pkv_status pkv_decode_plan(const pkv_cache_desc *desc, int32_t num_seqs,
  *              it the plan assumes full tables.
  *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL): k = code * k_scale[h],
  *              v = code * v_scale[h] (InferX, "The kernels underneath": FP8 KV cache).
- *   workspace: >= pkv_prefill_workspace_size(...) bytes, 256-byte aligned, or
- *              NULL.  Only an e4m3 batch that runs the short-query kernel uses
- *              it: a bf16 copy of the batch's visible blocks (exact: every e4m3
- *              code is a bf16 value), staged by the call before that kernel.
- *              The tcgen05 kernel converts each e4m3 K / V tile to f16 in
- *              shared memory (exact) and runs f16 MMAs, q rounded to f16
- *              (exact for |q| in [2^-14, 65504]); it takes no workspace.
+ *   workspace: unused (may be NULL; pkv_prefill_workspace_size returns 0).
+ *              Over e4m3 pools both kernels read the codes and convert them
+ *              exactly on chip: the tcgen05 kernel into f16 tiles in shared
+ *              memory, the short-query kernel into f16 MMA fragments; the
+ *              MMAs are f16 with q rounded to f16 (exact for |q| in
+ *              [2^-14, 65504]) and P in f16.
  * No ring cache (PKV_ERR_UNSUPPORTED): a ring takes pkv_prefill_ring_commit. */
 pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc *desc, const void *q,
                                         const int32_t *qo_indptr, const void *k_cache,
@@ -312,9 +311,8 @@ pkv_status pkv_prefill_ring_commit(const pkv_cache_desc *desc, const void *q, co
 size_t pkv_prefill_ring_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs, int32_t window,
                                        int32_t max_q_len);
 
-/* Host: workspace bytes pkv_prefill_attention_ragged may need: 0 for bf16
- * pools; for e4m3, a staging copy of num_seqs * max_blocks_per_seq blocks in
- * bf16, used only when the batch runs the short-query kernel. */
+/* Host: workspace bytes pkv_prefill_attention_ragged needs: 0 (every path
+ * reads bf16 and e4m3 pools directly; kept so that callers may size one). */
 size_t pkv_prefill_workspace_size(const pkv_cache_desc *desc, int32_t num_seqs,
                                   int32_t total_q_tokens);
 
@@ -351,11 +349,7 @@ pkv_status pkv_merge_states(const float *o_parts, const float *lse_parts, int32_
  *   suffix_tables: int32 [num_seqs][max_blocks_per_seq]; suffix_lens: int32
  *               [num_seqs], each in [1, max_suffix_len] (the new token is in the suffix).
  *   k_scale, v_scale: fp32 [Hkv], e4m3 pools only (else NULL), as in
- *               pkv_decode_attention.  A prefix pass on the tcgen05 kernel
- *               converts the e4m3 tiles in shared memory; one on the
- *               short-query kernel (groups of at most 64 query rows) reads
- *               the groups' prefix blocks staged as exact bf16 copies in the
- *               workspace first.
+ *               pkv_decode_attention; every pass reads the codes directly.
  *   window   : <= 0 for full attention; > 0 a sliding window over each
  *               sequence's positions (its query at prefix + suffix_len - 1
  *               sees keys t > that position - window).  A window reaches at

@@ -349,22 +349,6 @@ DecodeWs decode_ws_layout(const pkv_cache_desc* d, int num_seqs, int splits) {
     return w;
 }
 
-// FP8 prefill staging: a bf16 copy of every visible block of the batch,
-// block j of sequence s at s * max_blocks_per_seq + j, and its table.
-struct PrefillStageWs {
-    size_t tables, k, v, total;
-};
-PrefillStageWs prefill_stage_ws(const pkv_cache_desc* d, int num_seqs) {
-    PrefillStageWs w{};
-    const size_t blocks = size_t(num_seqs) * d->max_blocks_per_seq;
-    const size_t block_bytes = size_t(d->num_kv_heads) * d->block_size * d->head_dim * 2;
-    w.tables = 0;
-    w.k = align256(blocks * sizeof(int32_t));
-    w.v = w.k + align256(blocks * block_bytes);
-    w.total = w.v + align256(blocks * block_bytes);
-    return w;
-}
-
 }  // namespace
 
 namespace pkv {
@@ -621,9 +605,11 @@ pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, const void
 
 size_t pkv_prefill_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs,
                                   int32_t total_q_tokens) {
+    // every prefill path reads the pools (bf16 or e4m3) directly
+    (void)desc;
+    (void)num_seqs;
     (void)total_q_tokens;
-    if (check_desc(desc) != PKV_OK || num_seqs <= 0 || desc->kv_dtype != PKV_KV_FP8_E4M3) return 0;
-    return prefill_stage_ws(desc, num_seqs).total;
+    return 0;
 }
 
 }  // extern "C"
@@ -690,43 +676,13 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
     }
     const bool short_q = qo_indptr_host && max_q * G <= pkv::kSqMaxRowTiles * 16 &&
                          plan_short_query(kv_bound, max_q, window, &sq_chunk, &sq_splits);
-    // e4m3 pools: the tcgen05 kernel converts every K / V tile to f16 in shared
-    // memory.  The short-query kernel reads bf16 tiles: for it the batch's
-    // visible blocks are staged as bf16 (exact) in the workspace, and it reads
-    // the staged pool with the scales folded in.
-    pkv_cache_desc staged = *desc;
+    // e4m3 pools: both kernels read the codes and convert them on chip (the
+    // tcgen05 kernel into f16 tiles in shared memory, the short-query kernel
+    // into f16 MMA fragments), with the scales folded in; no workspace
+    const pkv_cache_desc staged = *desc;
     const void* kpool = k_cache;
     const void* vpool = v_cache;
     const int32_t* tables = block_tables;
-    if (fp8 && short_q) {
-        const PrefillStageWs sw = prefill_stage_ws(desc, num_seqs);
-        if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", sw.total);
-        if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-        if (workspace_bytes < sw.total)
-            return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, sw.total);
-        uint8_t* wsb = static_cast<uint8_t*>(workspace);
-        pkv::StageArgs g{};
-        g.k_cache = static_cast<const uint8_t*>(k_cache);
-        g.v_cache = static_cast<const uint8_t*>(v_cache);
-        g.block_tables = block_tables;
-        g.kv_lens = kv_lens;
-        g.k_stage = reinterpret_cast<uint16_t*>(wsb + sw.k);
-        g.v_stage = reinterpret_cast<uint16_t*>(wsb + sw.v);
-        g.stage_tables = reinterpret_cast<int32_t*>(wsb + sw.tables);
-        g.num_seqs = num_seqs;
-        g.mbps = desc->max_blocks_per_seq;
-        g.hkv = desc->num_kv_heads;
-        g.d = desc->head_dim;
-        g.num_blocks = desc->num_blocks;
-        g.err = err;
-        cudaError_t e = pkv::launch_stage_fp8(g, reinterpret_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "FP8 staging launch");
-        staged.kv_dtype = PKV_KV_BF16;
-        staged.num_blocks = static_cast<int64_t>(num_seqs) * desc->max_blocks_per_seq;
-        kpool = g.k_stage;
-        vpool = g.v_stage;
-        tables = g.stage_tables;
-    }
     pkv::PrefillArgs a{};
     a.k_scale = fp8 || scaled_codes ? k_scale : nullptr;
     a.v_scale = fp8 || scaled_codes ? v_scale : nullptr;
@@ -772,6 +728,7 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
         a.sq_chunk = sq_chunk;
         a.sq_splits = sq_splits;
         a.sq_row_tiles = (max_q * G + 15) / 16;
+        a.fp8 = fp8 ? 1 : 0;
         cudaError_t e = pkv::launch_short_query(a, tkmap, tvmap, reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "short-query launch");
         return PKV_OK;
@@ -1065,16 +1022,15 @@ pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_
 // query sees the whole prefix), which reads each prefix block once for the
 // whole group; each sequence's own suffix goes through the decode kernel;
 // the two fp32 (o, lse) states merge exactly as split-KV partials do.
-// e4m3 pools: the groups' prefix blocks are first staged as bf16 (exact),
-// and the prefix pass folds the scales in.  With a sliding window a query
+// e4m3 pools: the prefix pass reads the codes and folds the scales in, as
+// the prefill does.  With a sliding window a query
 // sees at most window - 1 prefix keys, the last ones before its suffix, and
 // they differ per sequence: the prefix pass is then the decode kernel over
 // the group's prefix table with each sequence's own window start.
 
 namespace {
 struct CascadeWs {
-    size_t o, lse, dec, dec_bytes, pre, pre_bytes, stage, stage_bytes, total;
-    int stage_mbps;
+    size_t o, lse, dec, dec_bytes, pre, pre_bytes, total;
 };
 CascadeWs cascade_ws_layout(const pkv_cache_desc* d, int num_groups, int num_seqs, int max_prefix_len,
                             int max_suffix_len, int window, int sms) {
@@ -1090,14 +1046,8 @@ CascadeWs cascade_ws_layout(const pkv_cache_desc* d, int num_groups, int num_seq
     if (window > 0 && max_prefix_len > 0 &&
         plan_decode(d, num_seqs, max_prefix_len, window, sms, 0, &c, &sp) == PKV_OK)
         w.pre_bytes = decode_ws_layout(d, num_seqs, sp).total;
-    w.stage = w.pre + align256(w.pre_bytes);
-    w.stage_mbps = std::max(1, (max_prefix_len + 15) / 16);
-    if (window <= 0 && d->kv_dtype == PKV_KV_FP8_E4M3 && max_prefix_len > 0) {
-        const size_t blocks = size_t(num_groups) * w.stage_mbps;
-        const size_t block_bytes = size_t(d->num_kv_heads) * d->block_size * d->head_dim * 2;
-        w.stage_bytes = align256(blocks * sizeof(int32_t)) + 2 * align256(blocks * block_bytes);
-    }
-    w.total = w.stage + w.stage_bytes;
+    w.total = w.pre + align256(w.pre_bytes);
+    (void)num_groups;
     return w;
 }
 }  // namespace
@@ -1220,42 +1170,11 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         int sq_chunk = 0, sq_splits = 0;
         const bool short_q = max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
                              plan_short_query(max_prefix, max_group, -1, &sq_chunk, &sq_splits);
-        // e4m3 pools: the tcgen05 kernel converts each tile in shared memory;
-        // the short-query kernel reads the groups' prefix blocks as exact
-        // bf16 copies staged in the workspace
-        pkv_cache_desc pd = *desc;
+        // e4m3 pools: either kernel converts the codes on chip, scales folded in
+        const pkv_cache_desc pd = *desc;
         const void* kpool = k_cache;
         const void* vpool = v_cache;
         const int32_t* ptables = prefix_tables;
-        if (fp8 && short_q && max_prefix > 0) {
-            const size_t blocks = size_t(num_groups) * ws.stage_mbps;
-            const size_t block_bytes = size_t(desc->num_kv_heads) * desc->block_size * desc->head_dim * 2;
-            uint8_t* sb = wsb + ws.stage;
-            pkv::StageArgs g{};
-            g.k_cache = static_cast<const uint8_t*>(k_cache);
-            g.v_cache = static_cast<const uint8_t*>(v_cache);
-            g.block_tables = prefix_tables;
-            g.kv_lens = prefix_lens;
-            g.stage_tables = reinterpret_cast<int32_t*>(sb);
-            g.k_stage = reinterpret_cast<uint16_t*>(sb + align256(blocks * sizeof(int32_t)));
-            g.v_stage = reinterpret_cast<uint16_t*>(sb + align256(blocks * sizeof(int32_t)) +
-                                                    align256(blocks * block_bytes));
-            g.num_seqs = num_groups;
-            g.mbps = desc->max_blocks_per_seq;
-            g.stage_mbps = ws.stage_mbps;
-            g.hkv = desc->num_kv_heads;
-            g.d = desc->head_dim;
-            g.num_blocks = desc->num_blocks;
-            g.err = err;
-            cudaError_t e = pkv::launch_stage_fp8(g, s);
-            if (e != cudaSuccess) return cuda_fail(e, "cascade prefix staging launch");
-            pd.kv_dtype = PKV_KV_BF16;
-            pd.num_blocks = static_cast<int64_t>(blocks);
-            pd.max_blocks_per_seq = ws.stage_mbps;
-            kpool = g.k_stage;
-            vpool = g.v_stage;
-            ptables = g.stage_tables;
-        }
         pkv::PrefillArgs a{};
         a.q = q;
         a.k_scale = fp8 ? k_scale : nullptr;
@@ -1289,6 +1208,7 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
             a.sq_chunk = sq_chunk;
             a.sq_splits = sq_splits;
             a.sq_row_tiles = (max_group * G + 15) / 16;
+            a.fp8 = fp8 ? 1 : 0;
             cudaError_t e = pkv::launch_short_query(a, tkmap, tvmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
             prefix_launched = true;

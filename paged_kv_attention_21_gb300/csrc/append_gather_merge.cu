@@ -219,60 +219,6 @@ cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
     return launch_pdl(copy_blocks_kernel, dim3(a.num_pairs, 2), dim3(256), 0, stream, a);
 }
 
-// --------------------------------------------------- FP8 prefill staging --
-//
-// One CTA per (block slot j, sequence); 16 e4m3 codes per thread step become
-// 16 bf16 values (via f16, exact for every code, NaN included).
-
-__global__ void __launch_bounds__(256) stage_fp8_kernel(StageArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int j = blockIdx.x;
-    const int s = blockIdx.y;
-    const int smbps = a.stage_mbps > 0 ? a.stage_mbps : a.mbps;
-    int kv_len = a.kv_lens[s];
-    kv_len = min(kv_len, smbps * kBlockSize);  // the prefill kernel flags an overlong length
-    if (j >= (kv_len + kBlockSize - 1) / kBlockSize) return;
-    const int src = a.block_tables[static_cast<size_t>(s) * a.mbps + j];
-    const size_t dst = static_cast<size_t>(s) * smbps + j;
-    if (threadIdx.x == 0) a.stage_tables[dst] = static_cast<int32_t>(dst);
-    if (src < 0 || src >= a.num_blocks) {
-        if (threadIdx.x == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-        return;
-    }
-    const size_t block_elems = static_cast<size_t>(a.hkv) * kBlockSize * a.d;
-    const int n16 = static_cast<int>(block_elems / 16);
-    for (int pool = 0; pool < 2; ++pool) {
-        const uint4* in = reinterpret_cast<const uint4*>((pool ? a.v_cache : a.k_cache) + src * block_elems);
-        uint4* outp = reinterpret_cast<uint4*>((pool ? a.v_stage : a.k_stage) + dst * block_elems);
-        for (int c = threadIdx.x; c < n16; c += blockDim.x) {
-            const uint4 v = in[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(
-                        static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hh)) & 0xFFFFu), __NV_E4M3);
-                    __half2 hv;
-                    *reinterpret_cast<__half2_raw*>(&hv) = h2;
-                    const float2 f = __half22float2(hv);
-                    o[2 * i + hh] = pack2<false>(f.x, f.y);  // bf16, exact
-                }
-            }
-            outp[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
-            outp[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-    }
-}
-
-cudaError_t launch_stage_fp8(const StageArgs& a, cudaStream_t stream) {
-    if (a.num_seqs == 0) return cudaSuccess;
-    return launch_pdl(stage_fp8_kernel, dim3(a.stage_mbps > 0 ? a.stage_mbps : a.mbps, a.num_seqs), dim3(256),
-                      0, stream, a);
-}
-
 // ---------------------------------------------------------------- merge --
 //
 // One warp per (row, head); lanes stride over head_dim.

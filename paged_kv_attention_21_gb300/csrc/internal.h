@@ -52,25 +52,6 @@ struct CopyArgs {
 };
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 
-// e4m3 -> bf16 staging of the visible blocks of a batch (FP8 prefill, e4m3
-// cascade prefixes): block j < ceil(kv_lens[s] / 16) of sequence s goes to
-// staging block s * stage_mbps + j, and the staging table gets that id.
-// Exact: every e4m3 code is a bf16 value.
-struct StageArgs {
-    const uint8_t* k_cache;   // e4m3 pools
-    const uint8_t* v_cache;
-    const int32_t* block_tables;
-    const int32_t* kv_lens;
-    uint16_t* k_stage;        // bf16 staging pools [num_seqs * stage_mbps][Hkv][16][D]
-    uint16_t* v_stage;
-    int32_t* stage_tables;    // [num_seqs][stage_mbps]
-    int32_t num_seqs, mbps, hkv, d;
-    int32_t stage_mbps;       // staging blocks per sequence (<= mbps; 0: mbps)
-    int64_t num_blocks;
-    uint32_t* err;
-};
-cudaError_t launch_stage_fp8(const StageArgs& a, cudaStream_t stream);
-
 // Ring-cache prefill (RustInfer, "Status": Tensor Core prefill over an SWA
 // ring cache, followed by a stream-ordered cache commit).  Sequence s has
 // q_len = qo_indptr[s+1] - qo_indptr[s] new tokens at positions [kv_len -

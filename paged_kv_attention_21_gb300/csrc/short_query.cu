@@ -29,9 +29,11 @@ constexpr int kSqWarps = 4;
 constexpr int kSqThreads = kSqWarps * 32;
 constexpr int kSqStages = 2;  // per-warp ring of (K, V) block tiles
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct SqCfg {
-    static constexpr int kTileBytes = kBlockSize * D * 2;  // one bf16 (block, head) tile
+    // one (block, head) tile: bf16 (128-byte swizzled slices) or e4m3 (one
+    // unswizzled row of D bytes per token)
+    static constexpr int kTileBytes = kBlockSize * D * (kFp8 ? 1 : 2);
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kWarpBytes = kSqStages * kStageBytes;
     static constexpr int kCombStride = D + 8;  // fp32 row stride of the combine buffer
@@ -51,11 +53,15 @@ __device__ __forceinline__ uint32_t sq_off(int r, int chunk) {
 
 // One CTA = (chunk, KV head and 16-row tile, sequence).  Rows of tile t are
 // R = 16 t + r -> query token R / G, head R % G of the KV group.
-template <int D, bool kCluster>
+// kFp8: e4m3 pools, read straight into f16 MMA fragments as the decode
+// kernel does (K words of the raw rows with q in the same dim order, V token
+// pairs joined by a byte permute, O dims permuted and put back in the
+// combine); P is f16 and the scales fold into the logit scale and the output.
+template <int D, bool kFp8, bool kCluster>
 __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillArgs a,
                                                                  const __grid_constant__ CUtensorMap kmap,
                                                                  const __grid_constant__ CUtensorMap vmap) {
-    using C = SqCfg<D>;
+    using C = SqCfg<D, kFp8>;
     constexpr int KSTEPS = D / 16;
     constexpr int NTILES = D / 8;
     extern __shared__ uint8_t smem_raw[];
@@ -157,8 +163,13 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
         if (lane == 0 && kk < my_n) {
             uint8_t* dst = wbase + kk * C::kStageBytes;
             mbar_arrive_expect_tx(&bars[warp][kk], C::kStageBytes);
-            tma_load_5d(dst, &kmap, &bars[warp][kk], 0, 0, 0, kvh, pb);
-            tma_load_5d(dst + C::kTileBytes, &vmap, &bars[warp][kk], 0, 0, 0, kvh, pb);
+            if constexpr (kFp8) {
+                tma_load_4d(dst, &kmap, &bars[warp][kk], 0, 0, kvh, pb);
+                tma_load_4d(dst + C::kTileBytes, &vmap, &bars[warp][kk], 0, 0, kvh, pb);
+            } else {
+                tma_load_5d(dst, &kmap, &bars[warp][kk], 0, 0, 0, kvh, pb);
+                tma_load_5d(dst + C::kTileBytes, &vmap, &bars[warp][kk], 0, 0, 0, kvh, pb);
+            }
         }
     }
 
@@ -179,13 +190,17 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
 #pragma unroll
         for (int part = 0; part < 4; ++part) {
             const int r = g0 + ((part & 1) ? 8 : 0);
-            const int col = kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
+            // e4m3: k-step kk of lane (g, tig) covers dims tig D/4 + 4 kk + {0..3},
+            // the order its K words come in (the dot product is a sum over dims)
+            const int col = kFp8 ? tig * (D / 4) + 4 * kk + ((part & 2) ? 2 : 0)
+                                 : kk * 16 + 2 * tig + ((part & 2) ? 8 : 0);
             uint32_t v = 0;
             if (r < trows) {
                 const int R = 16 * tile + r;
                 const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
                                             (static_cast<size_t>(q0 + R / G) * a.hq + kvh * G + R % G) * D;
                 v = *reinterpret_cast<const uint32_t*>(qrow + col);
+                if constexpr (kFp8) v = pack2<true>(bf16_lo(v), bf16_hi(v));
             }
             qa[kk][part] = v;
         }
@@ -215,7 +230,29 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
         float sacc[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-        {
+        if constexpr (kFp8) {
+            // rows g (tokens 0-7) and g + 8 (tokens 8-15), bytes [tig D/4, (tig+1) D/4)
+            const uint8_t* ktile = wbase + st * C::kStageBytes;
+            uint32_t kw[2][D / 16];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int q4 = 0; q4 < D / 64; ++q4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(ktile + (g0 + 8 * n) * D + tig * (D / 4) + 16 * q4);
+                    kw[n][4 * q4] = v.x;
+                    kw[n][4 * q4 + 1] = v.y;
+                    kw[n][4 * q4 + 2] = v.z;
+                    kw[n][4 * q4 + 3] = v.w;
+                }
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                uint32_t b0, b1, b2, b3;
+                e4m3x4_to_f16x4(kw[0][kk], b0, b1);
+                e4m3x4_to_f16x4(kw[1][kk], b2, b3);
+                mma_16816<true>(sacc[0], qa[kk], b0, b1);
+                mma_16816<true>(sacc[1], qa[kk], b2, b3);
+            }
+        } else {
             const int tok = (lane & 7) + ((lane >> 4) << 3);
             const int csel = (lane >> 3) & 1;
 #pragma unroll
@@ -270,10 +307,10 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
             }
         }
         uint32_t pa[4];
-        pa[0] = pack2<false>(p[0][0], p[0][1]);
-        pa[1] = pack2<false>(p[0][2], p[0][3]);
-        pa[2] = pack2<false>(p[1][0], p[1][1]);
-        pa[3] = pack2<false>(p[1][2], p[1][3]);
+        pa[0] = pack2<kFp8>(p[0][0], p[0][1]);
+        pa[1] = pack2<kFp8>(p[0][2], p[0][3]);
+        pa[2] = pack2<kFp8>(p[1][0], p[1][1]);
+        pa[3] = pack2<kFp8>(p[1][2], p[1][3]);
         // ---- O += P . V, V rows outside [klo, kv_len) zeroed (0 * NaN never
         // reaches the MMA)
         uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
@@ -284,7 +321,47 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
             keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
             keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
         }
-        {
+        if constexpr (kFp8) {
+            // lane (g, tig) takes dims [g D/8, (g+1) D/8) of V rows 2 tig, 2 tig + 1
+            // (b0) and 2 tig + 8, 2 tig + 9 (b1); n-tile nt's column is dim g D/8 + nt
+            constexpr int W = D / 32;  // 32-bit words of a lane's slice of one row
+            const uint8_t* vb = wbase + st * C::kStageBytes + C::kTileBytes + g0 * (D / 8);
+            uint32_t r0[W], r1[W], r8[W], r9[W];
+            auto row_words = [&](int row, uint32_t (&w)[W]) {
+                if constexpr (W == 2) {
+                    const uint2 t = *reinterpret_cast<const uint2*>(vb + row * D);
+                    w[0] = t.x;
+                    w[1] = t.y;
+                } else {
+                    const uint4 t = *reinterpret_cast<const uint4*>(vb + row * D);
+                    w[0] = t.x;
+                    w[1] = t.y;
+                    w[2] = t.z;
+                    w[3] = t.w;
+                }
+            };
+            row_words(2 * tig, r0);
+            row_words(2 * tig + 1, r1);
+            row_words(2 * tig + 8, r8);
+            row_words(2 * tig + 9, r9);
+#pragma unroll
+            for (int nt = 0; nt < NTILES; nt += 2) {
+                // bytes s, s+1 of word nt/4 from both rows of a pair: (a_s, b_s, a_s+1, b_s+1)
+                const uint32_t sel = (nt % 4 == 0) ? 0x5140u : 0x7362u;
+                uint32_t plo, phi;
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(plo) : "r"(r0[nt / 4]), "r"(r1[nt / 4]), "r"(sel));
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(phi) : "r"(r8[nt / 4]), "r"(r9[nt / 4]), "r"(sel));
+                uint32_t b0a, b0b, b1a, b1b;
+                e4m3x4_to_f16x4(plo, b0a, b0b);
+                e4m3x4_to_f16x4(phi, b1a, b1b);
+                b0a &= keep_lo;
+                b0b &= keep_lo;
+                b1a &= keep_hi;
+                b1b &= keep_hi;
+                mma_16816<true>(o[nt], pa, b0a, b1a);
+                mma_16816<true>(o[nt + 1], pa, b0b, b1b);
+            }
+        } else {
             const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
             const int csel = lane >> 4;
 #pragma unroll
@@ -307,8 +384,13 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
             fence_proxy_async_smem();
             uint8_t* dst = wbase + st * C::kStageBytes;
             mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
-            tma_load_5d(dst, &kmap, &bars[warp][st], 0, 0, 0, kvh, pb);
-            tma_load_5d(dst + C::kTileBytes, &vmap, &bars[warp][st], 0, 0, 0, kvh, pb);
+            if constexpr (kFp8) {
+                tma_load_4d(dst, &kmap, &bars[warp][st], 0, 0, kvh, pb);
+                tma_load_4d(dst + C::kTileBytes, &vmap, &bars[warp][st], 0, 0, kvh, pb);
+            } else {
+                tma_load_5d(dst, &kmap, &bars[warp][st], 0, 0, 0, kvh, pb);
+                tma_load_5d(dst + C::kTileBytes, &vmap, &bars[warp][st], 0, 0, 0, kvh, pb);
+            }
         }
     }
     if (failed) {
@@ -333,9 +415,19 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
         float* cw = comb + warp * 16 * C::kCombStride;
 #pragma unroll
         for (int nt = 0; nt < NTILES; ++nt) {
-            const int col = nt * 8 + 2 * tig;
-            *reinterpret_cast<float2*>(cw + g0 * C::kCombStride + col) = make_float2(o[nt][0], o[nt][1]);
-            *reinterpret_cast<float2*>(cw + (g0 + 8) * C::kCombStride + col) = make_float2(o[nt][2], o[nt][3]);
+            if constexpr (kFp8) {  // dims 2 tig D/8 + nt and (2 tig + 1) D/8 + nt
+                const int c0 = 2 * tig * (D / 8) + nt;
+                const int c1 = c0 + D / 8;
+                cw[g0 * C::kCombStride + c0] = o[nt][0];
+                cw[g0 * C::kCombStride + c1] = o[nt][1];
+                cw[(g0 + 8) * C::kCombStride + c0] = o[nt][2];
+                cw[(g0 + 8) * C::kCombStride + c1] = o[nt][3];
+            } else {
+                const int col = nt * 8 + 2 * tig;
+                *reinterpret_cast<float2*>(cw + g0 * C::kCombStride + col) = make_float2(o[nt][0], o[nt][1]);
+                *reinterpret_cast<float2*>(cw + (g0 + 8) * C::kCombStride + col) =
+                    make_float2(o[nt][2], o[nt][3]);
+            }
         }
         if (tig == 0) {
             s_m[warp][g0] = m_run[0];
@@ -457,14 +549,14 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
     }
 }
 
-template <int D>
+template <int D, bool kFp8>
 cudaError_t launch_sq_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         cudaStream_t stream) {
-    using C = SqCfg<D>;
+    using C = SqCfg<D, kFp8>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert((kSqMaxSplits + 2) * 16 <= 16 * C::kCombStride, "cluster merge scratch");
     const bool cluster = a.sq_splits > 1;
-    auto kern = cluster ? short_query_kernel<D, true> : short_query_kernel<D, false>;
+    auto kern = cluster ? short_query_kernel<D, kFp8, true> : short_query_kernel<D, kFp8, false>;
     static bool attr_set[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -484,7 +576,11 @@ cudaError_t launch_sq_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUt
 
 cudaError_t launch_short_query(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream) {
-    return a.d == 64 ? launch_sq_d<64>(a, kmap, vmap, stream) : launch_sq_d<128>(a, kmap, vmap, stream);
+    if (a.fp8)
+        return a.d == 64 ? launch_sq_d<64, true>(a, kmap, vmap, stream)
+                         : launch_sq_d<128, true>(a, kmap, vmap, stream);
+    return a.d == 64 ? launch_sq_d<64, false>(a, kmap, vmap, stream)
+                     : launch_sq_d<128, false>(a, kmap, vmap, stream);
 }
 
 }  // namespace pkv

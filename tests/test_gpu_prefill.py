@@ -194,9 +194,9 @@ def test_mixed_step_workload_full_size():
 def test_fp8_prefill_matches_oracle(hq, hkv, d, window, short):
     """Ragged causal prefill over e4m3 pools with per-head scales (InferX, "The
     kernels underneath": FP8 KV cache): against the oracle on the same codes.
-    short: at most 64 query rows per sequence, so the staged pool is read by
-    the short-query kernel with the scales folded in; otherwise the tcgen05
-    kernel converts the tiles itself, with no workspace."""
+    short: at most 64 query rows per sequence, so the short-query kernel
+    converts the codes into its MMA fragments; otherwise the tcgen05 kernel
+    converts the tiles in shared memory.  Neither takes a workspace."""
     from tests._cases import PagedCase
     rng = np.random.default_rng(80 + d + hq + (window > 0) + 7 * short)
     q_lens = [min(8, 64 // (hq // hkv)), 1, 3, 1, 1] if short else [64, 200, 77, 1, 1]
@@ -209,11 +209,9 @@ def test_fp8_prefill_matches_oracle(hq, hkv, d, window, short):
     q = t(case.q).view(torch.int16).view(torch.bfloat16) if case.q.dtype == np.uint16 else t(case.q)
     out = torch.full((T, hq, d), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.full((T, hq), float("nan"), device=DEV)
-    # the short-query kernel reads a bf16 staging copy in the workspace; the
-    # tcgen05 kernel converts e4m3 tiles in shared memory and takes none
-    ws = torch.zeros(max(pkv.pkv_prefill_workspace_size(desc, len(case.lens), T), 256), dtype=torch.uint8,
-                     device=DEV) if short else None
-    for _ in range(2):  # the staging workspace is reused
+    assert pkv.pkv_prefill_workspace_size(desc, len(case.lens), T) == 0
+    ws = None
+    for _ in range(2):  # two calls in a row
         pkv.pkv_prefill_attention_ragged(desc, q, t(case.qo), t(case.k_cache), t(case.v_cache), t(case.tables),
                                          t(case.lens), sm, out, lse, qo_indptr_host=case.qo,
                                          kv_lens_host=case.lens, window=window, workspace=ws,
