@@ -38,6 +38,13 @@
 // instead measured 8 % slower.  Operands: Q, K (K-major, SW128) via
 // shared-memory descriptors, P from TMEM, V read MN-major (head_dim
 // contiguous), as stored.
+//
+// e4m3 pools (kFp8; InferX, "The kernels underneath": FP8 KV cache): the
+// producers TMA each (block, head) box of codes into one of eight one-block
+// slots and convert it exactly to f16, in the layout above, into the ring
+// stage; the softmax warps turn Q into f16 in place, P is packed as f16, and
+// the MMAs run f16 x f16 -> fp32 (one operand type per MMA).  k_scale folds
+// into the logit scale and v_scale into the final normalisation.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
