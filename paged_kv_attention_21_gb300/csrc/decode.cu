@@ -233,6 +233,9 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int seq, int kvh, in
 //     O[16 x D] += P . V
 // tok_base is the block's first token position.  Rows g0 + 8 take part only
 // when hi_rows (a group of more than 8 heads).
+// log2 of the largest factor a stale running max may leave in p
+constexpr float kLazyRescale = 8.0f;
+
 template <int D, bool kFp8>
 __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
                                              float (&m_run)[2], float (&l_run)[2], const uint8_t* ktile,
@@ -291,19 +294,26 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            x[n][e] = sacc[n][e] * scale_log2;
-            if (edge) {
-                const int t = tok_base + n * 8 + 2 * tig + (e & 1);
-                if (t < lo || t >= ctx) x[n][e] = -INFINITY;
-            }
-        }
+        for (int e = 0; e < 4; ++e) x[n][e] = sacc[n][e] * scale_log2;
+    if (edge) {  // the block straddles lo or ctx: token t is visible iff t - lo < ctx - lo (unsigned)
+        const int base = tok_base + 2 * tig - lo;
+        const uint32_t cnt = static_cast<uint32_t>(ctx - lo);
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (static_cast<uint32_t>(base + n * 8 + (e & 1)) >= cnt) x[n][e] = -INFINITY;
+    }
     float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-    const float mn0 = fmaxf(m_run[0], mx0);
+    // Lazy rescale: a row keeps its running max m (p = 2^(x - m) <= 2^8)
+    // until a block's max exceeds it by more than 2^8; only then are l and O
+    // rescaled.  The final state (m, l, O) is exact for any such m.
+    const bool grow0 = mx0 > m_run[0] + kLazyRescale;   // -inf + 8 = -inf: a first finite max grows
+    const float mn0 = grow0 ? mx0 : m_run[0];
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float al0 = fast_exp2(m_run[0] - mu0);
+    const float al0 = grow0 ? fast_exp2(m_run[0] - mu0) : 1.f;
     m_run[0] = mn0;
     float p[2][4];
 #pragma unroll
@@ -318,9 +328,10 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
         float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-        const float mn1 = fmaxf(m_run[1], mx1);
+        const bool grow1 = mx1 > m_run[1] + kLazyRescale;
+        const float mn1 = grow1 ? mx1 : m_run[1];
         const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        al1 = fast_exp2(m_run[1] - mu1);
+        al1 = grow1 ? fast_exp2(m_run[1] - mu1) : 1.f;
         m_run[1] = mn1;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
@@ -349,11 +360,11 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
     // e4m3 tiles a block whose rows are all visible skips the masking)
     uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
     if (edge) {
-        const int t0 = tok_base + 2 * tig;
-        const bool v0 = t0 >= lo && t0 < ctx, v1 = t0 + 1 >= lo && t0 + 1 < ctx;
-        const bool v8 = t0 + 8 >= lo && t0 + 8 < ctx, v9 = t0 + 9 >= lo && t0 + 9 < ctx;
-        keep_lo = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
-        keep_hi = (v8 ? 0x0000FFFFu : 0u) | (v9 ? 0xFFFF0000u : 0u);
+        const int base = tok_base + 2 * tig - lo;
+        const uint32_t cnt = static_cast<uint32_t>(ctx - lo);
+        auto vis = [&](int d) { return static_cast<uint32_t>(base + d) < cnt; };
+        keep_lo = (vis(0) ? 0x0000FFFFu : 0u) | (vis(1) ? 0xFFFF0000u : 0u);
+        keep_hi = (vis(8) ? 0x0000FFFFu : 0u) | (vis(9) ? 0xFFFF0000u : 0u);
     }
     auto pv = [&](auto masked) {
         constexpr bool kMask = decltype(masked)::value;
