@@ -226,21 +226,23 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int seq, int kvh, in
     if (rot_pos >= 0) rotate_q<D>(qa, cs);
 }
 
+// log2 of the largest factor a stale running max may leave in p
+constexpr float kLazyRescale = 8.0f;
+
 // One block of K and V (16 tokens of one KV head, in shared memory) into a
 // warp's running state:
 //     S[16 x 16] = Q . K^T              (rows: the group's query heads, padded)
 //     online softmax of S over the keys in [lo, ctx), exp2 domain
 //     O[16 x D] += P . V
 // tok_base is the block's first token position.  Rows g0 + 8 take part only
-// when hi_rows (a group of more than 8 heads).
-// log2 of the largest factor a stale running max may leave in p
-constexpr float kLazyRescale = 8.0f;
-
-template <int D, bool kFp8>
+// when kHi (a group of more than 8 heads); otherwise they are padding and
+// cost no softmax work.
+template <int D, bool kFp8, bool kHi>
 __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
                                              float (&m_run)[2], float (&l_run)[2], const uint8_t* ktile,
                                              const uint8_t* vtile, int lane, int tok_base, int lo, int ctx,
-                                             float scale_log2, bool hi_rows) {
+                                             float scale_log2) {
+    constexpr int kRowVals = kHi ? 4 : 2;  // accumulator values of real rows per n-tile
     constexpr int KSTEPS = D / 16;
     constexpr int NTILES = D / 8;
     const int g0 = lane >> 2;
@@ -294,14 +296,14 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[n][e] = sacc[n][e] * scale_log2;
+        for (int e = 0; e < 4; ++e) x[n][e] = e < kRowVals ? sacc[n][e] * scale_log2 : -INFINITY;
     if (edge) {  // the block straddles lo or ctx: token t is visible iff t - lo < ctx - lo (unsigned)
         const int base = tok_base + 2 * tig - lo;
         const uint32_t cnt = static_cast<uint32_t>(ctx - lo);
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < kRowVals; ++e)
                 if (static_cast<uint32_t>(base + n * 8 + (e & 1)) >= cnt) x[n][e] = -INFINITY;
     }
     float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -324,7 +326,7 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
     }
     l_run[0] = l_run[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
     float al1 = 1.f;
-    if (hi_rows) {  // rows 8-15 are query heads only when the group has more than 8
+    if constexpr (kHi) {  // rows 8-15 are query heads only when the group has more than 8
         float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
@@ -661,32 +663,40 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     bool failed = false;
     const bool inject = a.inject_timeout != 0 && warp == 0 && is_first_cta();
     int k = 0;
-    for (; k < my_n; ++k) {
-        const int st = k % C::kStages;
-        const uint32_t ph = (k / C::kStages) & 1;
-        const bool ready = __all_sync(
-            0xFFFFFFFFu, (inject && k == 0) ? mbar_wait(&probe, 0, 1000ull * a.inject_limit_us)
-                                            : mbar_wait(&bars[warp][st], ph));
-        if (!ready) {
-            failed = true;
-            break;
+    // the same loop for groups of more than 8 heads (rows 8-15 real) or not
+    auto run_blocks = [&](auto hi) {
+        for (; k < my_n; ++k) {
+            const int st = k % C::kStages;
+            const uint32_t ph = (k / C::kStages) & 1;
+            const bool ready = __all_sync(
+                0xFFFFFFFFu, (inject && k == 0) ? mbar_wait(&probe, 0, 1000ull * a.inject_limit_us)
+                                                : mbar_wait(&bars[warp][st], ph));
+            if (!ready) {
+                failed = true;
+                return;
+            }
+            const uint8_t* ktile = wbase + st * C::kStageBytes;
+            attend_block<D, kFp8, decltype(hi)::value>(qa, o, m_run, l_run, ktile, ktile + C::kTileBytes,
+                                                         lane, (b0 + warp + k * kW) * kBlockSize, lo, ctx,
+                                                         scale_log2);
+            __syncwarp();
+            // refill this stage with the block NSTAGE ahead
+            const int kn = k + C::kStages;
+            const int pb = __shfl_sync(0xFFFFFFFFu, phys, kn & 31);
+            if (lane == 0 && kn < my_n) {
+                fence_proxy_async_smem();
+                uint8_t* kdst = wbase + st * C::kStageBytes;
+                uint8_t* vdst = kdst + C::kTileBytes;
+                mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
+                load_tile<kFp8>(kdst, &kmap, &bars[warp][st], kvh, pb);
+                load_tile<kFp8>(vdst, &vmap, &bars[warp][st], kvh, pb);
+            }
         }
-        const uint8_t* ktile = wbase + st * C::kStageBytes;
-        attend_block<D, kFp8>(qa, o, m_run, l_run, ktile, ktile + C::kTileBytes, lane,
-                              (b0 + warp + k * kW) * kBlockSize, lo, ctx, scale_log2, hi_rows);
-        __syncwarp();
-        // refill this stage with the block NSTAGE ahead
-        const int kn = k + C::kStages;
-        const int pb = __shfl_sync(0xFFFFFFFFu, phys, kn & 31);
-        if (lane == 0 && kn < my_n) {
-            fence_proxy_async_smem();
-            uint8_t* kdst = wbase + st * C::kStageBytes;
-            uint8_t* vdst = kdst + C::kTileBytes;
-            mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
-            load_tile<kFp8>(kdst, &kmap, &bars[warp][st], kvh, pb);
-            load_tile<kFp8>(vdst, &vmap, &bars[warp][st], kvh, pb);
-        }
-    }
+    };
+    if (hi_rows)
+        run_blocks(std::true_type{});
+    else
+        run_blocks(std::false_type{});
     if (failed) {
         // drain the loads still in flight -- the stage that gave up and the
         // ones after it (bounded) -- so that no copy lands after exit, then report
