@@ -377,11 +377,11 @@ __global__ void __launch_bounds__(kSqThreads) short_query_kernel(const PrefillAr
             }
         }
         __syncwarp();
-        // refill this stage with the block NSTAGE ahead
+        // refill this stage with the block NSTAGE ahead (the stage was only
+        // read, and the reads' values are consumed: no proxy fence needed)
         const int kn = k + kSqStages;
         const int pb = block_id(kn & 127);
         if (lane == 0 && kn < my_n) {
-            fence_proxy_async_smem();
             uint8_t* dst = wbase + st * C::kStageBytes;
             mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
             if constexpr (kFp8) {
