@@ -624,8 +624,7 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
                         const float* v_scale, const int32_t* block_tables, const int32_t* kv_lens,
                         int32_t num_seqs, int32_t total_q_tokens, const int32_t* qo_indptr_host,
                         const int32_t* kv_lens_host, float sm_scale, int32_t causal, int32_t window,
-                        void* out, float* lse_out, void* workspace, size_t workspace_bytes,
-                        pkv_stream_t stream, bool scaled_codes) {
+                        void* out, float* lse_out, pkv_stream_t stream, bool scaled_codes) {
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (desc->ring_blocks > 0)
@@ -679,10 +678,6 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
     // e4m3 pools: both kernels read the codes and convert them on chip (the
     // tcgen05 kernel into f16 tiles in shared memory, the short-query kernel
     // into f16 MMA fragments), with the scales folded in; no workspace
-    const pkv_cache_desc staged = *desc;
-    const void* kpool = k_cache;
-    const void* vpool = v_cache;
-    const int32_t* tables = block_tables;
     pkv::PrefillArgs a{};
     a.k_scale = fp8 || scaled_codes ? k_scale : nullptr;
     a.v_scale = fp8 || scaled_codes ? v_scale : nullptr;
@@ -691,7 +686,7 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
     a.lse_out = lse_out;
     a.qo_indptr = qo_indptr;
     a.kv_lens = kv_lens;
-    a.block_tables = tables;
+    a.block_tables = block_tables;
     a.err = err;
     a.num_seqs = num_seqs;
     a.hq = desc->num_q_heads;
@@ -704,7 +699,7 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
     a.max_qtiles = max_qtiles;
     a.q_tile = QT;
     a.total_q = total_q_tokens;
-    a.num_blocks = staged.num_blocks;
+    a.num_blocks = desc->num_blocks;
     a.sm_scale = sm_scale;
     if (qo_indptr_host && kv_lens_host && num_seqs <= pkv::kPrefillOrderMax) {
         // dispatch the sequences with the most causal work first: key-query
@@ -721,9 +716,9 @@ pkv_status prefill_impl(const pkv_cache_desc* desc, const void* q, const int32_t
     }
     if (short_q) {
         CUtensorMap tkmap, tvmap;
-        st = pool_map(kpool, &staged, &tkmap, kMapTileRows);
+        st = pool_map(k_cache, desc, &tkmap, kMapTileRows);
         if (st != PKV_OK) return st;
-        st = pool_map(vpool, &staged, &tvmap, kMapTileRows);
+        st = pool_map(v_cache, desc, &tvmap, kMapTileRows);
         if (st != PKV_OK) return st;
         a.sq_chunk = sq_chunk;
         a.sq_splits = sq_splits;
@@ -785,9 +780,11 @@ pkv_status pkv_prefill_attention_ragged(const pkv_cache_desc* desc, const void* 
                                         float* lse_out, void* workspace,
                                         size_t workspace_bytes, pkv_stream_t stream) {
     g_last_error[0] = 0;
+    (void)workspace;  // no prefill path needs one (pkv_prefill_workspace_size is 0)
+    (void)workspace_bytes;
     return prefill_impl(desc, q, qo_indptr, k_cache, v_cache, k_scale, v_scale, block_tables, kv_lens,
                         num_seqs, total_q_tokens, qo_indptr_host, kv_lens_host, sm_scale, causal, window,
-                        out, lse_out, workspace, workspace_bytes, stream, false);
+                        out, lse_out, stream, false);
 }
 
 size_t pkv_prefill_ring_workspace_size(const pkv_cache_desc* desc, int32_t num_seqs, int32_t window,
@@ -886,7 +883,7 @@ pkv_status pkv_prefill_ring_commit(const pkv_cache_desc* desc, const void* q, co
     staged.max_blocks_per_seq = cap;
     return prefill_impl(&staged, q, qo_indptr, g.k_stage, g.v_stage, k_scale, v_scale, g.stage_tables,
                         g.stage_lens, num_seqs, total_q_tokens, qo_indptr_host, stage_lens_host.data(),
-                        sm_scale, 1, window, out, lse_out, nullptr, 0, stream, fp8);
+                        sm_scale, 1, window, out, lse_out, stream, fp8);
 }
 
 pkv_status pkv_append_rope(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
@@ -1171,10 +1168,6 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         const bool short_q = max_qtiles > 0 && max_group * G <= pkv::kSqMaxRowTiles * 16 &&
                              plan_short_query(max_prefix, max_group, -1, &sq_chunk, &sq_splits);
         // e4m3 pools: either kernel converts the codes on chip, scales folded in
-        const pkv_cache_desc pd = *desc;
-        const void* kpool = k_cache;
-        const void* vpool = v_cache;
-        const int32_t* ptables = prefix_tables;
         pkv::PrefillArgs a{};
         a.q = q;
         a.k_scale = fp8 ? k_scale : nullptr;
@@ -1184,26 +1177,26 @@ pkv_status pkv_cascade_decode(const pkv_cache_desc* desc, const void* q, const v
         a.lse_out = lse_parts;
         a.qo_indptr = group_indptr;
         a.kv_lens = prefix_lens;
-        a.block_tables = ptables;
+        a.block_tables = prefix_tables;
         a.err = err;
         a.num_seqs = num_groups;
         a.hq = desc->num_q_heads;
         a.hkv = desc->num_kv_heads;
         a.group = G;
         a.d = desc->head_dim;
-        a.mbps = pd.max_blocks_per_seq;
+        a.mbps = desc->max_blocks_per_seq;
         a.causal = 0;
         a.window = -1;
         a.max_qtiles = max_qtiles;
         a.q_tile = QT;
         a.total_q = num_seqs;
-        a.num_blocks = pd.num_blocks;
+        a.num_blocks = desc->num_blocks;
         a.sm_scale = sm_scale;
         if (short_q) {
             CUtensorMap tkmap, tvmap;
-            st = pool_map(kpool, &pd, &tkmap, kMapTileRows);
+            st = pool_map(k_cache, desc, &tkmap, kMapTileRows);
             if (st != PKV_OK) return st;
-            st = pool_map(vpool, &pd, &tvmap, kMapTileRows);
+            st = pool_map(v_cache, desc, &tvmap, kMapTileRows);
             if (st != PKV_OK) return st;
             a.sq_chunk = sq_chunk;
             a.sq_splits = sq_splits;
