@@ -61,6 +61,9 @@ def parse_args():
                         "rows, each "
                         "on its own seeded workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefetch-kv", action="store_true",
+                   help="decode steps read nothing before the previous kernel ends "
+                        "(PKV_DESC_PREFETCH_KV off)")
     p.add_argument("--chunk-blocks", type=int, default=0,
                    help="decode chunk length in blocks passed to the library (0: the planner's "
                         "choice)")
@@ -223,9 +226,16 @@ class DecodeWorkload:
     """A decode workload: instances over disjoint regions of one pool (per
     layer), each with its own device workspace-free inputs."""
 
-    def __init__(self, config, dev, rank, fused=True, chunk=0):
+    def __init__(self, config, dev, rank, fused=True, chunk=0, prefetch=True):
         import paged_kv_attention_21_gb300 as pkv
         self.fused = fused
+        # The fused step's predecessor on the stream never writes the K/V
+        # rows, tables or lengths it reads: the previous step used another
+        # batch's pool region (or another layer's pools, or it was the
+        # prefill, which writes no pool), so the decode may start its first
+        # K/V loads while that kernel drains.  The two-launch step's
+        # predecessor is the append kernel, which writes the rows it reads.
+        self.prefetch = bool(prefetch and fused)
         self.chunk = chunk
         from paged_kv_attention_21_gb300 import workloads as wl
         self.pkv = pkv
@@ -259,7 +269,8 @@ class DecodeWorkload:
         self.desc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
                                   head_dim=spec.head_dim, num_blocks=b0.k_cache.shape[0],
                                   max_blocks_per_seq=b0.tables_host.shape[1],
-                                  kv_dtype=spec.kv_dtype)
+                                  kv_dtype=spec.kv_dtype,
+                                  flags=pkv.DESC_PREFETCH_KV if self.prefetch else 0)
         self.max_ctx = spec.ctx_hi
         ws = max(pkv.pkv_decode_workspace_size(self.desc, spec.batch, self.max_ctx, w, chunk)
                  for w in self.windows)
@@ -389,7 +400,8 @@ def time_pkv(args, rank, world, local, config=None, steps=None, min_seconds=2.0,
     config = args.config if config is None else config
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    W = DecodeWorkload(config, dev, rank, fused=not args.two_launch, chunk=args.chunk_blocks)
+    W = DecodeWorkload(config, dev, rank, fused=not args.two_launch, chunk=args.chunk_blocks,
+                       prefetch=not args.no_prefetch_kv)
     K = max(1, args.steps if steps is None else steps)
     Wm = max(3, args.warmup)
     R = graph_len(K, W.n_inst)
@@ -480,7 +492,8 @@ def time_pkv(args, rank, world, local, config=None, steps=None, min_seconds=2.0,
                dec_p90=float(np.percentile(dec_ms[li_dom], 90)),
                per_launch_gbs=float(np.median(per_launch_gbs)),
                launches=launches_per_replay * replays * len(win_ms),
-               launches_per_step=launches_per_replay / R)
+               launches_per_step=launches_per_replay / R,
+               step_ms=med_ms / K, step_bytes=bytes_per_window / K)
     if pre_ms:
         res.update(pre_ms=float(np.mean(pre_ms)), pre_p10=float(np.percentile(pre_ms, 10)),
                    pre_p90=float(np.percentile(pre_ms, 90)))
@@ -841,6 +854,7 @@ def workload_config(W, extra=None):
                     "layer, replayed as a CUDA graph")}
     if W.prefill is not None:
         cfg["step"] += " + ragged causal prefill of 8x512 tokens over shared prefixes"
+    cfg["prefetch_kv"] = W.prefetch
     if extra:
         cfg.update(extra)
     return cfg
@@ -1263,20 +1277,48 @@ def workload_name(config):
 
 
 def decode_roofline(r, peak, peak_kind, fused, config):
-    achieved = r["dom_bytes"] / (r["dom_ms"] / 1e3) / 1e9
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-            "traffic": kernel_traffic_per_launch("decode_kernel", config),
-            "kernel": ("decode_kernel (append+RoPE, split-KV GQA decode and merge, one launch)"
-                       if fused else "decode_kernel (split-KV GQA decode, merge fused)"),
-            "peak_source": "%s hbm_gbs" % peak_kind,
-            "algorithmic_bytes_per_launch": int(r["dom_bytes"]),
-            "avg_launch_ms": round(r["dom_ms"], 5),
-            "p10_launch_ms": round(r["dec_p10"], 5), "p90_launch_ms": round(r["dec_p90"], 5),
-            "median_launch_gbs": round(r["per_launch_gbs"], 1),
-            "timed_by": "CUDA events around the decode launch of every %d-th step of every "
-                        "timed window's last graph replay" % r["ev_stride"]}
+    """The decode kernel's roofline.  When every launch of the step is a
+    decode_kernel launch (no prefill, no separate append), the timed windows
+    themselves give its average launch duration as launches run back to back:
+    window time / launches.  Events around single launches (kept below as
+    isolated_*) cut the programmatic dependent launch between neighbours, so
+    they time a launch without the overlap the stream gives it.  The mixed
+    step also runs the prefill, so there the bracketed launches are the
+    measurement."""
+    iso = r["dom_bytes"] / (r["dom_ms"] / 1e3) / 1e9
+    whole = fused and r["W"].prefill is None
+    if whole:
+        n = r["launches_per_step"]
+        bytes_launch = r["step_bytes"] / n
+        ms_launch = r["step_ms"] / n
+    else:
+        bytes_launch, ms_launch = r["dom_bytes"], r["dom_ms"]
+    achieved = bytes_launch / (ms_launch / 1e3) / 1e9
+    out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+           "frac": round(achieved / peak, 4),
+           "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+           "traffic": kernel_traffic_per_launch("decode_kernel", config),
+           "kernel": ("decode_kernel (append+RoPE, split-KV GQA decode and merge, one launch)"
+                      if fused else "decode_kernel (split-KV GQA decode, merge fused)"),
+           "peak_source": "%s hbm_gbs" % peak_kind,
+           "algorithmic_bytes_per_launch": int(bytes_launch),
+           "avg_launch_ms": round(ms_launch, 5)}
+    if whole:
+        out.update({
+            "timed_by": "CUDA events around each timed window of graph replays; every launch "
+                        "of the step is decode_kernel: window time / launches",
+            "isolated_launch_ms": round(r["dom_ms"], 5),
+            "isolated_bytes_per_launch": int(r["dom_bytes"]),
+            "frac_isolated": round(iso / peak, 4),
+            "isolated_timed_by": "CUDA events around the decode launch of every %d-th step of the "
+                                 "last graph replay of every window (an event between two launches "
+                                 "cuts their overlap)" % r["ev_stride"]})
+    else:
+        out["timed_by"] = ("CUDA events around the decode launch of every %d-th step of every "
+                           "timed window's last graph replay" % r["ev_stride"])
+    out.update({"p10_launch_ms": round(r["dec_p10"], 5), "p90_launch_ms": round(r["dec_p90"], 5),
+                "median_launch_gbs": round(r["per_launch_gbs"], 1)})
+    return out
 
 
 def main():
@@ -1359,6 +1401,9 @@ def main():
             "ms_per_step": round(carry["elapsed_s"] * 1e3 / carry["K"], 5),
             "frac_per_step": round(cv / world / peak, 4),
             "frac_per_launch": croof["frac"], "avg_launch_ms": croof["avg_launch_ms"],
+            "frac_isolated_launch": croof.get("frac_isolated"),
+            "isolated_launch_ms": croof.get("isolated_launch_ms"),
+            "prefetch_kv": cW.prefetch,
             "median_launch_gbs": croof["median_launch_gbs"],
             "algorithmic_bytes_per_launch": croof["algorithmic_bytes_per_launch"],
             "traffic": croof["traffic"],

@@ -86,7 +86,21 @@ typedef struct {
     int32_t max_blocks_per_seq;  /* row length of block_tables (int32 [num_seqs][this]) */
     int64_t num_blocks;          /* blocks in each pool */
     int32_t ring_blocks;         /* 0: linear tables; > 0: ring of this many blocks (<= max_blocks_per_seq) */
+    uint32_t flags;              /* PKV_DESC_* bits; 0 for none */
 } pkv_cache_desc;
+
+/* pkv_cache_desc.flags.
+ * PKV_DESC_PREFETCH_KV: a promise about the stream the calls run on: the
+ *   kernel launched just before a decode call (pkv_decode_attention, _step,
+ *   _static) writes none of the K/V rows, block-table entries or context
+ *   lengths that call reads -- it may write q, k_new and v_new, as the layer's
+ *   QKV projection does.  The decode kernel then reads the lengths and block
+ *   ids and starts its first K/V loads while that kernel drains (programmatic
+ *   dependent launch, llm-infer "What It Does": CUDA-graphed decode), and
+ *   waits for it before it reads q, k_new or v_new and before any write.
+ *   Without the promise (the default) nothing is read before that wait.  A
+ *   call whose predecessor breaks the promise may read stale K/V rows. */
+#define PKV_DESC_PREFETCH_KV 0x1u
 
 /* Bytes of one pool (K or V): num_blocks * Hkv * block_size * head_dim * elem.
  * Host only; 0 for an invalid desc. */

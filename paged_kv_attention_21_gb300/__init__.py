@@ -22,6 +22,7 @@ from . import build as _build
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+DESC_PREFETCH_KV = 0x1  # pkv_cache_desc.flags: see PKV_DESC_PREFETCH_KV in pkv.h
 DEVERR_BLOCK_ID = 0x1
 DEVERR_POSITION = 0x2
 DEVERR_TIMEOUT = 0x4
@@ -45,15 +46,18 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int64), ("ring_blocks", ctypes.c_int32)]
+                ("num_blocks", ctypes.c_int64), ("ring_blocks", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
 
 
 def make_desc(*, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
-              kv_dtype=KV_BF16, block_size=16, ring_blocks=0) -> CacheDesc:
+              kv_dtype=KV_BF16, block_size=16, ring_blocks=0, flags=0) -> CacheDesc:
+    """flags: DESC_PREFETCH_KV (see pkv.h) or 0."""
     if isinstance(kv_dtype, str):
         kv_dtype = KV_FP8_E4M3 if kv_dtype.startswith("fp8") else KV_BF16
     return CacheDesc(int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-                     int(kv_dtype), int(max_blocks_per_seq), int(num_blocks), int(ring_blocks))
+                     int(kv_dtype), int(max_blocks_per_seq), int(num_blocks), int(ring_blocks),
+                     int(flags))
 
 
 _lock = threading.Lock()

@@ -481,15 +481,19 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     }
     // With defer_wait the grid-dependency wait moves to every exit: the work
     // overlaps the previous kernel, and this grid still completes only after
-    // it, so kernels after this one see both.
+    // it, so kernels after this one see both.  With early_kv the wait comes
+    // after the lengths, the block ids and the first ring loads (the previous
+    // kernel writes none of them) and before anything touches q, k_new, v_new
+    // or an output; an exit before that point still waits.
     struct WaitAtExit {
         bool on;
         __device__ ~WaitAtExit() {
             if (on) pdl_wait();
         }
     };
-    const WaitAtExit wait_at_exit{a.defer_wait != 0};
-    if (!a.defer_wait) pdl_wait();
+    const bool early = a.early_kv != 0 && a.defer_wait == 0;
+    const WaitAtExit wait_at_exit{a.defer_wait != 0 || early};
+    if (!a.defer_wait && !early) pdl_wait();
     pdl_launch_dependents();
     const int split = blockIdx.x;
     const int kvh = blockIdx.y;
@@ -532,10 +536,15 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     // the host checked against the table capacity
     bool clamped = false;
     if (ctx > a.max_ctx) {
-        if (threadIdx.x == 0 && split == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
         ctx = a.max_ctx;
         clamped = true;
     }
+    // (errors are flagged after the grid-dependency wait: the error word is
+    // written by earlier kernels too)
+    auto flag_length = [&]() {
+        if (clamped && threadIdx.x == 0 && split == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+    };
+    if (!early) flag_length();
     int lo = (a.window > 0 && ctx > a.window) ? ctx - a.window : 0;
     if (a.group_indptr) {
         // the query at position ctx + suffix - 1 sees prefix keys t >= ctx + suffix - window
@@ -543,6 +552,10 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         if (lo >= ctx) ctx = 0;
     }
     if (ctx <= 0) {  // no visible key: o = 0, lse = -inf
+        if (early) {
+            pdl_wait();
+            flag_length();
+        }
         if (split == 0) {
             const size_t o0 = (static_cast<size_t>(seq) * a.hq + kvh * G) * D;
             for (int i = threadIdx.x; i < G * D; i += kThreads) {
@@ -579,7 +592,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         const int lb = b0 + warp + lane * kW;  // logical block
         if (a.window > 0 && !ring_lanes) phys = bt[a.ring > 0 ? lb % a.ring : lb];
         if (phys < 0 || phys >= a.num_blocks) {
-            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+            if (!early) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
             phys = 0;  // read a valid block; the output is flagged invalid
             bad_id = true;
         }
@@ -597,19 +610,36 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         const bool bad = __shfl_sync(0xFFFFFFFFu, bad_id, k_last & 31);
         if (!bad) append_new_token<D, kFp8>(a, seq, kvh, pb, ctx - 1, lane);
     };
-    if (appender && k_last < C::kStages) append();
     // Lane 0 issues the prologue; the shuffle reads lane k's id from lane 0's
     // point of view, so every lane takes part in it.
-#pragma unroll
-    for (int k = 0; k < C::kStages; ++k) {
+    auto load_stage = [&](int k) {
         const int pb = __shfl_sync(0xFFFFFFFFu, phys, k & 31);
         if (lane == 0 && k < my_n) {
-            const int st = k;
-            uint8_t* kdst = wbase + st * C::kStageBytes;
+            uint8_t* kdst = wbase + k * C::kStageBytes;
             uint8_t* vdst = kdst + C::kTileBytes;
-            mbar_arrive_expect_tx(&bars[warp][st], C::kStageBytes);
-            load_tile<kFp8>(kdst, &kmap, &bars[warp][st], kvh, pb);
-            load_tile<kFp8>(vdst, &vmap, &bars[warp][st], kvh, pb);
+            mbar_arrive_expect_tx(&bars[warp][k], C::kStageBytes);
+            load_tile<kFp8>(kdst, &kmap, &bars[warp][k], kvh, pb);
+            load_tile<kFp8>(vdst, &vmap, &bars[warp][k], kvh, pb);
+        }
+    };
+    const bool append_first = appender && k_last < C::kStages;  // the new token's block is in the prologue
+    if (!early) {
+        if (append_first) append();
+#pragma unroll
+        for (int k = 0; k < C::kStages; ++k) load_stage(k);
+    } else {
+        // every stage but the one the new token goes into, then the wait
+#pragma unroll
+        for (int k = 0; k < C::kStages; ++k)
+            if (!(append_first && k == k_last)) load_stage(k);
+        pdl_wait();
+        flag_length();
+        if (__any_sync(0xFFFFFFFFu, bad_id)) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+        }
+        if (append_first) {
+            append();
+            load_stage(k_last);
         }
     }
     if (appender && k_last >= C::kStages) append();

@@ -127,6 +127,11 @@ struct DecodeArgs {
     // stream writes (that kernel only waited for its own predecessors), so
     // it starts without the grid-dependency wait and takes it before exiting
     int32_t defer_wait;
+    // early_kv != 0: the previous kernel in the stream writes none of the
+    // block-table entries, lengths and K/V rows this launch reads (only what
+    // it reads through q, k_new, v_new, cos_sin): the lengths, the block ids
+    // and the first ring loads are issued before the grid-dependency wait
+    int32_t early_kv;
     // test hook: inject_timeout != 0 makes warp 0 of CTA (0, 0, 0) give up
     // its first pipeline wait after inject_limit_us (see common.cuh)
     int32_t inject_timeout;

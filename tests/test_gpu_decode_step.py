@@ -192,6 +192,63 @@ def test_decode_step_in_a_graph_repeats():
     assert pkv.pkv_device_errors() == 0
 
 
+@pytest.mark.parametrize("hq,hkv,d,fp8", [(16, 2, 128, False), (64, 8, 64, True), (32, 8, 128, False)])
+def test_prefetch_kv_steps_back_to_back_match_oracle(hq, hkv, d, fp8):
+    """PKV_DESC_PREFETCH_KV: a step reads its lengths and block ids and
+    starts its first K/V loads before the previous kernel on the stream has
+    finished, and waits for it before touching q, k_new, v_new or writing.
+    Two batches over separate pools alternate on one stream (each step's
+    predecessor writes only the other batch's pools, as the promise asks),
+    launched directly and replayed from a graph: every step's cache and
+    output equal the oracle's, for planned, 1-block and 3-block chunks (the
+    new token's block inside and outside each warp's first ring loads)."""
+    cases = [_setup(210 + i + d + fp8, LENS, hq, hkv, d, fp8, True) for i in range(2)]
+    refs = [_oracle_step(c, kn, vn, t, c.tables, c.k_cache, c.v_cache, -1) for (c, kn, vn, t) in cases]
+    B = len(LENS)
+    for chunk in (0, 1, 3):
+        runs = []
+        for (case, k_new, v_new, table) in cases:
+            desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                 num_blocks=case.k_cache.shape[0], max_blocks_per_seq=case.tables.shape[1],
+                                 kv_dtype=1 if fp8 else 0, flags=pkv.DESC_PREFETCH_KV)
+            max_ctx = int(case.lens.max())
+            runs.append(dict(
+                desc=desc, max_ctx=max_ctx, kd=_pool(case.k_cache), vd=_pool(case.v_cache), q=_pool(case.q),
+                kn=_pool(k_new), vn=_pool(v_new), cs=_dev(table), tabs=_dev(case.tables),
+                lens=_dev(case.lens), ks=_dev(case.k_scale), vs=_dev(case.v_scale),
+                out=torch.full((B, hq, d), float("nan"), dtype=torch.bfloat16, device=DEV),
+                lse=torch.full((B, hq), float("nan"), device=DEV),
+                ws=torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, chunk), 256),
+                               dtype=torch.uint8, device=DEV)))
+        s = torch.cuda.Stream()
+
+        def step(r):
+            pkv.pkv_decode_step(r["desc"], r["q"], r["kn"], r["vn"], r["kd"], r["vd"], r["tabs"], r["lens"],
+                                r["max_ctx"], 1 / math.sqrt(d), r["out"], r["lse"], r["ws"], cos_sin=r["cs"],
+                                chunk_blocks=chunk, k_scale=r["ks"], v_scale=r["vs"], stream=s)
+
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                for r in runs:
+                    step(r)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(2):
+                for r in runs:
+                    step(r)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_errors() == 0
+        for r, (kc, vc, ref, ref_lse) in zip(runs, refs):
+            assert np.array_equal(pool_np(r["kd"]), kc) and np.array_equal(pool_np(r["vd"]), vc), \
+                "cache after prefetching steps differs from the oracle's append"
+            assert_close(r["out"], ref, "prefetching step %d/%d/%d fp8=%d chunk %d" % (hq, hkv, d, fp8, chunk))
+            assert_lse_close(r["lse"], ref_lse, "prefetching step lse")
+            assert int(r["ws"][:4 * B * hkv].view(torch.int32).abs().sum().item()) == 0, "tickets not reset"
+
+
 def test_bound_decode_step_equals_the_unbound_call():
     """bind_decode_step marshals the arguments once; refilling the bound q
     and calling again gives the bits of a fresh unbound call."""
