@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         }
     };
     const bool early = a.early_kv != 0 && a.defer_wait == 0;
-    const WaitAtExit wait_at_exit{a.defer_wait != 0 || early};
+    WaitAtExit wait_at_exit{a.defer_wait != 0 || early};
     if (!a.defer_wait && !early) pdl_wait();
     pdl_launch_dependents();
     const int split = blockIdx.x;
@@ -573,7 +573,14 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const int first_blk = lo / kBlockSize;
     const int last_blk = (ctx - 1) / kBlockSize;
     const int nsplit = (last_blk - first_blk + a.chunk_blocks) / a.chunk_blocks;
-    if (split >= nsplit) return;
+    if (split >= nsplit) {
+        // no chunk here.  In early mode the CTA leaves without waiting, so
+        // its slot frees at once: chunk 0 of the same (sequence, KV head)
+        // waits before it reads q or writes, so the grid still completes
+        // after the previous kernel
+        if (early) wait_at_exit.on = false;
+        return;
+    }
     const int b0 = first_blk + split * a.chunk_blocks;
     const int b1 = min(last_blk + 1, b0 + a.chunk_blocks);
     const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kW - 1) / kW : 0;
