@@ -61,6 +61,9 @@ def parse_args():
                         "rows, each "
                         "on its own seeded workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--decode-first", action="store_true",
+                   help="mixed step: decode, then prefill waiting for it (the order before "
+                        "PKV_DESC_INDEPENDENT)")
     p.add_argument("--no-prefetch-kv", action="store_true",
                    help="decode steps read nothing before the previous kernel ends "
                         "(PKV_DESC_PREFETCH_KV off)")
@@ -226,7 +229,7 @@ class DecodeWorkload:
     """A decode workload: instances over disjoint regions of one pool (per
     layer), each with its own device workspace-free inputs."""
 
-    def __init__(self, config, dev, rank, fused=True, chunk=0, prefetch=True):
+    def __init__(self, config, dev, rank, fused=True, chunk=0, prefetch=True, prefill_first=True):
         import paged_kv_attention_21_gb300 as pkv
         self.fused = fused
         # The fused step's predecessor on the stream never writes the K/V
@@ -236,6 +239,12 @@ class DecodeWorkload:
         # K/V loads while that kernel drains.  The two-launch step's
         # predecessor is the append kernel, which writes the rows it reads.
         self.prefetch = bool(prefetch and fused)
+        # The mixed step's two halves -- the decode tokens' attention and the
+        # prefill chunks' -- both read one layer's QKV output and touch
+        # different sequences' blocks and different outputs: the prefill runs
+        # first and the decode after it without waiting for it (its CTAs take
+        # the SMs the prefill's last CTAs leave idle), then waits at its end.
+        self.independent = bool(config == 4 and fused and prefill_first)
         self.chunk = chunk
         from paged_kv_attention_21_gb300 import workloads as wl
         self.pkv = pkv
@@ -270,7 +279,8 @@ class DecodeWorkload:
                                   head_dim=spec.head_dim, num_blocks=b0.k_cache.shape[0],
                                   max_blocks_per_seq=b0.tables_host.shape[1],
                                   kv_dtype=spec.kv_dtype,
-                                  flags=pkv.DESC_PREFETCH_KV if self.prefetch else 0)
+                                  flags=(pkv.DESC_PREFETCH_KV if self.prefetch else 0) |
+                                        (pkv.DESC_INDEPENDENT if self.independent else 0))
         self.max_ctx = spec.ctx_hi
         ws = max(pkv.pkv_decode_workspace_size(self.desc, spec.batch, self.max_ctx, w, chunk)
                  for w in self.windows)
@@ -307,6 +317,8 @@ class DecodeWorkload:
         Returns the launch count."""
         pkv = self.pkv
         n = 0
+        if self.prefill is not None and self.independent:
+            n += self._prefill(pev)
         for li, (layer, w) in enumerate(zip(self.layers, self.windows)):
             b = layer[i]
             if self.fused:
@@ -334,14 +346,17 @@ class DecodeWorkload:
             if ev_pairs is not None:
                 ev_pairs[li][1].record()
             n += 2
-        if self.prefill is not None:
-            if pev is not None:
-                pev[0].record()
-            self.prefill.run()
-            if pev is not None:
-                pev[1].record()
-            n += 1
+        if self.prefill is not None and not self.independent:
+            n += self._prefill(pev)
         return n
+
+    def _prefill(self, pev):
+        if pev is not None:
+            pev[0].record()
+        self.prefill.run()
+        if pev is not None:
+            pev[1].record()
+        return 1
 
 
 class PrefillPart:
@@ -401,7 +416,7 @@ def time_pkv(args, rank, world, local, config=None, steps=None, min_seconds=2.0,
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     W = DecodeWorkload(config, dev, rank, fused=not args.two_launch, chunk=args.chunk_blocks,
-                       prefetch=not args.no_prefetch_kv)
+                       prefetch=not args.no_prefetch_kv, prefill_first=not args.decode_first)
     K = max(1, args.steps if steps is None else steps)
     Wm = max(3, args.warmup)
     R = graph_len(K, W.n_inst)
@@ -418,7 +433,7 @@ def time_pkv(args, rank, world, local, config=None, steps=None, min_seconds=2.0,
     # so every instance is sampled): an event between two launches breaks
     # their programmatic dependent launch, so the other steps keep
     # back-to-back launches.
-    stride = 2 * W.n_inst + 1
+    stride = 11 if W.n_inst % 11 else 13
     sampled = list(range(0, R, stride))
     mk = lambda: (torch.cuda.Event(enable_timing=True, external=True),
                   torch.cuda.Event(enable_timing=True, external=True))
@@ -706,14 +721,18 @@ def time_e2e(W, dev, steps):
         stream.wait_event(ev_in[sl])
         if i >= 2:
             stream.wait_event(ev_out[sl])     # step i-2's outputs have left this slot
-        for li in range(len(W.layers)):
-            slot_calls[(sl, i % W.n_inst, li)]()
-        if pio is not None:
+        def prefill():
             b = p_buf[sl]
             pkv.pkv_prefill_attention_ragged(P.desc, b["q"], b["qo_indptr"], P.pb.k_cache, P.pb.v_cache,
                                              b["block_tables"], b["kv_lens"], P.spec.sm_scale, p_out[sl],
                                              qo_indptr_host=P.pb.qo_indptr_host,
                                              kv_lens_host=P.pb.kv_lens_host, stream=sh)
+        if pio is not None and W.independent:
+            prefill()   # the step's order, as in the timed graph
+        for li in range(len(W.layers)):
+            slot_calls[(sl, i % W.n_inst, li)]()
+        if pio is not None and not W.independent:
+            prefill()
         ev_comp[sl].record(stream)
 
     def issue_out(i):
@@ -853,7 +872,11 @@ def workload_config(W, extra=None):
                     "append+RoPE of the new token, then split-KV decode: two launches per "
                     "layer, replayed as a CUDA graph")}
     if W.prefill is not None:
-        cfg["step"] += " + ragged causal prefill of 8x512 tokens over shared prefixes"
+        cfg["step"] = (("ragged causal prefill of 8x512 tokens over shared prefixes, then " + cfg["step"] +
+                        "; the decode does not wait for the prefill (PKV_DESC_INDEPENDENT: the two "
+                        "halves of one layer's mixed step) and waits at its end")
+                       if W.independent else
+                       cfg["step"] + " + ragged causal prefill of 8x512 tokens over shared prefixes")
     cfg["prefetch_kv"] = W.prefetch
     if extra:
         cfg.update(extra)

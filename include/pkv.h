@@ -101,6 +101,15 @@ typedef struct {
  *   Without the promise (the default) nothing is read before that wait.  A
  *   call whose predecessor breaks the promise may read stale K/V rows. */
 #define PKV_DESC_PREFETCH_KV 0x1u
+/* PKV_DESC_INDEPENDENT: a stronger promise: the kernel launched just before a
+ *   decode call reads and writes nothing the call reads or writes -- as when
+ *   the call is the decode half of one layer's mixed step and the prefill half
+ *   ran just before it (both read the same QKV projection's output, different
+ *   sequences' blocks, different outputs).  The decode kernel then runs
+ *   without waiting for that kernel (its CTAs take the SMs the prefill's last
+ *   CTAs leave idle) and waits for it only at its end, so kernels launched
+ *   after the call still see both.  Implies PKV_DESC_PREFETCH_KV. */
+#define PKV_DESC_INDEPENDENT 0x2u
 
 /* Bytes of one pool (K or V): num_blocks * Hkv * block_size * head_dim * elem.
  * Host only; 0 for an invalid desc. */

@@ -23,6 +23,7 @@ from . import build as _build
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 DESC_PREFETCH_KV = 0x1  # pkv_cache_desc.flags: see PKV_DESC_PREFETCH_KV in pkv.h
+DESC_INDEPENDENT = 0x2  # pkv_cache_desc.flags: see PKV_DESC_INDEPENDENT in pkv.h
 DEVERR_BLOCK_ID = 0x1
 DEVERR_POSITION = 0x2
 DEVERR_TIMEOUT = 0x4

@@ -238,7 +238,8 @@ pkv_status check_desc(const pkv_cache_desc* d) {
     if (d->ring_blocks < 0 || d->ring_blocks > d->max_blocks_per_seq)
         return fail(PKV_ERR_INVALID_ARG, "ring_blocks %d outside [0, max_blocks_per_seq = %d]", d->ring_blocks,
                     d->max_blocks_per_seq);
-    if (d->flags & ~PKV_DESC_PREFETCH_KV) return fail(PKV_ERR_INVALID_ARG, "unknown desc flags 0x%x", d->flags);
+    if (d->flags & ~(PKV_DESC_PREFETCH_KV | PKV_DESC_INDEPENDENT))
+        return fail(PKV_ERR_INVALID_ARG, "unknown desc flags 0x%x", d->flags);
     return PKV_OK;
 }
 
@@ -564,6 +565,7 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
     a.inject_timeout = g_inject_kernels.load() & 1;
     a.inject_limit_us = g_inject_limit_us.load();
     a.early_kv = (desc->flags & PKV_DESC_PREFETCH_KV) ? 1 : 0;
+    a.defer_wait = (desc->flags & PKV_DESC_INDEPENDENT) ? 1 : 0;
     if (step) {
         a.k_new = step->k_new;
         a.v_new = step->v_new;

@@ -479,9 +479,11 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         s_flag = 0;
         if (a.inject_timeout) mbar_init(&probe, 1);
     }
-    // With defer_wait the grid-dependency wait moves to every exit: the work
-    // overlaps the previous kernel, and this grid still completes only after
-    // it, so kernels after this one see both.  With early_kv the wait comes
+    // With defer_wait the work overlaps the previous kernel and the
+    // grid-dependency wait moves to the exit of CTA (0, 0, 0), which every
+    // launch has: this grid then completes only after the previous one, so
+    // kernels after this one see both, while every other CTA leaves as soon
+    // as its work is done and frees its slot.  With early_kv the wait comes
     // after the lengths, the block ids and the first ring loads (the previous
     // kernel writes none of them) and before anything touches q, k_new, v_new
     // or an output; an exit before that point still waits.
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         }
     };
     const bool early = a.early_kv != 0 && a.defer_wait == 0;
-    WaitAtExit wait_at_exit{a.defer_wait != 0 || early};
+    WaitAtExit wait_at_exit{(a.defer_wait != 0 && is_first_cta()) || early};
     if (!a.defer_wait && !early) pdl_wait();
     pdl_launch_dependents();
     const int split = blockIdx.x;

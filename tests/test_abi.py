@@ -89,7 +89,7 @@ def test_invalid_arguments_return_status_before_any_device_work(lib):
         (_desc(block_size=32), 2, "block_size"),
         (_desc(kv_dtype=7), 2, "kv_dtype"),
         (_desc(num_blocks=0), 1, "num_blocks"),
-        (_desc(flags=0x2), 1, "flags"),
+        (_desc(flags=0x4), 1, "flags"),
     ]
     for d, code, word in bad:
         st = lib.pkv_decode_attention(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, 1,

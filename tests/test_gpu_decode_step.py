@@ -249,6 +249,70 @@ def test_prefetch_kv_steps_back_to_back_match_oracle(hq, hkv, d, fp8):
             assert int(r["ws"][:4 * B * hkv].view(torch.int32).abs().sum().item()) == 0, "tickets not reset"
 
 
+def test_independent_decode_step_after_prefill_matches_oracle():
+    """PKV_DESC_INDEPENDENT, one layer's mixed step: a ragged causal prefill
+    (its own pools) and then the decode step of other sequences, which does
+    not wait for the prefill and waits only at its end.  Alternating on one
+    stream, directly and replayed from a graph, both outputs and the decode's
+    cache equal the oracle's."""
+    from tests.test_gpu_prefill import _oracle_prefill
+    spec = wl.dataclasses.replace(wl.LLAMA3_8B_PREFILL, num_chunks=4, chunk_len=96, prefix_hi=700, seed=5)
+    pb = wl.make_prefill_batch(spec, "cpu")
+    p_ref, p_ref_lse = _oracle_prefill(spec, pb)
+    pdesc = pkv.make_desc(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                          head_dim=spec.head_dim, num_blocks=pb.k_cache.shape[0],
+                          max_blocks_per_seq=pb.tables_host.shape[1])
+    pq, pk, pv = pb.q.to(DEV), pb.k_cache.to(DEV), pb.v_cache.to(DEV)
+    pqo, pkvl, ptab = (torch.from_numpy(x).to(DEV) for x in (pb.qo_indptr_host, pb.kv_lens_host, pb.tables_host))
+    p_out = torch.full((pb.total_q, spec.num_q_heads, spec.head_dim), float("nan"), dtype=torch.bfloat16,
+                       device=DEV)
+    p_lse = torch.full((pb.total_q, spec.num_q_heads), float("nan"), device=DEV)
+
+    hq, hkv, d = 32, 8, 128
+    case, k_new, v_new, table = _setup(230, LENS, hq, hkv, d, False, True)
+    kc, vc, ref, ref_lse = _oracle_step(case, k_new, v_new, table, case.tables, case.k_cache, case.v_cache, -1)
+    B = len(LENS)
+    for chunk in (0, 3):
+        desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=case.k_cache.shape[0],
+                             max_blocks_per_seq=case.tables.shape[1],
+                             flags=pkv.DESC_INDEPENDENT | pkv.DESC_PREFETCH_KV)
+        max_ctx = int(case.lens.max())
+        kd, vd, q = _pool(case.k_cache), _pool(case.v_cache), _pool(case.q)
+        kn, vn, cs = _pool(k_new), _pool(v_new), _dev(table)
+        tabs, lens = _dev(case.tables), _dev(case.lens)
+        out = torch.full((B, hq, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((B, hq), float("nan"), device=DEV)
+        ws = torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, chunk), 256),
+                         dtype=torch.uint8, device=DEV)
+        s = torch.cuda.Stream()
+
+        def mixed():
+            pkv.pkv_prefill_attention_ragged(pdesc, pq, pqo, pk, pv, ptab, pkvl, spec.sm_scale, p_out, p_lse,
+                                             qo_indptr_host=pb.qo_indptr_host, kv_lens_host=pb.kv_lens_host,
+                                             stream=s)
+            pkv.pkv_decode_step(desc, q, kn, vn, kd, vd, tabs, lens, max_ctx, 1 / math.sqrt(d), out, lse, ws,
+                                cos_sin=cs, chunk_blocks=chunk, stream=s)
+
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                mixed()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(2):
+                mixed()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_errors() == 0
+        assert np.array_equal(pool_np(kd), kc) and np.array_equal(pool_np(vd), vc)
+        assert_close(out, ref, "independent decode step chunk %d" % chunk)
+        assert_lse_close(lse, ref_lse, "independent decode step lse")
+        assert_close(p_out, p_ref, "prefill before an independent decode step")
+        assert_lse_close(p_lse, p_ref_lse, "prefill lse")
+        assert int(ws[:4 * B * hkv].view(torch.int32).abs().sum().item()) == 0, "tickets not reset"
+
+
 def test_bound_decode_step_equals_the_unbound_call():
     """bind_decode_step marshals the arguments once; refilling the bound q
     and calling again gives the bits of a fresh unbound call."""
