@@ -2,7 +2,8 @@
 steps captured in a CUDA graph and replayed, decode steps whose descriptor
 carries PKV_DESC_PREFETCH_KV, the Llama-3-8B-shaped mixed step as the ragged
 prefill followed by a decode that does not wait for it (PKV_DESC_INDEPENDENT),
-and the Qwen2.5-3B-shaped step rotating over four batches of one pool.
+the Qwen2.5-3B-shaped step rotating over four batches of one pool, and the
+FP8 step's full-attention and window layers.
 
 After the replays, sampled sequences are checked against the oracle: their
 appended cache rows byte for byte, and the attention outputs (decode and
@@ -43,8 +44,7 @@ def _sample(lens, rng, extra=2):
                       rng.choice(len(lens), size=extra, replace=False).tolist()))
 
 
-def _check_decode(W, inst, seqs, before, label, check_out=True):
-    b = W.insts[inst]
+def _check_decode(W, b, seqs, before, label, check_out=True, window=-1):
     spec = W.spec
     k0, v0, tabs = before
     lens = b.lens_host[seqs]
@@ -66,7 +66,7 @@ def _check_decode(W, inst, seqs, before, label, check_out=True):
     ref, ref_lse = oracle.paged_attention(q=q_rot, k_cache=k0, v_cache=v0, block_tables=tabs,
                                           qo_indptr=np.arange(len(seqs) + 1), kv_lens=lens,
                                           num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
-                                          sm_scale=spec.sm_scale, kv_dtype=1 if fp8 else 0,
+                                          sm_scale=spec.sm_scale, window=window, kv_dtype=1 if fp8 else 0,
                                           k_scale=ks, v_scale=vs, nthreads=NTHREADS)
     idx = torch.tensor(seqs, device=DEV)
     assert_close(W.out[idx], ref, label)
@@ -84,7 +84,7 @@ def test_mixed_step_as_benchmarked():
     before = compact_pool(b.k_cache, b.v_cache, b.tables_host, seqs)
     _run(W, [0, 0])
     assert W.pkv.pkv_device_errors(reset=True) == 0
-    _check_decode(W, 0, seqs, before, "mixed-step decode as benchmarked")
+    _check_decode(W, W.insts[0], seqs, before, "mixed-step decode as benchmarked")
 
     # the prefill half: every row of the sequence with the shortest prefix,
     # the last 16 query tokens of the one with the longest
@@ -120,4 +120,24 @@ def test_rotating_decode_step_as_benchmarked():
     last = order[-1]
     for i in order:
         # the shared output buffer holds the last batch's result
-        _check_decode(W, i, samples[i], befores[i], "rotating step, batch %d" % i, check_out=i == last)
+        _check_decode(W, W.insts[i], samples[i], befores[i], "rotating step, batch %d" % i,
+                      check_out=i == last)
+
+
+def test_fp8_two_layer_step_as_benchmarked():
+    """FP8 e4m3 step: a full-attention layer, then the window-128 layer (its
+    own pools and scales), each launch's predecessor the other layer's,
+    with PKV_DESC_PREFETCH_KV.  Both layers' appended rows are checked; the
+    shared output buffer holds the window layer's result."""
+    W = bench.DecodeWorkload(5, DEV, 0)
+    assert W.prefetch and len(W.layers) == 2
+    rng = np.random.default_rng(43)
+    b0 = W.layers[0][0]
+    seqs = _sample(b0.lens_host, rng)
+    befores = [compact_pool(layer[0].k_cache, layer[0].v_cache, layer[0].tables_host, seqs)
+               for layer in W.layers]
+    _run(W, [0, 0])
+    assert W.pkv.pkv_device_errors(reset=True) == 0
+    for li, (layer, w) in enumerate(zip(W.layers, W.windows)):
+        _check_decode(W, layer[0], seqs, befores[li], "FP8 step, layer %d (window %d)" % (li, w),
+                      check_out=li == len(W.layers) - 1, window=w)
