@@ -195,7 +195,7 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc *desc, void *k_cache, void *v_ca
  *              ring) when desc->ring_blocks > 0.
  *   sinks    : fp32 [Hq] sink logits in the units of sm_scale * q.k, or NULL.
  *   chunk_blocks : blocks per chunk; 0 lets the planner choose
- *              (pkv_decode_plan), else 1..128.
+ *              (pkv_decode_plan), else 1..256 (1..128 for e4m3 pools).
  *   workspace: >= pkv_decode_workspace_size(...) bytes, 256-byte aligned,
  *              zero-filled before its first use; every call leaves it
  *              zeroed again.  Calls that share a workspace must not overlap

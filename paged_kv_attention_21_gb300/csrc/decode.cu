@@ -61,6 +61,11 @@ struct DecodeCfg {
     // The 2-warp variant runs windows of at most 9 blocks: with e4m3 tiles a
     // warp's whole share (5 blocks) is in flight after one round of loads.
     static constexpr int kStages = kFp8 ? (kW < kWarps ? 5 : 3) : 2;
+    // block-id registers per lane: a warp holds ids for 32 kIdRegs blocks, so
+    // a CTA takes chunks of up to 32 kIdRegs kW blocks: 256 with 4 warps on
+    // bf16 pools, 128 on e4m3 pools (whose issue-bound loop measured 0.7 %
+    // slower with the second register's select)
+    static constexpr int kIdRegs = (kW < kWarps || kFp8) ? 1 : 2;
     static constexpr int kElem = kFp8 ? 1 : 2;
     static constexpr int kTileBytes = kBlockSize * D * kElem;  // one block of one head
     static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
@@ -523,10 +528,17 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         row = g_lo;
     }
     const int32_t* bt = a.block_tables + static_cast<size_t>(row) * a.mbps;
-    int phys = 0;
+    // Block ids of this warp's blocks: the k-th one in register k / 32 of
+    // lane k % 32 (kIdRegs registers: up to 32 kIdRegs blocks per warp).
+    int phys[C::kIdRegs];
+#pragma unroll
+    for (int r = 0; r < C::kIdRegs; ++r) phys[r] = 0;
     if (a.window <= 0) {
-        const int lb = split * a.chunk_blocks + warp + lane * kW;
-        if (lane * kW < a.chunk_blocks && lb < a.mbps) phys = bt[lb];
+#pragma unroll
+        for (int r = 0; r < C::kIdRegs; ++r) {
+            const int lb = split * a.chunk_blocks + warp + (32 * r + lane) * kW;
+            if ((32 * r + lane) * kW < a.chunk_blocks && lb < a.mbps) phys[r] = bt[lb];
+        }
     }
     // A ring table of at most 32 entries holds every block a window can
     // touch: read all of it (lane k: entry k) while the length is in flight.
@@ -590,22 +602,35 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     fence_barrier_init();
     __syncthreads();
 
-    // Physical block ids of this warp's blocks: lane k holds the k-th one.
-    bool bad_id = false;
-    if (ring_lanes) {
-        const int lb = b0 + warp + lane * kW;
-        const int v = __shfl_sync(0xFFFFFFFFu, ring_id, lane < my_n ? lb % a.ring : 0);
-        if (lane < my_n) phys = v;
-    }
-    if (lane < my_n) {
-        const int lb = b0 + warp + lane * kW;  // logical block
-        if (a.window > 0 && !ring_lanes) phys = bt[a.ring > 0 ? lb % a.ring : lb];
-        if (phys < 0 || phys >= a.num_blocks) {
-            if (!early) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-            phys = 0;  // read a valid block; the output is flagged invalid
-            bad_id = true;
+    // Physical block ids of this warp's blocks, checked: bit r of bad_ids
+    // marks a bad id in register r (it reads block 0; the output is flagged).
+    uint32_t bad_ids = 0;
+#pragma unroll
+    for (int r = 0; r < C::kIdRegs; ++r) {
+        const int kb = 32 * r + lane;          // this lane's block in register r
+        const int lb = b0 + warp + kb * kW;    // its logical block
+        if (ring_lanes) {
+            const int v = __shfl_sync(0xFFFFFFFFu, ring_id, kb < my_n ? lb % a.ring : 0);
+            if (kb < my_n) phys[r] = v;
+        }
+        if (kb < my_n) {
+            if (a.window > 0 && !ring_lanes) phys[r] = bt[a.ring > 0 ? lb % a.ring : lb];
+            if (phys[r] < 0 || phys[r] >= a.num_blocks) {
+                if (!early) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                phys[r] = 0;
+                bad_ids |= 1u << r;
+            }
         }
     }
+    // the id of this warp's k-th block, read from its lane (every lane takes
+    // part; k is the same in every lane, so all pick the same register)
+    auto block_id = [&](int k) {
+        int src = phys[0];
+#pragma unroll
+        for (int r = 1; r < C::kIdRegs; ++r)
+            if ((k >> 5) == r) src = phys[r];
+        return __shfl_sync(0xFFFFFFFFu, src, k & 31);
+    };
     uint8_t* wbase = smem + warp * C::kWarpBytes;
 
     // Fused append: the warp that loads the sequence's last block writes the
@@ -615,14 +640,14 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const bool appender = a.k_new != nullptr && !clamped && split == nsplit - 1 &&
                           warp == (last_blk - b0) % kW;
     auto append = [&]() {
-        const int pb = __shfl_sync(0xFFFFFFFFu, phys, k_last & 31);
-        const bool bad = __shfl_sync(0xFFFFFFFFu, bad_id, k_last & 31);
+        const int pb = block_id(k_last);
+        const bool bad = (__shfl_sync(0xFFFFFFFFu, bad_ids, k_last & 31) >> (k_last >> 5)) & 1u;
         if (!bad) append_new_token<D, kFp8>(a, seq, kvh, pb, ctx - 1, lane);
     };
     // Lane 0 issues the prologue; the shuffle reads lane k's id from lane 0's
     // point of view, so every lane takes part in it.
     auto load_stage = [&](int k) {
-        const int pb = __shfl_sync(0xFFFFFFFFu, phys, k & 31);
+        const int pb = block_id(k);
         if (lane == 0 && k < my_n) {
             uint8_t* kdst = wbase + k * C::kStageBytes;
             uint8_t* vdst = kdst + C::kTileBytes;
@@ -643,7 +668,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
             if (!(append_first && k == k_last)) load_stage(k);
         pdl_wait();
         flag_length();
-        if (__any_sync(0xFFFFFFFFu, bad_id)) {
+        if (__any_sync(0xFFFFFFFFu, bad_ids != 0)) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
         }
         if (append_first) {
@@ -724,7 +749,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
             // before the __syncwarp: no proxy fence is needed before the copy
             // overwrites it (measured 2 % faster on the e4m3 decode without it)
             const int kn = k + C::kStages;
-            const int pb = __shfl_sync(0xFFFFFFFFu, phys, kn & 31);
+            const int pb = block_id(kn);
             if (lane == 0 && kn < my_n) {
                 uint8_t* kdst = wbase + st * C::kStageBytes;
                 uint8_t* vdst = kdst + C::kTileBytes;
@@ -1036,7 +1061,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
                             cudaStream_t stream) {
     // A windowed plan of one chunk per sequence has a few blocks per CTA:
     // 2-warp CTAs, more of them resident, keep such a layer to one wave.
-    // (Each lane holds one block id of its warp: at most 32 blocks per warp.)
+    // (Each lane of a 2-warp CTA holds one block id of its warp: at most 32
+    // blocks per warp.)
     if (a.window > 0 && a.max_splits == 1 && a.chunk_blocks <= 2 * 32)
         return launch_decode_v<D, kFp8, false, 2>(a, kmap, vmap, stream);
     if (a.max_splits >= 2 && a.max_splits <= kMaxClusterSplits)

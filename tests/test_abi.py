@@ -201,7 +201,7 @@ def test_planner_fills_the_gpu_and_respects_limits(lib):
                              max_blocks_per_seq=(ctx + 15) // 16, kv_dtype=dt)
         chunk, splits = pkv.pkv_decode_plan(desc, B, ctx, win, sms)
         vis_blocks = (ctx + 15) // 16 if win <= 0 else min((ctx + 15) // 16, (win + 14) // 16 + 1)
-        assert 1 <= chunk <= 128
+        assert 1 <= chunk <= 256
         assert splits == math.ceil(vis_blocks / chunk) and splits <= 512
         if B * hkv * vis_blocks >= 16 * sms * 8:
             # large batches: enough CTAs for several waves, none smaller than 16 blocks
@@ -220,7 +220,12 @@ def test_workspace_size_layout(lib):
     pairs, G, D, S = B * 2, 8, 128, 4
     a256 = lambda x: (x + 255) // 256 * 256
     assert sz == a256(pairs * 4) + a256(pairs * S * G * 4) + a256(pairs * S * G * D * 4)
-    assert pkv.pkv_decode_workspace_size(d, B, ctx, -1, 129) == 0  # chunk > 128 rejected
+    assert pkv.pkv_decode_workspace_size(d, B, ctx, -1, 257) == 0  # chunk > 256 rejected
+    # 250 blocks: chunks of 200 (bf16) or 128 (e4m3) give two; an e4m3 chunk above 128 is refused
+    assert pkv.pkv_decode_workspace_size(d, 4, 4000, -1, 200) > 0
+    d8 = _desc(num_q_heads=64, num_kv_heads=8, head_dim=64, kv_dtype=pkv.KV_FP8_E4M3)
+    assert pkv.pkv_decode_workspace_size(d8, 4, 4000, -1, 128) > 0
+    assert pkv.pkv_decode_workspace_size(d8, 4, 4000, -1, 129) == 0
 
 
 def test_wait_timeout_hook_validates_its_arguments(lib):
