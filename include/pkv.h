@@ -108,7 +108,12 @@ typedef struct {
  *   sequences' blocks, different outputs).  The decode kernel then runs
  *   without waiting for that kernel (its CTAs take the SMs the prefill's last
  *   CTAs leave idle) and waits for it only at its end, so kernels launched
- *   after the call still see both.  Implies PKV_DESC_PREFETCH_KV. */
+ *   after the call still see both.  Implies PKV_DESC_PREFETCH_KV.
+ * Both promises are about the kernel just before the call.  Kernels launched
+ * earlier are complete by the time the call starts as long as that kernel
+ * lets its dependents start only once its own predecessor has completed, as
+ * every kernel of this library does (and as any kernel launched without
+ * programmatic stream serialization does by construction). */
 #define PKV_DESC_INDEPENDENT 0x2u
 
 /* Bytes of one pool (K or V): num_blocks * Hkv * block_size * head_dim * elem.

@@ -501,7 +501,13 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const bool early = a.early_kv != 0 && a.defer_wait == 0;
     WaitAtExit wait_at_exit{(a.defer_wait != 0 && is_first_cta()) || early};
     if (!a.defer_wait && !early) pdl_wait();
-    pdl_launch_dependents();
+    // The next kernel may start once every CTA has triggered or exited, and
+    // some CTA triggers only after its grid-dependency wait -- every CTA here,
+    // the early-mode CTAs after their wait below (those without a chunk by
+    // exiting; chunk 0 of each pair waits), CTA (0, 0, 0) of a deferred launch
+    // by exiting after its wait at exit -- so the next kernel starts only once
+    // this launch's predecessor has completed.
+    if (!early && !(a.defer_wait != 0 && is_first_cta())) pdl_launch_dependents();
     const int split = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
@@ -667,6 +673,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         for (int k = 0; k < C::kStages; ++k)
             if (!(append_first && k == k_last)) load_stage(k);
         pdl_wait();
+        pdl_launch_dependents();
         flag_length();
         if (__any_sync(0xFFFFFFFFu, bad_ids != 0)) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
