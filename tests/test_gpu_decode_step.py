@@ -249,6 +249,64 @@ def test_prefetch_kv_steps_back_to_back_match_oracle(hq, hkv, d, fp8):
             assert int(r["ws"][:4 * B * hkv].view(torch.int32).abs().sum().item()) == 0, "tickets not reset"
 
 
+def test_prefetch_kv_alternating_batches_growing_steps():
+    """Two batches alternate on one stream for four steps each, with
+    PKV_DESC_PREFETCH_KV and growing lengths: step t of a batch appends at
+    position len + t - 1 and reads the row its own step t - 1 appended, two
+    launches earlier (the other batch's step in between, as the promise
+    allows).  Every step's output equals the oracle's step-by-step append and
+    attention."""
+    hq, hkv, d = 16, 2, 128
+    steps = 4
+    runs = []
+    for i in range(2):
+        rng = np.random.default_rng(240 + i)
+        lens = np.array([4, 17, 33, 130, 700, 2050], dtype=np.int32)
+        case = PagedCase(rng, lens, hq, hkv, d)
+        B = len(lens)
+        k_new = [bf16_bits(rng.standard_normal((B, hkv, d)).astype(np.float32)) for _ in range(steps)]
+        v_new = [bf16_bits(rng.standard_normal((B, hkv, d)).astype(np.float32)) for _ in range(steps)]
+        qs = [bf16_bits(rng.standard_normal((B, hq, d)).astype(np.float32)) for _ in range(steps)]
+        table = oracle.rope_table(1e6, d, int(lens.max()))
+        # the oracle, step by step on one host copy of the cache
+        kc, vc = case.k_cache.copy(), case.v_cache.copy()
+        refs = []
+        for t in range(steps):
+            lt = (lens - steps + 1 + t).astype(np.int32)
+            q_rot = oracle.append_rope(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=BS, kv_dtype=0,
+                                       k_cache=kc, v_cache=vc, block_tables=case.tables,
+                                       token_to_seq=np.arange(B, dtype=np.int32), positions=lt - 1,
+                                       k_new=k_new[t], v_new=v_new[t], q=qs[t], cos_sin=table)
+            refs.append(oracle.paged_attention(q=q_rot, k_cache=kc, v_cache=vc, block_tables=case.tables,
+                                               qo_indptr=np.arange(B + 1), kv_lens=lt, num_q_heads=hq,
+                                               num_kv_heads=hkv, sm_scale=1 / math.sqrt(d), nthreads=NTHREADS))
+        desc = pkv.make_desc(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=case.k_cache.shape[0],
+                             max_blocks_per_seq=case.tables.shape[1], flags=pkv.DESC_PREFETCH_KV)
+        max_ctx = int(lens.max())
+        runs.append(dict(
+            desc=desc, max_ctx=max_ctx, refs=refs, kd=_pool(case.k_cache), vd=_pool(case.v_cache),
+            q=[_pool(x) for x in qs], kn=[_pool(x) for x in k_new], vn=[_pool(x) for x in v_new],
+            lens=[_dev((lens - steps + 1 + t).astype(np.int32)) for t in range(steps)], tabs=_dev(case.tables),
+            cs=_dev(table), out=[torch.empty((B, hq, d), dtype=torch.bfloat16, device=DEV) for _ in range(steps)],
+            lse=[torch.empty((B, hq), device=DEV) for _ in range(steps)],
+            ws=torch.zeros(max(pkv.pkv_decode_workspace_size(desc, B, max_ctx, -1, 2), 256), dtype=torch.uint8,
+                           device=DEV)))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for t in range(steps):
+            for r in runs:
+                pkv.pkv_decode_step(r["desc"], r["q"][t], r["kn"][t], r["vn"][t], r["kd"], r["vd"], r["tabs"],
+                                    r["lens"][t], r["max_ctx"], 1 / math.sqrt(d), r["out"][t], r["lse"][t], r["ws"],
+                                    cos_sin=r["cs"], chunk_blocks=2, stream=s)
+    s.synchronize()
+    assert pkv.pkv_device_errors() == 0
+    for i, r in enumerate(runs):
+        for t in range(steps):
+            ref, ref_lse = r["refs"][t]
+            assert_close(r["out"][t], ref, "alternating batch %d, step %d" % (i, t))
+            assert_lse_close(r["lse"][t], ref_lse, "alternating batch %d, step %d" % (i, t))
+
+
 def test_independent_decode_step_after_prefill_matches_oracle():
     """PKV_DESC_INDEPENDENT, one layer's mixed step: a ragged causal prefill
     (its own pools) and then the decode step of other sequences, which does
