@@ -69,11 +69,11 @@ def _oracle_step(case, k_new, v_new, table, tables, k_cache, v_cache, window, ri
 
 
 def _gpu(case, k_new, v_new, table, tables, k_cache, v_cache, window, chunk, fused, ring=0,
-         sinks=None):
+         sinks=None, flags=0):
     B = len(case.lens)
     desc = pkv.make_desc(num_q_heads=case.hq, num_kv_heads=case.hkv, head_dim=case.d,
                          num_blocks=k_cache.shape[0], max_blocks_per_seq=tables.shape[1],
-                         kv_dtype=1 if case.fp8 else 0, ring_blocks=ring)
+                         kv_dtype=1 if case.fp8 else 0, ring_blocks=ring, flags=flags)
     max_ctx = int(case.lens.max())
     kd, vd = _pool(k_cache), _pool(v_cache)
     q = _pool(case.q)
@@ -127,9 +127,11 @@ def test_decode_step_matches_oracle_and_two_launch_path(hq, hkv, d, fp8, rope):
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-def test_decode_step_window_sinks_ring(fp8):
+@pytest.mark.parametrize("flags", [0, pkv.DESC_PREFETCH_KV])
+def test_decode_step_window_sinks_ring(fp8, flags):
     """Sliding window 128 over a 9-block ring, with sink logits: the step
-    writes into ring entry ((len - 1) / 16) mod 9."""
+    writes into ring entry ((len - 1) / 16) mod 9.  With PKV_DESC_PREFETCH_KV
+    the ring entries and the first blocks are read before the wait."""
     hq, hkv, d = (64, 8, 64) if fp8 else (32, 8, 128)
     case, k_new, v_new, table = _setup(90 + fp8, [1, 16, 17, 128, 129, 145, 1000, 3001], hq, hkv, d,
                                        fp8, True)
@@ -148,7 +150,7 @@ def test_decode_step_window_sinks_ring(fp8):
                                         sinks=sinks)
     for chunk in (0, 2):
         out, lse, kd, vd = _gpu(case, k_new, v_new, table, rtabs, rk, rv, 128, chunk, fused=True,
-                                ring=ring, sinks=sinks)
+                                ring=ring, sinks=sinks, flags=flags)
         assert np.array_equal(pool_np(kd), kc) and np.array_equal(pool_np(vd), vc)
         assert_close(out, ref, "ring step chunk %d" % chunk)
         assert_lse_close(lse, ref_lse, "ring step lse")
