@@ -210,6 +210,15 @@ def test_planner_fills_the_gpu_and_respects_limits(lib):
     desc = pkv.make_desc(num_q_heads=64, num_kv_heads=8, head_dim=64, num_blocks=10,
                          max_blocks_per_seq=1024, kv_dtype=1)
     assert pkv.pkv_decode_plan(desc, 128, 16384, 128, sms) == (9, 1)
+    # chunks above 128 blocks only while the batch spans >= 8 waves with them: the
+    # Llama-3-8B-shaped decode (120 x 8 pairs, up to 2048 blocks) takes 256-block
+    # chunks; the FP8 layer (e4m3, one block id per lane) stays at 128
+    d8b = pkv.make_desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_blocks=10, max_blocks_per_seq=2048)
+    assert pkv.pkv_decode_plan(d8b, 120, 32768, -1, sms) == (256, 8)
+    assert pkv.pkv_decode_plan(desc, 128, 16384, -1, sms) == (128, 8)
+    # a small bf16 batch of the same length spans few waves: 128 at most
+    chunk, _ = pkv.pkv_decode_plan(d8b, 8, 32768, -1, sms)
+    assert chunk <= 128
 
 
 def test_workspace_size_layout(lib):
