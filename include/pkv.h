@@ -200,7 +200,10 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc *desc, void *k_cache, void *v_ca
  *              ring) when desc->ring_blocks > 0.
  *   sinks    : fp32 [Hq] sink logits in the units of sm_scale * q.k, or NULL.
  *   chunk_blocks : blocks per chunk; 0 lets the planner choose
- *              (pkv_decode_plan), else 1..256 (1..128 for e4m3 pools).
+ *              (pkv_decode_plan), else 1..256 (1..128 for e4m3 pools).  A
+ *              context is cut into at most 512 chunks, so the visible keys of
+ *              one sequence are limited to 512 x 256 x 16 (bf16) or
+ *              512 x 128 x 16 (e4m3) tokens: PKV_ERR_UNSUPPORTED beyond.
  *   workspace: >= pkv_decode_workspace_size(...) bytes, 256-byte aligned,
  *              zero-filled before its first use; every call leaves it
  *              zeroed again.  Calls that share a workspace must not overlap

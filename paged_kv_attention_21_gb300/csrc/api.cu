@@ -318,6 +318,9 @@ pkv_status plan_decode(const pkv_cache_desc* desc, int num_seqs, int max_ctx, in
         if (s > kClusterSplits && s <= 2 * kClusterSplits && (mb + kClusterSplits - 1) / kClusterSplits <= cap)
             chunk = (mb + kClusterSplits - 1) / kClusterSplits;
     }
+    if (chunk > max_chunk)  // more than kMaxSplits chunks of the longest a CTA takes
+        return fail(PKV_ERR_UNSUPPORTED, "context of %d blocks needs more than %d chunks of %d blocks", mb,
+                    kMaxSplits, max_chunk);
     const int splits = (mb + chunk - 1) / chunk;
     if (splits > kMaxSplits)
         return fail(PKV_ERR_UNSUPPORTED, "context needs %d splits of %d blocks (max %d)", splits, chunk,

@@ -219,6 +219,13 @@ def test_planner_fills_the_gpu_and_respects_limits(lib):
     # a small bf16 batch of the same length spans few waves: 128 at most
     chunk, _ = pkv.pkv_decode_plan(d8b, 8, 32768, -1, sms)
     assert chunk <= 128
+    # contexts past 512 chunks of the longest a CTA takes (256 blocks bf16, 128 e4m3) are refused
+    for dt, limit in ((0, 512 * 256), (1, 512 * 128)):
+        dl = pkv.make_desc(num_q_heads=16, num_kv_heads=2, head_dim=128, num_blocks=10,
+                           max_blocks_per_seq=limit + 1, kv_dtype=dt)
+        assert pkv.pkv_decode_plan(dl, 1, limit * 16, -1, sms)[1] == 512
+        with pytest.raises(pkv.PkvError):
+            pkv.pkv_decode_plan(dl, 1, limit * 16 + 1, -1, sms)
 
 
 def test_workspace_size_layout(lib):
