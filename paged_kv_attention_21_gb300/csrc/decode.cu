@@ -603,7 +603,14 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     }
     const int b0 = first_blk + split * a.chunk_blocks;
     const int b1 = min(last_blk + 1, b0 + a.chunk_blocks);
-    const int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kW - 1) / kW : 0;
+    int my_n = (b1 - b0 > warp) ? (b1 - b0 - warp + kW - 1) / kW : 0;
+    // a chunk longer than the warp's id registers hold (the host plans none):
+    // flagged, and only the blocks whose ids it holds are read
+    const bool too_long = my_n > 32 * C::kIdRegs;
+    if (too_long) {
+        if (!early && lane == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+        my_n = 32 * C::kIdRegs;
+    }
 
     fence_barrier_init();
     __syncthreads();
@@ -644,7 +651,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     // of the first NSTAGE, else right after (the refill that loads it comes later).
     const int k_last = (last_blk - b0) / kW;
     const bool appender = a.k_new != nullptr && !clamped && split == nsplit - 1 &&
-                          warp == (last_blk - b0) % kW;
+                          warp == (last_blk - b0) % kW && k_last < my_n;
     auto append = [&]() {
         const int pb = block_id(k_last);
         const bool bad = (__shfl_sync(0xFFFFFFFFu, bad_ids, k_last & 31) >> (k_last >> 5)) & 1u;
@@ -675,6 +682,7 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
         pdl_wait();
         pdl_launch_dependents();
         flag_length();
+        if (too_long && lane == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
         if (__any_sync(0xFFFFFFFFu, bad_ids != 0)) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
         }
