@@ -516,8 +516,8 @@ __global__ void __launch_bounds__(kW * 32) decode_kernel(const DecodeArgs a,
     const int G = a.group;
 
     // Without a window a chunk's blocks do not depend on the context length:
-    // read this warp's block ids (lane k: the k-th one) while the length is
-    // still in flight.  Entries past the sequence's end are read but unused.
+    // read this warp's block ids (below) while the length is still in
+    // flight.  Entries past the sequence's end are read but unused.
     // Windowed cascade prefix pass: sequence seq reads the shared prefix of
     // its group (table row and length of the group; its own query position
     // is prefix + suffix_len - 1, so its window starts there).
